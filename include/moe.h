@@ -1,0 +1,197 @@
+/*
+ * moe.h -- C ABI of the GB300 (sm_103a) mixture-of-experts FFN layer library (libmoe_gb300.so).
+ *
+ * The layer is the Kimi K2 / DeepSeek-V3 MoE feed-forward block and the Kimi K3 latent variant:
+ *
+ *   z = x W_r ; s = sigma(z) ; selected = top_k(s + b) ; G_i = gate_scale * s_i / sum_sel s_j
+ *   E_i(x) = (SiLU(x W1_i) * (x W3_i)) W2_i ;  y = sum_sel G_i E_i(x) + E_shared(x)
+ *
+ * Sources (page title and section):
+ *   [K2-MoE]   "Kimi K2 · Transformer blocks > MoE transformer block", "Mixture of experts" steps.
+ *   [K2-PARAM] same page, "Parameters" table (exact per-instance accounting).
+ *   [NN-MOE]   nnterp encyclopedia "kimi_k2", note "The mixture of experts" (bias selects only;
+ *              gates are renormalised unbiased sigmoids times 2.827; routed + shared = output).
+ *   [NN-API]   nnterp "kimi_k2", "02 · support()" (router_logits, expert_weights, expert_indices,
+ *              routed_output, shared_expert_output and their layouts).
+ *   [NN-CFG]   nnterp "kimi_k2", "Config" table (hidden 7168, 384 experts, top 8, moe intermediate
+ *              2048, 1 shared expert, routed_scaling_factor 2.827, n_group 1, rms_norm_eps 1e-6).
+ *   [K3-UP]    "Kimi K3 · Latent up-projection": equation y_routed = u_hat W_up, parameter table,
+ *              and the `__init__`, `forward` and `moe_infer` code excerpts (dispatch by expert,
+ *              per-expert MLP, un-permute, gate-weighted sum; latent down/up projections, RMSNorm).
+ *
+ * Conventions for every entry point
+ *   - Pointers named x, W*, b, out, logits, topk_*, counts, offsets, perm_*, y_perm and ws are
+ *     DEVICE pointers on the current CUDA device; the library never allocates, frees or copies to
+ *     the host on these paths.  The caller owns every buffer, the workspace included.
+ *   - All work is enqueued on `stream` (a cudaStream_t; NULL = the legacy default stream).  Calls
+ *     return once the work is enqueued: execution errors surface at the caller's next
+ *     synchronisation, and device-side checks (index range, bounded waits) raise flags in the first
+ *     word of the workspace, read with moe_device_status().
+ *   - Layouts are row-major.  Weights are stored [out][in] as on the pages ("The reference module
+ *     holds the weight output by input"), i.e. K-contiguous.
+ *   - Every pointer must be 16-byte aligned; every row pitch is the row's width (no padding).
+ *   - Errors are return codes; nothing is launched when host validation fails.
+ *   - The functions hold no state between calls other than cached kernel attributes and the
+ *     driver entry point of cuTensorMapEncodeTiled; they are safe to call from several threads on
+ *     distinct workspaces.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,  /* null / misaligned pointer, inconsistent shape                     */
+  MOE_ERR_UNSUPPORTED = 2,  /* a shape or dtype combination this build does not implement        */
+  MOE_ERR_WORKSPACE = 3,    /* ws is null or smaller than moe_workspace_size()                   */
+  MOE_ERR_CUDA = 4,         /* a CUDA runtime / driver call failed at launch time                */
+  MOE_ERR_DEVICE_CHECK = 5, /* a kernel found an out-of-range expert index or row                */
+  MOE_ERR_TIMEOUT = 6       /* a kernel gave up a bounded wait (pipeline stalled) and returned   */
+} moe_status_t;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2 } moe_dtype_t;
+
+/* moe_config_t.flags */
+#define MOE_FLAG_GEMM_ROWS_MAJOR 0x1u /* force the token-rows-as-M tensor-core GEMM tiles       */
+#define MOE_FLAG_GEMM_SWAP_AB 0x2u    /* force the weight-rows-as-M (swap-AB) GEMM tiles         */
+#define MOE_FLAG_ROUTER_SIMT 0x4u     /* force the CUDA-core fp32 router GEMM                    */
+#define MOE_FLAG_ROUTER_TC 0x8u       /* force the tensor-core (3 x bf16 split) router GEMM      */
+
+/* Layer shapes and constants.  Names follow [NN-CFG]. */
+typedef struct {
+  int64_t T;           /* tokens (batch x positions), >= 0                                       */
+  int32_t d;           /* hidden size (7168)                                                     */
+  int32_t E;           /* routed experts (384)                                                   */
+  int32_t k;           /* experts per token (8), 1 <= k <= E, k <= 32                            */
+  int32_t I;           /* routed expert intermediate size (2048)                                 */
+  int32_t I_shared;    /* shared expert intermediate size (2048 = I x n_shared_experts)          */
+  int32_t n_shared;    /* 0 or 1 shared expert                                                   */
+  int32_t d_latent;    /* 0: K2 path; L > 0: K3 latent width (3584) [K3-UP]                      */
+  int32_t latent_norm; /* 1: RMSNorm with unit weight on the latent gate-weighted sum [K3-UP]    */
+  int32_t act_dtype;   /* MOE_F32 or MOE_BF16: x, out, W_down, W_up, intermediates               */
+  int32_t w_dtype;     /* expert weights: equal to act_dtype, or MOE_FP8_E4M3 (with block scales) */
+  int32_t quant_block; /* fp8 block edge (128): weight scales per 128x128, activations per 1x128  */
+  uint32_t flags;      /* MOE_FLAG_* tuning overrides; 0 = automatic choice                      */
+  float gate_scale;    /* routed_scaling_factor (2.827) [NN-CFG]                                 */
+  float rms_eps;       /* rms_norm_eps (1e-6) [NN-CFG]                                           */
+  int32_t reserved_;   /* must be 0                                                              */
+} moe_config_t;
+
+/* Bytes of device workspace every entry point below needs for this configuration.  The first
+ * 256 bytes hold the device status word (see moe_device_status).  Returns 0 for an invalid
+ * configuration. */
+size_t moe_workspace_size(const moe_config_t* cfg);
+
+/* Router, selection and gates [K2-MoE] steps z, s, E_sel, G; [NN-MOE]; [NN-API] router_logits,
+ * expert_indices, expert_weights.
+ *   x            [T][d]  act_dtype
+ *   W_r          [E][d]  fp32 (one logit per expert)
+ *   b            [E]     fp32 selection bias (used for the selection only)
+ *   logits       [T][E]  fp32 out, z = x W_r^T, or NULL
+ *   topk_idx     [T][k]  int32 out: the k experts with the largest s + b, slot order by s + b
+ *                        descending, equal keys ordered by the lower expert index
+ *   topk_weight  [T][k]  fp32 out: gate_scale * s_i / sum of the selected s (unbiased sigmoids);
+ *                        sums to gate_scale per token
+ * s = 1/(1+exp(-z)) and s + b are evaluated in fp32. */
+moe_status_t moe_router(const moe_config_t* cfg, const void* x, const float* W_r, const float* b,
+                        float* logits, int32_t* topk_idx, float* topk_weight, void* ws,
+                        size_t ws_bytes, void* stream);
+
+/* Dispatch bookkeeping: the `moe_infer` front half of [K3-UP] (per-expert token counts and the
+ * expert-major order of the (token, slot) pairs), without the host synchronisation.
+ *   topk_idx  [T][k]   int32 in; pair p = t*k + j
+ *   counts    [E+1]    int32 out: rows of each routed expert; counts[E] = T*n_shared (the shared
+ *                      expert's rows, every token)
+ *   offsets   [E+2]    int32 out: exclusive prefix sum of counts (offsets[E] = T*k,
+ *                      offsets[E+1] = T*k + T*n_shared)
+ *   perm_src  [T*k]    int32 out: permuted row r holds pair perm_src[r]; rows of one expert are
+ *                      contiguous and in increasing pair order (a stable sort by expert)
+ *   perm_dst  [T*k]    int32 out: inverse permutation, perm_src[perm_dst[p]] == p
+ * An index outside [0, E) raises MOE_ERR_DEVICE_CHECK in the device status and is not counted. */
+moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, int32_t* counts,
+                         int32_t* offsets, int32_t* perm_src, int32_t* perm_dst, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* Expert MLPs [K2-MoE] steps g, u, a, h, E_i and y_shared; the per-expert loop of `moe_infer`
+ * [K3-UP] as grouped GEMMs over the permuted rows; on the K3 path the down-projection
+ * x_lat = x W_down^T first [K3-UP].
+ *   x         [T][d]               act_dtype
+ *   offsets   [E+2], perm_src [T*k] from moe_permute
+ *   W13       [E][2I][d_e]         rows 0..I-1 = W1 (gate_proj), rows I..2I-1 = W3 (up_proj);
+ *                                  d_e = d (K2) or d_latent (K3); w_dtype
+ *   W2        [E][d_e][I]          down_proj; w_dtype
+ *   W13_scale [E][2I/qb][d_e/qb], W2_scale [E][d_e/qb][I/qb]   fp32 block scales, fp8 only
+ *   Ws13      [2 I_shared][d], Ws2 [d][I_shared] (+ Ws13_scale, Ws2_scale for fp8); NULL when
+ *             n_shared == 0
+ *   W_down    [d_latent][d] act_dtype, K3 only (else NULL)
+ *   y_perm    out, act_dtype: [T*k][d_e] un-weighted expert outputs in permuted row order,
+ *             followed by [T*n_shared][d] shared-expert outputs in token order.
+ * fp8 (w_dtype MOE_FP8_E4M3): the activations entering both GEMMs are quantised per token per
+ * quant_block channels to e4m3 with scale = amax/448 (1 for an all-zero group), accumulation in
+ * fp32. */
+moe_status_t moe_experts(const moe_config_t* cfg, const void* x, const int32_t* offsets,
+                         const int32_t* perm_src, const void* W13, const void* W2,
+                         const float* W13_scale, const float* W2_scale, const void* Ws13,
+                         const void* Ws2, const float* Ws13_scale, const float* Ws2_scale,
+                         const void* W_down, void* y_perm, void* ws, size_t ws_bytes,
+                         void* stream);
+
+/* Un-permute and gate-weighted sum, plus the shared expert: [K2-MoE] y_routed = sum_i G_i E_i,
+ * D_ffn = y_routed + y_shared; the `moe_infer` back half of [K3-UP]; on the K3 path the RMSNorm of
+ * the latent sum (when latent_norm) and the up-projection y_routed = u_hat W_up^T [K3-UP].
+ *   y_perm       from moe_experts;  perm_dst [T*k] from moe_permute
+ *   topk_weight  [T][k] fp32 from moe_router
+ *   W_up         [d][d_latent] act_dtype, K3 only (else NULL)
+ *   out          [T][d] act_dtype: D_ffn.  The sum is taken in fp32 and rounded once. */
+moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int32_t* perm_dst,
+                         const float* topk_weight, const void* W_up, void* out, void* ws,
+                         size_t ws_bytes, void* stream);
+
+/* The whole layer: moe_router -> moe_permute -> moe_experts -> moe_combine, with every
+ * intermediate in the workspace, enqueued on one stream with no host synchronisation.
+ * Arguments as above.  Clears the device status word on entry. */
+moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const float* W_r, const float* b,
+                         const void* W13, const void* W2, const float* W13_scale,
+                         const float* W2_scale, const void* Ws13, const void* Ws2,
+                         const float* Ws13_scale, const float* Ws2_scale, const void* W_down,
+                         const void* W_up, void* out, void* ws, size_t ws_bytes, void* stream);
+
+/* The whole layer from HOST buffers: copies x (pinned or pageable host memory, [T][d] act_dtype)
+ * to the workspace, runs moe_forward on resident device weights, and copies the output back to
+ * out_host ([T][d] act_dtype).  Synchronises `stream` before returning.  Weights stay device
+ * pointers. */
+moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, const float* W_r,
+                                 const float* b, const void* W13, const void* W2,
+                                 const float* W13_scale, const float* W2_scale, const void* Ws13,
+                                 const void* Ws2, const float* Ws13_scale, const float* Ws2_scale,
+                                 const void* W_down, const void* W_up, void* out_host, void* ws,
+                                 size_t ws_bytes, void* stream);
+
+/* Reset the device status word (first 256 bytes of ws) to "no error", enqueued on stream. */
+moe_status_t moe_reset_device_status(void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronise `stream`, read the device status word and translate it: MOE_OK,
+ * MOE_ERR_DEVICE_CHECK (an index or row out of range was skipped) or MOE_ERR_TIMEOUT (a kernel's
+ * bounded wait expired; its outputs are incomplete).  MOE_ERR_CUDA if the stream reports an
+ * error. */
+moe_status_t moe_device_status(const void* ws, size_t ws_bytes, void* stream);
+
+/* A static, human-readable name of a status code. */
+const char* moe_status_string(moe_status_t status);
+
+/* Number of this library's kernels enqueued by the calling thread since the last reset (a launch
+ * counter for benchmarks), and its reset. */
+uint64_t moe_launch_count(void);
+void moe_reset_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,493 @@
+// gemm_tc.cu -- grouped GEMM on the 5th-generation tensor cores (tcgen05, TMEM, TMA), bf16 in,
+// fp32 accumulation.
+//
+// The expert MLPs of the "Mixture of experts" steps (g = x W1, u = x W3, a = g sigma(g), h = a * u,
+// E_i = h W2; the shared expert the same) run as grouped GEMMs over the permuted rows: one group per
+// routed expert (rows [offsets[g], offsets[g+1])) plus a trailing dense group (the shared expert,
+// every token, or a plain dense projection).  This replaces the per-expert host loop of the
+// `moe_infer` excerpt on "Kimi K3 · Latent up-projection"; group sizes stay on the device.
+//
+// Kernel shape: persistent, one CTA per SM, 192 threads, warp-specialised:
+//   warp 0      TMA producer: K-blocks of 64 bf16 (one 128-byte swizzle row) into a ring of
+//               shared-memory stages, completion counted on full[s] mbarriers;
+//   warp 1      MMA issuer (one thread): tcgen05.mma kind::f16, M = 128, into one of two TMEM
+//               accumulators, frees stages with tcgen05.commit -> empty[s], signals tmem_full[a];
+//   warps 2..5  epilogue: tcgen05.ld from TMEM (each warp reads its 32-lane quarter), SwiGLU or a
+//               plain store, then release the accumulator (tmem_empty[a]) so the next tile's
+//               mainloop overlaps this tile's epilogue.
+// Two tile orientations:
+//   rows  (swap = 0): MMA M = 128 token rows, N = 256 weight rows.  SwiGLU tiles load 128 W1 rows and
+//                     the matching 128 W3 rows, so each thread (= one token row) holds g and u of the
+//                     same features in its own TMEM lane and the epilogue needs no exchange.
+//   swap  (swap = 1): MMA M = 128 weight rows, N = 32 tokens, for groups with few rows (decode):
+//                     the weights stream once per 32 tokens instead of once per 128-row tile padded
+//                     with empty rows.  SwiGLU keeps a W1 accumulator and a W3 accumulator.
+// Every wait is bounded (common.cuh): on expiry the kernel flags kErrTimeout, drains its in-flight
+// copies and MMAs, frees TMEM and returns.
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+#include "sched.cuh"
+
+namespace moe {
+
+constexpr int kTcThreads = 192;
+constexpr int kBK = 64;                  // bf16 K-elements per stage (128 bytes per row)
+constexpr int kBoxBytes = 128 * 128;     // one 128-row x 128-byte operand box
+constexpr int kTcMaxGroups = 1025;
+constexpr int kSmemLimit = 232448;       // 227 KB per CTA
+
+struct TcParams {
+  CUtensorMap map_act;    // routed activations [rows][K]
+  CUtensorMap map_w;      // routed weights [E * w_group_rows][K]
+  CUtensorMap map_act_d;  // dense-group activations
+  CUtensorMap map_w_d;    // dense-group weights
+  const int32_t* offsets;
+  int32_t n_routed, w_group_rows, u_off, u_off_d;
+  int32_t dense_rows, dense_act_row0, dense_out_row0;
+  int32_t K, k_wrap, F;
+  void* out;
+  int64_t ldo;
+  int32_t out_f32;
+  const __nv_bfloat16* addend;
+  int64_t ld_add;
+  uint32_t* err;
+};
+
+template <bool kSwap, int kBN, int kEpi>
+struct TcShape {
+  static constexpr bool kSwiGLU = kEpi == EPI_SWIGLU;
+  static constexpr int RPT = kSwap ? kBN : 128;                         // token rows per tile
+  static constexpr int FPT = kSwap ? 128 : (kSwiGLU ? kBN / 2 : kBN);  // features per tile
+  static constexpr int OPA = (kSwap && kSwiGLU) ? 2 * kBoxBytes : kBoxBytes;  // A bytes / stage
+  static constexpr int OPB = kBN * 128;                                       // B bytes / stage
+  static constexpr int STAGE = OPA + OPB;
+  static constexpr int ACC_COLS = (kSwap && kSwiGLU) ? 2 * kBN : kBN;  // fp32 columns per tile
+  static constexpr int TMEM_NEED = 2 * ACC_COLS;
+  static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
+                                   : TMEM_NEED <= 64  ? 64
+                                   : TMEM_NEED <= 128 ? 128
+                                   : TMEM_NEED <= 256 ? 256
+                                                      : 512;
+  static constexpr int TABLE_BYTES = 2 * (kTcMaxGroups + 1) * 4 + kTcThreads * 4;
+  static constexpr int BAR_BYTES = 256 + 64;  // barriers, TMEM base, abort flag
+  static constexpr int STAGES_FIT = (kSmemLimit - 1024 - TABLE_BYTES - BAR_BYTES) / STAGE;
+  static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + BAR_BYTES + TABLE_BYTES;
+  static_assert(STAGES >= 2, "not enough shared memory for two stages");
+  static_assert(TMEM_NEED <= 512, "accumulators exceed TMEM");
+  static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment for SWIZZLE_128B");
+  static_assert(2 * STAGES + 5 <= 32, "barrier area too small");
+};
+
+template <bool kSwap, int kBN, int kEpi>
+__global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid_constant__ TcParams p) {
+  using S = TcShape<kSwap, kBN, kEpi>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::STAGES * S::STAGE);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + S::STAGES;
+  uint64_t* tfull = bars + 2 * S::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint64_t* drain = tempty + 2;
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 32);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+  int* tile_start = reinterpret_cast<int*>(smem + S::STAGES * S::STAGE + S::BAR_BYTES);
+  int* row_start = tile_start + (kTcMaxGroups + 1);
+  int* scratch = row_start + (kTcMaxGroups + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_map(&p.map_act);
+    tma_prefetch_map(&p.map_w);
+    if (p.dense_rows > 0) {
+      tma_prefetch_map(&p.map_act_d);
+      tma_prefetch_map(&p.map_w_d);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_holder, S::TMEM_COLS);
+    tmem_relinquish();
+  }
+  build_tile_table(tile_start, row_start, scratch, p.offsets, p.n_routed, p.dense_rows, S::RPT,
+                   p.F / S::FPT);  // ends with __syncthreads
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_holder;
+  const int G = p.n_routed + (p.dense_rows > 0 ? 1 : 0);
+  const int total = tile_start[G];
+  const int nkb = p.K / kBK;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      uint32_t stage = 0, phase = 0;
+      int armed = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
+                                        p.dense_rows, p.dense_act_row0, S::RPT);
+        const CUtensorMap* ma = ti.dense ? &p.map_act_d : &p.map_act;
+        const CUtensorMap* mw = ti.dense ? &p.map_w_d : &p.map_w;
+        const int act_y = ti.grp_row0 + ti.rt * S::RPT;
+        const int w_y = (ti.dense ? 0 : ti.g * p.w_group_rows) + ti.ft * S::FPT;
+        const int u_off = ti.dense ? p.u_off_d : p.u_off;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = smem + stage * S::STAGE;
+          uint8_t* sb = sa + S::OPA;
+          mbar_arrive_expect_tx(&full[stage], S::STAGE);
+          const int kx = kb * kBK;
+          const int ax = kx % p.k_wrap;
+          if (!kSwap) {
+            tma_load_2d(sa, ma, &full[stage], ax, act_y);
+            if (S::kSwiGLU) {
+              tma_load_2d(sb, mw, &full[stage], kx, w_y);
+              tma_load_2d(sb + kBoxBytes, mw, &full[stage], kx, w_y + u_off);
+            } else {
+#pragma unroll
+              for (int j = 0; j < kBN / 128; ++j)
+                tma_load_2d(sb + j * kBoxBytes, mw, &full[stage], kx, w_y + j * 128);
+            }
+          } else {
+            tma_load_2d(sa, mw, &full[stage], kx, w_y);
+            if (S::kSwiGLU) tma_load_2d(sa + kBoxBytes, mw, &full[stage], kx, w_y + u_off);
+            tma_load_2d(sb, ma, &full[stage], ax, act_y);
+          }
+          if (armed < S::STAGES) ++armed;
+          if (++stage == S::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // drain: wait (briefly) for the copies of the most recent stage uses to land
+        for (int i = 0; i < armed; ++i) {
+          if (stage == 0) {
+            stage = S::STAGES;
+            phase ^= 1u;
+          }
+          --stage;
+          mbar_wait(&full[stage], phase, nullptr, nullptr, kDrainLimitNs);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t kIdesc = idesc_bf16_f32<128, kBN>();
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) break;
+        tc_fence_after();
+        const uint32_t d0 = tmem_base + acc * S::ACC_COLS;
+        for (int kb = 0; kb < nkb; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = smem_u32(smem + stage * S::STAGE);
+          const uint32_t sb = sa + S::OPA;
+#pragma unroll
+          for (int k16 = 0; k16 < kBK / 16; ++k16) {
+            const uint32_t accum = (kb | k16) != 0;
+            const uint64_t bdesc = sw128_kmajor_desc(sb + k16 * 32);
+            mma_bf16(d0, sw128_kmajor_desc(sa + k16 * 32), bdesc, kIdesc, accum);
+            if (kSwap && S::kSwiGLU)
+              mma_bf16(d0 + kBN, sw128_kmajor_desc(sa + kBoxBytes + k16 * 32), bdesc, kIdesc,
+                       accum);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == S::STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // every MMA issued above has completed once this commit arrives
+      mma_commit(drain);
+      mbar_wait(drain, 0, nullptr, nullptr, kDrainLimitNs);
+    }
+  } else {
+    // ------------------------------------------------------------------ epilogue (warps 2..5)
+    const int quarter = warp & 3;       // TMEM lanes this warp may read: 32 * quarter + [0, 32)
+    const int r = quarter * 32 + lane;  // tile row (rows) or tile feature (swap)
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
+                                      p.dense_rows, p.dense_act_row0, S::RPT);
+      int ok = 1;
+      if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err) ? 1 : 0;
+      ok = __shfl_sync(0xffffffffu, ok, 0);
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tb = tmem_base + acc * S::ACC_COLS + ((uint32_t)(quarter * 32) << 16);
+      const int64_t out_row0 = (ti.dense ? (int64_t)p.dense_out_row0 : (int64_t)ti.grp_row0) +
+                               (int64_t)ti.rt * S::RPT;
+      if (!kSwap) {
+        const bool valid = r < ti.valid;
+        const int64_t orow = out_row0 + r;
+        if (S::kSwiGLU) {
+          __nv_bfloat16* dst = (__nv_bfloat16*)p.out + orow * p.ldo + (int64_t)ti.ft * S::FPT;
+#pragma unroll 1
+          for (int c = 0; c < S::FPT; c += 16) {
+            uint32_t g[16], u[16];
+            tmem_ld16(tb + c, g);
+            tmem_ld16(tb + S::FPT + c, u);
+            tmem_ld_wait();
+            if (valid) {
+              uint32_t pk[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float h0 = silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+                const float h1 =
+                    silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+                pk[i] = pack_bf16x2(h0, h1);
+              }
+              uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+              d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+              d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+            }
+          }
+        } else {
+          const int64_t col0 = (int64_t)ti.ft * S::FPT;
+#pragma unroll 1
+          for (int c = 0; c < S::FPT; c += 16) {
+            uint32_t v[16];
+            tmem_ld16(tb + c, v);
+            tmem_ld_wait();
+            if (valid) {
+              if (p.out_f32) {
+                float4* d4 = reinterpret_cast<float4*>((float*)p.out + orow * p.ldo + col0 + c);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                  d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                      __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+              } else {
+                float f[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+                if (kEpi == EPI_STORE_ADD) {
+                  const uint4* a4 =
+                      reinterpret_cast<const uint4*>(p.addend + orow * p.ld_add + col0 + c);
+#pragma unroll
+                  for (int h = 0; h < 2; ++h) {
+                    const uint4 raw = __ldg(a4 + h);
+                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                      const float2 af = __bfloat1622float2(b2[i]);
+                      f[8 * h + 2 * i] += af.x;
+                      f[8 * h + 2 * i + 1] += af.y;
+                    }
+                  }
+                }
+                uint32_t pk[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+                uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)p.out + orow * p.ldo + col0 + c);
+                d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              }
+            }
+          }
+        }
+      } else {
+        // swap: TMEM lane = output feature, columns = tokens of this tile
+        const int64_t feat = (int64_t)ti.ft * 128 + r;
+#pragma unroll 1
+        for (int c = 0; c < kBN; c += 16) {
+          uint32_t g[16], u[16];
+          tmem_ld16(tb + c, g);
+          if (S::kSwiGLU) tmem_ld16(tb + kBN + c, u);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            if (c + i < ti.valid) {
+              const int64_t orow = out_row0 + c + i;
+              float v = __uint_as_float(g[i]);
+              if (S::kSwiGLU) v = silu_fast(v) * __uint_as_float(u[i]);
+              if (p.out_f32) {
+                ((float*)p.out)[orow * p.ldo + feat] = v;
+              } else {
+                if (kEpi == EPI_STORE_ADD) v += __bfloat162float(p.addend[orow * p.ld_add + feat]);
+                ((__nv_bfloat16*)p.out)[orow * p.ldo + feat] = __float2bfloat16_rn(v);
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, S::TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------------------------
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2D bf16 map over [rows][cols] (cols contiguous), box {64 cols, box_rows rows}, 128-byte swizzle,
+// out-of-range elements read as zero.
+static bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
+                          int box_rows) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !base || rows <= 0 || cols <= 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kBK, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <bool kSwap, int kBN, int kEpi>
+static cudaError_t launch_variant(const TcParams& p, int grid, cudaStream_t st) {
+  using S = TcShape<kSwap, kBN, kEpi>;
+  auto kern = moe_gemm_tc_kernel<kSwap, kBN, kEpi>;
+  static int attr_set_device = -1;  // the attribute is per device; refreshed when it changes
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_set_device != dev) {
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set_device = dev;
+  }
+  kern<<<grid, kTcThreads, S::SMEM, st>>>(p);
+  count_launch();
+  return cudaGetLastError();
+}
+
+bool gemm_tc_supported(const GroupedGemm& g, int swap) {
+  if (g.act_dtype != MOE_BF16 || g.w_dtype != MOE_BF16) return false;
+  if (g.K <= 0 || g.K % kBK) return false;
+  const int kw = g.k_wrap > 0 ? g.k_wrap : g.K;
+  if (kw % kBK || g.K % kw) return false;
+  if (g.n_routed > kTcMaxGroups - 1) return false;
+  if (g.epi == EPI_SWIGLU) {
+    if (g.F % 128) return false;
+    if (g.out_dtype != MOE_BF16) return false;
+  } else {
+    if (g.F % (swap ? 128 : 256) && !(g.F % 128 == 0 && !swap && g.out_dtype == MOE_F32))
+      return false;
+  }
+  if (g.ldo % 8) return false;
+  if (g.epi == EPI_STORE_ADD && (!g.addend || g.ld_add % 8 || g.out_dtype != MOE_BF16))
+    return false;
+  return true;
+}
+
+cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStream_t st) {
+  if (!gemm_tc_supported(g, swap)) return cudaErrorInvalidValue;
+  TcParams p;
+  memset(&p, 0, sizeof(p));
+  const bool f32_router = !swap && g.epi == EPI_STORE && g.out_dtype == MOE_F32 && g.F % 256;
+  const int act_box = swap ? 32 : 128;
+  const int kw = g.k_wrap > 0 ? g.k_wrap : g.K;
+  if (g.n_routed > 0) {
+    if (!make_map_bf16(&p.map_act, g.act, g.act_rows, kw, act_box)) return cudaErrorInvalidValue;
+    if (!make_map_bf16(&p.map_w, g.w, g.w_rows, g.K, 128)) return cudaErrorInvalidValue;
+  }
+  if (g.dense_rows > 0) {
+    if (!make_map_bf16(&p.map_act_d, g.act_d, g.act_d_rows, kw, act_box))
+      return cudaErrorInvalidValue;
+    if (!make_map_bf16(&p.map_w_d, g.w_d, g.w_d_rows, g.K, 128)) return cudaErrorInvalidValue;
+  }
+  if (g.n_routed == 0) {  // keep the unused maps valid objects
+    p.map_act = p.map_act_d;
+    p.map_w = p.map_w_d;
+  }
+  if (g.dense_rows == 0) {
+    p.map_act_d = p.map_act;
+    p.map_w_d = p.map_w;
+  }
+  p.offsets = g.offsets;
+  p.n_routed = g.n_routed;
+  p.w_group_rows = g.w_group_rows;
+  p.u_off = g.u_off;
+  p.u_off_d = g.u_off_d;
+  p.dense_rows = g.dense_rows;
+  p.dense_act_row0 = g.dense_act_row0;
+  p.dense_out_row0 = g.dense_out_row0;
+  p.K = g.K;
+  p.k_wrap = kw;
+  p.F = g.F;
+  p.out = g.out;
+  p.ldo = g.ldo;
+  p.out_f32 = g.out_dtype == MOE_F32;
+  p.addend = (const __nv_bfloat16*)g.addend;
+  p.ld_add = g.ld_add;
+  p.err = g.err;
+  const int grid = num_sms;
+  if (!swap) {
+    if (g.epi == EPI_SWIGLU) return launch_variant<false, 256, EPI_SWIGLU>(p, grid, st);
+    if (f32_router) return launch_variant<false, 128, EPI_STORE>(p, grid, st);
+    if (g.epi == EPI_STORE) return launch_variant<false, 256, EPI_STORE>(p, grid, st);
+    return launch_variant<false, 256, EPI_STORE_ADD>(p, grid, st);
+  }
+  if (g.epi == EPI_SWIGLU) return launch_variant<true, 32, EPI_SWIGLU>(p, grid, st);
+  if (g.epi == EPI_STORE) return launch_variant<true, 32, EPI_STORE>(p, grid, st);
+  return launch_variant<true, 32, EPI_STORE_ADD>(p, grid, st);
+}
+
+}  // namespace moe

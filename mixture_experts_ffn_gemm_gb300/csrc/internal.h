@@ -1,0 +1,103 @@
+// internal.h -- host-side interfaces between the C ABI (moe_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Flags of the device status word (first word of the workspace).
+enum : uint32_t {
+  kErrTimeout = 1u,  // a bounded wait expired
+  kErrIndex = 2u,    // an expert index / row outside its range was skipped
+};
+
+enum Epi { EPI_SWIGLU = 0, EPI_STORE = 1, EPI_STORE_ADD = 2 };
+
+// A grouped GEMM  out[row][f] = sum_k act[row][k] * w[wrow(f)][k]  over groups of rows, with the
+// SwiGLU epilogue h = SiLU(g) * u (g from the W1 row f, u from the W3 row f + u_off) or a plain
+// store (optionally plus a bf16 addend).
+struct GroupedGemm {
+  // routed groups: rows [offsets[g], offsets[g+1]) of act, weights rows [g*w_group_rows, ...)
+  const void* act = nullptr;  // [act_rows][K]
+  int64_t act_rows = 0;
+  const void* w = nullptr;    // [w_rows][K]
+  int64_t w_rows = 0;
+  const int32_t* offsets = nullptr;  // device [n_routed + 1]
+  int n_routed = 0;
+  int w_group_rows = 0;
+  int u_off = 0;
+  // trailing dense group (shared expert or a dense projection)
+  const void* act_d = nullptr;  // [act_d_rows][K]
+  int64_t act_d_rows = 0;
+  int dense_act_row0 = 0;
+  const void* w_d = nullptr;    // [w_d_rows][K]
+  int64_t w_d_rows = 0;
+  int dense_rows = 0;
+  int dense_out_row0 = 0;
+  int u_off_d = 0;
+  // shapes
+  int K = 0;
+  int k_wrap = 0;  // activation column = k mod k_wrap (3-way split router); K when unused
+  int F = 0;       // output features per group
+  int epi = EPI_STORE;
+  int act_dtype = MOE_BF16;
+  int w_dtype = MOE_BF16;
+  // output
+  void* out = nullptr;
+  int64_t ldo = 0;
+  int out_dtype = MOE_BF16;
+  const void* addend = nullptr;  // EPI_STORE_ADD: bf16 [rows][ld_add], indexed like out
+  int64_t ld_add = 0;
+  // split-K (SIMT router only): out slice s at out + s * split_stride elements
+  int k_splits = 1;
+  int64_t split_stride = 0;
+  uint32_t* err = nullptr;
+};
+
+// Tensor-core grouped GEMM (tcgen05 + TMA), bf16 operands, fp32 accumulation in TMEM.
+// swap = 0: token rows are the MMA M side (128-row tiles), weights the N side.
+// swap = 1: weight rows are the M side, tokens the N side (32-token tiles), for few rows per group.
+// Requires K % 64 == 0, F % 128 == 0 (F % 256 == 0 for swap = 0 stores).  Returns a CUDA error or
+// cudaErrorInvalidValue when the shapes are not supported (nothing launched).
+cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStream_t st);
+bool gemm_tc_supported(const GroupedGemm& g, int swap);
+
+// CUDA-core grouped GEMM (fp32 or bf16 operands, fp32 accumulation), 64x64 tiles.
+cudaError_t launch_gemm_simt(const GroupedGemm& g, int num_sms, cudaStream_t st);
+
+// Router: selection and gates from logits (split-K partial slices summed in a fixed order).
+cudaError_t launch_router_topk(const float* partial, int S, int64_t split_stride, int64_t T,
+                               int E, int k, const float* b, float gate_scale, float* logits_out,
+                               int32_t* idx, float* weight, cudaStream_t st);
+// fp32 [E][d] -> bf16 [E][3d] (hi | mid | lo) so that hi + mid + lo reproduces each weight.
+cudaError_t launch_split_router_weights(const float* W_r, int E, int d, __nv_bfloat16* out,
+                                        cudaStream_t st);
+
+// Permute: histogram, scan, stable scatter.
+int permute_chunks(int64_t P);
+cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int E, int n_shared,
+                           int32_t* chunk_counts, int32_t* counts, int32_t* offsets,
+                           int32_t* perm_src, int32_t* perm_dst, uint32_t* err, cudaStream_t st);
+// dst[r] = src[perm_src[r] / k] for r < P (rows of `width` elements of elem_bytes each).
+cudaError_t launch_gather_rows(const void* src, const int32_t* perm_src, int64_t P, int k,
+                               int width, int elem_bytes, void* dst, int num_sms, cudaStream_t st);
+
+// Combine: out[t] = sum_j w[t,j] * y[perm_dst[t*k+j]] + y_shared[t]  (fp32 sum, one rounding).
+cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* y_shared,
+                           const int32_t* perm_dst, const float* weight, int64_t T, int k, int d,
+                           void* out, int num_sms, cudaStream_t st);
+// K3: u_hat[t] = RMSNorm?( sum_j w[t,j] * y[perm_dst[t*k+j]] ) in bf16, width L.
+cudaError_t launch_latent_combine(const void* y_perm, const int32_t* perm_dst,
+                                  const float* weight, int64_t T, int k, int L, int norm,
+                                  float eps, void* u_hat, int num_sms, cudaStream_t st);
+
+// Launch counter (per host thread).
+void count_launch(int n = 1);
+
+}  // namespace moe

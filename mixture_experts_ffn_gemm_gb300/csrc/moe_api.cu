@@ -1,0 +1,591 @@
+// moe_api.cu -- the C ABI of include/moe.h: host validation, workspace layout and the order of
+// kernel launches for each entry point.  No allocation, no host synchronisation on the layer path.
+#include <cstring>
+
+#include "internal.h"
+
+namespace moe {
+
+static thread_local uint64_t g_launches = 0;
+void count_launch(int n) { g_launches += (uint64_t)n; }
+
+static int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1)
+    n = 1;
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+static size_t dtype_bytes(int dt) { return dt == MOE_F32 ? 4 : dt == MOE_BF16 ? 2 : 1; }
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+// Choices that depend only on the configuration (so that the workspace size is deterministic).
+struct Plan {
+  bool latent;
+  int de;             // expert width: d or d_latent
+  bool router_tc;     // tensor-core router (3 x bf16 split weights)
+  int router_splits;  // split-K slices of the CUDA-core router
+  int swap;           // 1: weight-rows-as-M tensor-core tiles
+  bool tc;            // tensor-core expert GEMMs
+};
+
+struct Layout {
+  size_t status, zbuf, wsplit, idx, weight, chunk_counts, counts, offsets, perm_src, perm_dst,
+      x_lat, x_perm, h, y_perm, u_hat, x_io, out_io, total;
+};
+
+static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+static moe_status_t validate(const moe_config_t* c) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->T < 0 || c->T > (int64_t)1 << 26) return MOE_ERR_INVALID_ARG;
+  if (c->d <= 0 || c->E < 1 || c->k < 1 || c->k > c->E || c->I <= 0) return MOE_ERR_INVALID_ARG;
+  if (c->n_shared != 0 && c->n_shared != 1) return MOE_ERR_INVALID_ARG;
+  if (c->d_latent < 0 || c->reserved_ != 0) return MOE_ERR_INVALID_ARG;
+  if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->w_dtype != MOE_F32 && c->w_dtype != MOE_BF16 && c->w_dtype != MOE_FP8_E4M3)
+    return MOE_ERR_INVALID_ARG;
+  if (c->k > 32 || c->E > 1023) return MOE_ERR_UNSUPPORTED;
+  if (c->n_shared && c->I_shared != c->I) return MOE_ERR_UNSUPPORTED;
+  if (c->T * c->k + c->T >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
+  if (c->w_dtype == MOE_FP8_E4M3) return MOE_ERR_UNSUPPORTED;
+  if (c->w_dtype != c->act_dtype) return MOE_ERR_UNSUPPORTED;
+  if (c->act_dtype == MOE_F32) {
+    if (c->d % 16 || c->I % 16 || c->d % 4) return MOE_ERR_UNSUPPORTED;
+    if (c->d_latent > 0) return MOE_ERR_UNSUPPORTED;
+  } else {
+    if (c->d % 256 || c->I % 128) return MOE_ERR_UNSUPPORTED;
+    if (c->d_latent > 0 && (c->d_latent % 256 || c->d_latent > 8192)) return MOE_ERR_UNSUPPORTED;
+  }
+  return MOE_OK;
+}
+
+static Plan make_plan(const moe_config_t* c) {
+  Plan p;
+  p.latent = c->d_latent > 0;
+  p.de = p.latent ? c->d_latent : c->d;
+  p.tc = c->act_dtype == MOE_BF16;
+  // router
+  const bool tc_ok = c->act_dtype == MOE_BF16 && c->E % 128 == 0 && c->d % 64 == 0;
+  if (c->flags & MOE_FLAG_ROUTER_SIMT)
+    p.router_tc = false;
+  else if (c->flags & MOE_FLAG_ROUTER_TC)
+    p.router_tc = tc_ok;
+  else
+    p.router_tc = tc_ok && c->T >= 1024;
+  p.router_splits = 1;
+  if (!p.router_tc) {
+    const int64_t tiles = ((c->T + 63) / 64) * ((c->E + 63) / 64);
+    int s = (int)((304 + (tiles > 0 ? tiles : 1) - 1) / (tiles > 0 ? tiles : 1));
+    if (s > 32) s = 32;
+    while (s > 1 && (c->d % (16 * s) != 0)) --s;
+    p.router_splits = s < 1 ? 1 : s;
+  }
+  // expert GEMM tile orientation
+  if (c->flags & MOE_FLAG_GEMM_SWAP_AB)
+    p.swap = 1;
+  else if (c->flags & MOE_FLAG_GEMM_ROWS_MAJOR)
+    p.swap = 0;
+  else
+    p.swap = c->T <= 512 ? 1 : 0;
+  return p;
+}
+
+static Layout make_layout(const moe_config_t* c, const Plan& pl) {
+  Layout L;
+  const int64_t T = c->T, P = T * c->k, E = c->E, d = c->d, I = c->I;
+  const size_t ab = dtype_bytes(c->act_dtype);
+  const int64_t shared_rows = T * c->n_shared;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  };
+  L.status = take(256);
+  L.zbuf = take((size_t)pl.router_splits * T * E * 4);
+  L.wsplit = take(pl.router_tc ? (size_t)E * 3 * d * 2 : 0);
+  L.idx = take((size_t)P * 4);
+  L.weight = take((size_t)P * 4);
+  L.chunk_counts = take((size_t)permute_chunks(P) * E * 4);
+  L.counts = take((size_t)(E + 1) * 4);
+  L.offsets = take((size_t)(E + 2) * 4);
+  L.perm_src = take((size_t)P * 4);
+  L.perm_dst = take((size_t)P * 4);
+  L.x_lat = take(pl.latent ? (size_t)T * c->d_latent * ab : 0);
+  L.x_perm = take((size_t)P * pl.de * ab);
+  L.h = take((size_t)(P + shared_rows) * I * ab);
+  L.y_perm = take(((size_t)P * pl.de + (size_t)shared_rows * d) * ab);
+  L.u_hat = take(pl.latent ? (size_t)T * c->d_latent * 2 : 0);
+  L.x_io = take((size_t)T * d * ab);
+  L.out_io = take((size_t)T * d * ab);
+  L.total = off;
+  return L;
+}
+
+static moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+template <typename T>
+static T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+struct Ctx {
+  const moe_config_t* c;
+  Plan pl;
+  Layout L;
+  void* ws;
+  cudaStream_t st;
+  int sms;
+  uint32_t* err;
+};
+
+static moe_status_t begin(Ctx& x, const moe_config_t* c, void* ws, size_t ws_bytes,
+                          void* stream) {
+  moe_status_t s = validate(c);
+  if (s != MOE_OK) return s;
+  x.c = c;
+  x.pl = make_plan(c);
+  x.L = make_layout(c, x.pl);
+  if (!ws || ws_bytes < x.L.total) return MOE_ERR_WORKSPACE;
+  if (!aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  x.ws = ws;
+  x.st = static_cast<cudaStream_t>(stream);
+  x.sms = 0;
+  x.err = at<uint32_t>(ws, x.L.status);
+  return MOE_OK;
+}
+
+// First CUDA runtime calls of an entry point, made only after every host-side check passed.
+static void ready(Ctx& x) {
+  x.sms = num_sms();
+  (void)cudaGetLastError();  // start from a clean launch-error state
+}
+
+// ---------------------------------------------------------------------------------------------
+// Stages
+// ---------------------------------------------------------------------------------------------
+static moe_status_t run_router(Ctx& x, const void* xin, const float* W_r, const float* b,
+                               float* logits, int32_t* idx, float* weight) {
+  const moe_config_t* c = x.c;
+  if (c->T == 0) return MOE_OK;
+  cudaError_t e;
+  if (x.pl.router_tc) {
+    __nv_bfloat16* ws_split = at<__nv_bfloat16>(x.ws, x.L.wsplit);
+    e = launch_split_router_weights(W_r, c->E, c->d, ws_split, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+    float* z = logits ? logits : at<float>(x.ws, x.L.zbuf);
+    GroupedGemm g;
+    g.act_d = xin;
+    g.act_d_rows = c->T;
+    g.w_d = ws_split;
+    g.w_d_rows = c->E;
+    g.dense_rows = (int)c->T;
+    g.K = 3 * c->d;
+    g.k_wrap = c->d;
+    g.F = c->E;
+    g.epi = EPI_STORE;
+    g.out = z;
+    g.ldo = c->E;
+    g.out_dtype = MOE_F32;
+    g.err = x.err;
+    e = launch_gemm_tc(g, 0, x.sms, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+    e = launch_router_topk(z, 1, 0, c->T, c->E, c->k, b, c->gate_scale, nullptr, idx, weight,
+                           x.st);
+    return from_cuda(e);
+  }
+  float* zp = at<float>(x.ws, x.L.zbuf);
+  GroupedGemm g;
+  g.act_d = xin;
+  g.act_d_rows = c->T;
+  g.w_d = W_r;
+  g.w_d_rows = c->E;
+  g.dense_rows = (int)c->T;
+  g.K = c->d;
+  g.k_wrap = c->d;
+  g.F = c->E;
+  g.epi = EPI_STORE;
+  g.act_dtype = c->act_dtype;
+  g.w_dtype = MOE_F32;
+  g.out = zp;
+  g.ldo = c->E;
+  g.out_dtype = MOE_F32;
+  g.k_splits = x.pl.router_splits;
+  g.split_stride = c->T * c->E;
+  g.err = x.err;
+  e = launch_gemm_simt(g, x.sms, x.st);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = launch_router_topk(zp, x.pl.router_splits, c->T * c->E, c->T, c->E, c->k, b,
+                         c->gate_scale, logits, idx, weight, x.st);
+  return from_cuda(e);
+}
+
+static moe_status_t run_permute(Ctx& x, const int32_t* idx, int32_t* counts, int32_t* offsets,
+                                int32_t* perm_src, int32_t* perm_dst) {
+  const moe_config_t* c = x.c;
+  return from_cuda(launch_permute(idx, c->T, c->k, c->E, c->n_shared,
+                                  at<int32_t>(x.ws, x.L.chunk_counts), counts, offsets, perm_src,
+                                  perm_dst, x.err, x.st));
+}
+
+static cudaError_t gemm(Ctx& x, const GroupedGemm& g) {
+  if (x.pl.tc) return launch_gemm_tc(g, x.pl.swap, x.sms, x.st);
+  return launch_gemm_simt(g, x.sms, x.st);
+}
+
+static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
+                                const int32_t* perm_src, const void* W13, const void* W2,
+                                const void* Ws13, const void* Ws2, const void* W_down,
+                                void* y_perm) {
+  const moe_config_t* c = x.c;
+  if (c->T == 0) return MOE_OK;
+  const int64_t T = c->T, P = T * c->k;
+  const int de = x.pl.de, I = c->I, d = c->d, E = c->E;
+  const size_t ab = dtype_bytes(c->act_dtype);
+  void* h = at<void>(x.ws, x.L.h);
+  void* x_perm = at<void>(x.ws, x.L.x_perm);
+  cudaError_t e;
+
+  const void* route_src = xin;
+  if (x.pl.latent) {  // x_lat = x W_down^T on every token (the router saw the full width)
+    void* x_lat = at<void>(x.ws, x.L.x_lat);
+    GroupedGemm g;
+    g.act_d = xin;
+    g.act_d_rows = T;
+    g.w_d = W_down;
+    g.w_d_rows = de;
+    g.dense_rows = (int)T;
+    g.K = d;
+    g.k_wrap = d;
+    g.F = de;
+    g.epi = EPI_STORE;
+    g.act_dtype = g.w_dtype = c->act_dtype;
+    g.out = x_lat;
+    g.ldo = de;
+    g.out_dtype = c->act_dtype;
+    g.err = x.err;
+    e = launch_gemm_tc(g, 0, x.sms, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+    route_src = x_lat;
+  }
+  e = launch_gather_rows(route_src, perm_src, P, c->k, de, (int)ab, x_perm, x.sms, x.st);
+  if (e != cudaSuccess) return from_cuda(e);
+
+  // W1 | W3 with the SwiGLU epilogue -> h [P + T][I]
+  const bool fuse_shared = c->n_shared && !x.pl.latent;
+  {
+    GroupedGemm g;
+    g.act = x_perm;
+    g.act_rows = P;
+    g.w = W13;
+    g.w_rows = (int64_t)E * 2 * I;
+    g.offsets = offsets;
+    g.n_routed = E;
+    g.w_group_rows = 2 * I;
+    g.u_off = I;
+    if (fuse_shared) {
+      g.act_d = xin;
+      g.act_d_rows = T;
+      g.w_d = Ws13;
+      g.w_d_rows = 2 * I;
+      g.dense_rows = (int)T;
+      g.dense_out_row0 = (int)P;
+      g.u_off_d = I;
+    }
+    g.K = de;
+    g.k_wrap = de;
+    g.F = I;
+    g.epi = EPI_SWIGLU;
+    g.act_dtype = g.w_dtype = c->act_dtype;
+    g.out = h;
+    g.ldo = I;
+    g.out_dtype = c->act_dtype;
+    g.err = x.err;
+    e = gemm(x, g);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  // W2 -> y_perm [P][de] (+ shared rows [T][d])
+  {
+    GroupedGemm g;
+    g.act = h;
+    g.act_rows = P + (fuse_shared ? T : 0);
+    g.w = W2;
+    g.w_rows = (int64_t)E * de;
+    g.offsets = offsets;
+    g.n_routed = E;
+    g.w_group_rows = de;
+    if (fuse_shared) {
+      g.act_d = h;
+      g.act_d_rows = P + T;
+      g.dense_act_row0 = (int)P;
+      g.w_d = Ws2;
+      g.w_d_rows = d;
+      g.dense_rows = (int)T;
+      g.dense_out_row0 = (int)P;
+    }
+    g.K = I;
+    g.k_wrap = I;
+    g.F = de;
+    g.epi = EPI_STORE;
+    g.act_dtype = g.w_dtype = c->act_dtype;
+    g.out = y_perm;
+    g.ldo = de;
+    g.out_dtype = c->act_dtype;
+    g.err = x.err;
+    e = gemm(x, g);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  if (c->n_shared && x.pl.latent) {  // shared expert on the full-width input
+    void* h_sh = static_cast<uint8_t*>(h) + (size_t)P * I * ab;
+    void* y_sh = static_cast<uint8_t*>(y_perm) + (size_t)P * de * ab;
+    GroupedGemm g;
+    g.act_d = xin;
+    g.act_d_rows = T;
+    g.w_d = Ws13;
+    g.w_d_rows = 2 * I;
+    g.dense_rows = (int)T;
+    g.u_off_d = I;
+    g.K = d;
+    g.k_wrap = d;
+    g.F = I;
+    g.epi = EPI_SWIGLU;
+    g.act_dtype = g.w_dtype = c->act_dtype;
+    g.out = h_sh;
+    g.ldo = I;
+    g.out_dtype = c->act_dtype;
+    g.err = x.err;
+    e = launch_gemm_tc(g, 0, x.sms, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+    GroupedGemm g2;
+    g2.act_d = h_sh;
+    g2.act_d_rows = T;
+    g2.w_d = Ws2;
+    g2.w_d_rows = d;
+    g2.dense_rows = (int)T;
+    g2.K = I;
+    g2.k_wrap = I;
+    g2.F = d;
+    g2.epi = EPI_STORE;
+    g2.act_dtype = g2.w_dtype = c->act_dtype;
+    g2.out = y_sh;
+    g2.ldo = d;
+    g2.out_dtype = c->act_dtype;
+    g2.err = x.err;
+    e = launch_gemm_tc(g2, 0, x.sms, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return MOE_OK;
+}
+
+static moe_status_t run_combine(Ctx& x, const void* y_perm, const int32_t* perm_dst,
+                                const float* weight, const void* W_up, void* out) {
+  const moe_config_t* c = x.c;
+  if (c->T == 0) return MOE_OK;
+  const int64_t T = c->T, P = T * c->k;
+  const size_t ab = dtype_bytes(c->act_dtype);
+  const int de = x.pl.de, d = c->d;
+  const void* y_sh =
+      c->n_shared ? static_cast<const uint8_t*>(y_perm) + (size_t)P * de * ab : nullptr;
+  if (!x.pl.latent)
+    return from_cuda(
+        launch_combine(c->act_dtype, y_perm, y_sh, perm_dst, weight, T, c->k, d, out, x.sms, x.st));
+  void* u_hat = at<void>(x.ws, x.L.u_hat);
+  cudaError_t e = launch_latent_combine(y_perm, perm_dst, weight, T, c->k, de, c->latent_norm,
+                                        c->rms_eps, u_hat, x.sms, x.st);
+  if (e != cudaSuccess) return from_cuda(e);
+  GroupedGemm g;  // y_routed = u_hat W_up^T (+ y_shared)
+  g.act_d = u_hat;
+  g.act_d_rows = T;
+  g.w_d = W_up;
+  g.w_d_rows = d;
+  g.dense_rows = (int)T;
+  g.K = de;
+  g.k_wrap = de;
+  g.F = d;
+  g.epi = y_sh ? EPI_STORE_ADD : EPI_STORE;
+  g.act_dtype = g.w_dtype = c->act_dtype;
+  g.out = out;
+  g.ldo = d;
+  g.out_dtype = c->act_dtype;
+  g.addend = y_sh;
+  g.ld_add = d;
+  g.err = x.err;
+  return from_cuda(launch_gemm_tc(g, 0, x.sms, x.st));
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+// ---------------------------------------------------------------------------------------------
+// C ABI
+// ---------------------------------------------------------------------------------------------
+extern "C" {
+
+size_t moe_workspace_size(const moe_config_t* cfg) {
+  if (validate(cfg) != MOE_OK) return 0;
+  return make_layout(cfg, make_plan(cfg)).total;
+}
+
+moe_status_t moe_router(const moe_config_t* cfg, const void* x, const float* W_r, const float* b,
+                        float* logits, int32_t* topk_idx, float* topk_weight, void* ws,
+                        size_t ws_bytes, void* stream) {
+  Ctx c;
+  moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
+  if (s != MOE_OK) return s;
+  if (!x || !W_r || !b || !topk_idx || !topk_weight) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(W_r) || (logits && !aligned16(logits)))
+    return MOE_ERR_INVALID_ARG;
+  ready(c);
+  return run_router(c, x, W_r, b, logits, topk_idx, topk_weight);
+}
+
+moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, int32_t* counts,
+                         int32_t* offsets, int32_t* perm_src, int32_t* perm_dst, void* ws,
+                         size_t ws_bytes, void* stream) {
+  Ctx c;
+  moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
+  if (s != MOE_OK) return s;
+  if (!topk_idx || !counts || !offsets || !perm_src || !perm_dst) return MOE_ERR_INVALID_ARG;
+  ready(c);
+  return run_permute(c, topk_idx, counts, offsets, perm_src, perm_dst);
+}
+
+moe_status_t moe_experts(const moe_config_t* cfg, const void* x, const int32_t* offsets,
+                         const int32_t* perm_src, const void* W13, const void* W2,
+                         const float* W13_scale, const float* W2_scale, const void* Ws13,
+                         const void* Ws2, const float* Ws13_scale, const float* Ws2_scale,
+                         const void* W_down, void* y_perm, void* ws, size_t ws_bytes,
+                         void* stream) {
+  (void)W13_scale;
+  (void)W2_scale;
+  (void)Ws13_scale;
+  (void)Ws2_scale;
+  Ctx c;
+  moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
+  if (s != MOE_OK) return s;
+  if (!x || !offsets || !perm_src || !W13 || !W2 || !y_perm) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_shared && (!Ws13 || !Ws2)) return MOE_ERR_INVALID_ARG;
+  if (cfg->d_latent > 0 && !W_down) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, W13, W2, Ws13, Ws2, W_down, y_perm};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  ready(c);
+  return run_experts(c, x, offsets, perm_src, W13, W2, Ws13, Ws2, W_down, y_perm);
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int32_t* perm_dst,
+                         const float* topk_weight, const void* W_up, void* out, void* ws,
+                         size_t ws_bytes, void* stream) {
+  Ctx c;
+  moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
+  if (s != MOE_OK) return s;
+  if (!y_perm || !perm_dst || !topk_weight || !out) return MOE_ERR_INVALID_ARG;
+  if (cfg->d_latent > 0 && !W_up) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(y_perm) || !aligned16(out) || (W_up && !aligned16(W_up)))
+    return MOE_ERR_INVALID_ARG;
+  ready(c);
+  return run_combine(c, y_perm, perm_dst, topk_weight, W_up, out);
+}
+
+moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const float* W_r, const float* b,
+                         const void* W13, const void* W2, const float* W13_scale,
+                         const float* W2_scale, const void* Ws13, const void* Ws2,
+                         const float* Ws13_scale, const float* Ws2_scale, const void* W_down,
+                         const void* W_up, void* out, void* ws, size_t ws_bytes, void* stream) {
+  (void)W13_scale;
+  (void)W2_scale;
+  (void)Ws13_scale;
+  (void)Ws2_scale;
+  Ctx c;
+  moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
+  if (s != MOE_OK) return s;
+  if (!x || !W_r || !b || !W13 || !W2 || !out) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_shared && (!Ws13 || !Ws2)) return MOE_ERR_INVALID_ARG;
+  if (cfg->d_latent > 0 && (!W_down || !W_up)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x, W_r, W13, W2, Ws13, Ws2, W_down, W_up, out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  ready(c);
+  if (cudaMemsetAsync(c.err, 0, 256, c.st) != cudaSuccess) return MOE_ERR_CUDA;
+  const Layout& L = c.L;
+  int32_t* idx = at<int32_t>(ws, L.idx);
+  float* wgt = at<float>(ws, L.weight);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* perm_src = at<int32_t>(ws, L.perm_src);
+  int32_t* perm_dst = at<int32_t>(ws, L.perm_dst);
+  void* y_perm = at<void>(ws, L.y_perm);
+  if ((s = run_router(c, x, W_r, b, nullptr, idx, wgt)) != MOE_OK) return s;
+  if ((s = run_permute(c, idx, at<int32_t>(ws, L.counts), offsets, perm_src, perm_dst)) != MOE_OK)
+    return s;
+  if ((s = run_experts(c, x, offsets, perm_src, W13, W2, Ws13, Ws2, W_down, y_perm)) != MOE_OK)
+    return s;
+  return run_combine(c, y_perm, perm_dst, wgt, W_up, out);
+}
+
+moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, const float* W_r,
+                                 const float* b, const void* W13, const void* W2,
+                                 const float* W13_scale, const float* W2_scale, const void* Ws13,
+                                 const void* Ws2, const float* Ws13_scale, const float* Ws2_scale,
+                                 const void* W_down, const void* W_up, void* out_host, void* ws,
+                                 size_t ws_bytes, void* stream) {
+  Ctx c;
+  moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
+  if (s != MOE_OK) return s;
+  if (!x_host || !out_host) return MOE_ERR_INVALID_ARG;
+  if (!W_r || !b || !W13 || !W2) return MOE_ERR_INVALID_ARG;
+  ready(c);
+  const size_t bytes = (size_t)cfg->T * cfg->d * dtype_bytes(cfg->act_dtype);
+  void* x_dev = at<void>(ws, c.L.x_io);
+  void* out_dev = at<void>(ws, c.L.out_io);
+  if (bytes && cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, c.st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  s = moe_forward(cfg, x_dev, W_r, b, W13, W2, W13_scale, W2_scale, Ws13, Ws2, Ws13_scale,
+                  Ws2_scale, W_down, W_up, out_dev, ws, ws_bytes, stream);
+  if (s != MOE_OK) return s;
+  if (bytes &&
+      cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, c.st) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return from_cuda(cudaStreamSynchronize(c.st));
+}
+
+moe_status_t moe_reset_device_status(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < 256) return MOE_ERR_WORKSPACE;
+  return from_cuda(cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_device_status(const void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < 256) return MOE_ERR_WORKSPACE;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+  uint32_t flags = 0;
+  if (cudaMemcpy(&flags, ws, sizeof flags, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (flags & kErrTimeout) return MOE_ERR_TIMEOUT;
+  if (flags & kErrIndex) return MOE_ERR_DEVICE_CHECK;
+  return MOE_OK;
+}
+
+const char* moe_status_string(moe_status_t s) {
+  switch (s) {
+    case MOE_OK: return "MOE_OK";
+    case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+    case MOE_ERR_UNSUPPORTED: return "MOE_ERR_UNSUPPORTED";
+    case MOE_ERR_WORKSPACE: return "MOE_ERR_WORKSPACE";
+    case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+    case MOE_ERR_DEVICE_CHECK: return "MOE_ERR_DEVICE_CHECK";
+    case MOE_ERR_TIMEOUT: return "MOE_ERR_TIMEOUT";
+  }
+  return "MOE_ERR_UNKNOWN";
+}
+
+uint64_t moe_launch_count(void) { return g_launches; }
+void moe_reset_launch_count(void) { g_launches = 0; }
+
+}  // extern "C"

@@ -1,0 +1,163 @@
+// permute.cu -- dispatch bookkeeping: group the (token, slot) pairs by expert.
+//
+// "Kimi K3 · Latent up-projection", `moe_infer` code excerpt: count tokens per expert, sort the
+// flattened top-k expert ids, gather the token rows in that order (then, per expert, run its MLP).
+// Here the sort is a stable counting sort done in three kernels, with no host synchronisation:
+//   1. count:   per chunk of pairs, a shared-memory histogram over experts -> chunk_counts[c][e]
+//   2. scan:    per expert, exclusive prefix over chunks; counts[e]; offsets = exclusive prefix of
+//               counts over experts (the shared expert appended as group E with T*n_shared rows)
+//   3. scatter: per chunk, one warp walks the pairs in order; lanes with the same expert get
+//               consecutive slots (__match_any_sync ranks), so each expert's rows stay in
+//               increasing pair order -- a deterministic layout.
+// The gather copies token rows into the permuted order (16-byte vectors).
+#include "common.cuh"
+#include "internal.h"
+
+namespace moe {
+
+constexpr int kChunk = 1024;     // pairs per chunk
+constexpr int kMaxExperts = 1024;
+
+int permute_chunks(int64_t P) { return (int)((P + kChunk - 1) / kChunk); }
+
+__global__ void __launch_bounds__(256)
+    permute_count_kernel(const int32_t* __restrict__ idx, int64_t P, int E,
+                         int32_t* __restrict__ chunk_counts, uint32_t* err) {
+  __shared__ int hist[kMaxExperts];
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t p0 = (int64_t)blockIdx.x * kChunk;
+  const int64_t p1 = min(P, p0 + kChunk);
+  bool bad = false;
+  for (int64_t p = p0 + threadIdx.x; p < p1; p += blockDim.x) {
+    const int e = idx[p];
+    if (e >= 0 && e < E)
+      atomicAdd(&hist[e], 1);
+    else
+      bad = true;
+  }
+  if (bad) raise_flag(err, kErrIndex);
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x)
+    chunk_counts[(int64_t)blockIdx.x * E + e] = hist[e];
+}
+
+__global__ void __launch_bounds__(1024)
+    permute_scan_kernel(int32_t* __restrict__ chunk_counts, int nchunks, int E, int64_t P,
+                        int64_t shared_rows, int32_t* __restrict__ counts,
+                        int32_t* __restrict__ offsets) {
+  __shared__ int sc[1024];
+  const int e = threadIdx.x;
+  int run = 0;
+  if (e < E) {
+    for (int c = 0; c < nchunks; ++c) {
+      const int v = chunk_counts[(int64_t)c * E + e];
+      chunk_counts[(int64_t)c * E + e] = run;  // rows of expert e in the chunks before c
+      run += v;
+    }
+    counts[e] = run;
+  }
+  sc[e] = (e < E) ? run : 0;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive scan over experts
+    const int v = e >= off ? sc[e - off] : 0;
+    __syncthreads();
+    sc[e] += v;
+    __syncthreads();
+  }
+  if (e < E) offsets[e] = sc[e] - run;
+  if (e == 0) {
+    counts[E] = (int32_t)shared_rows;
+    offsets[E] = (int32_t)P;
+    offsets[E + 1] = (int32_t)(P + shared_rows);
+  }
+}
+
+__global__ void __launch_bounds__(32)
+    permute_scatter_kernel(const int32_t* __restrict__ idx, int64_t P, int E,
+                           const int32_t* __restrict__ chunk_counts,
+                           const int32_t* __restrict__ offsets, int32_t* __restrict__ perm_src,
+                           int32_t* __restrict__ perm_dst) {
+  __shared__ int base[kMaxExperts];
+  const int lane = threadIdx.x;
+  for (int e = lane; e < E; e += 32)
+    base[e] = offsets[e] + chunk_counts[(int64_t)blockIdx.x * E + e];
+  __syncwarp();
+  const int64_t p0 = (int64_t)blockIdx.x * kChunk;
+  const int64_t p1 = min(P, p0 + kChunk);
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int64_t q = p0; q < p1; q += 32) {
+    const int64_t p = q + lane;
+    int e = -2;  // -2: lane past the chunk end
+    if (p < p1) {
+      e = idx[p];
+      if (e < 0 || e >= E) e = -1;  // out of range: skipped (the count kernel raised the flag)
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt);
+    const int leader = __ffs(peers) - 1;
+    int pos = 0;
+    if (e >= 0) pos = base[e] + rank;
+    __syncwarp();
+    if (e >= 0 && lane == leader) base[e] += __popc(peers);
+    __syncwarp();
+    if (e >= 0) {
+      perm_src[pos] = (int32_t)p;
+      perm_dst[p] = pos;
+    } else if (e == -1) {
+      perm_dst[p] = -1;
+    }
+  }
+}
+
+cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int E, int n_shared,
+                           int32_t* chunk_counts, int32_t* counts, int32_t* offsets,
+                           int32_t* perm_src, int32_t* perm_dst, uint32_t* err, cudaStream_t st) {
+  if (E > kMaxExperts - 1) return cudaErrorInvalidValue;
+  const int64_t P = T * k;
+  const int nchunks = permute_chunks(P);
+  if (nchunks > 0) {
+    permute_count_kernel<<<nchunks, 256, 0, st>>>(idx, P, E, chunk_counts, err);
+    count_launch();
+  }
+  permute_scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, nchunks, E, P, T * n_shared, counts,
+                                          offsets);
+  count_launch();
+  if (nchunks > 0) {
+    permute_scatter_kernel<<<nchunks, 32, 0, st>>>(idx, P, E, chunk_counts, offsets, perm_src,
+                                                   perm_dst);
+    count_launch();
+  }
+  return cudaGetLastError();
+}
+
+// dst[r][:] = src[perm_src[r] / k][:]; rows are `row_bytes` long (a multiple of 16).
+__global__ void __launch_bounds__(256)
+    gather_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ perm_src,
+                       int64_t P, int k, int vec_per_row, uint4* __restrict__ dst) {
+  for (int64_t r = blockIdx.x; r < P; r += gridDim.x) {
+    const int p = perm_src[r];
+    uint4* dd = dst + r * vec_per_row;
+    if (p < 0 || p >= P) {  // a row left unset by skipped (out-of-range) pairs
+      for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dd[v] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* s = src + (int64_t)(p / k) * vec_per_row;
+    for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dd[v] = __ldg(s + v);
+  }
+}
+
+cudaError_t launch_gather_rows(const void* src, const int32_t* perm_src, int64_t P, int k,
+                               int width, int elem_bytes, void* dst, int num_sms,
+                               cudaStream_t st) {
+  if (P <= 0) return cudaSuccess;
+  const int64_t row_bytes = (int64_t)width * elem_bytes;
+  if (row_bytes % 16) return cudaErrorInvalidValue;
+  const int64_t blocks = P < (int64_t)num_sms * 16 ? P : (int64_t)num_sms * 16;
+  gather_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(
+      (const uint4*)src, perm_src, P, k, (int)(row_bytes / 16), (uint4*)dst);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -30,3 +30,21 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+
+@pytest.fixture(scope="session")
+def moelib():
+    """The built CUDA library (compiled here if needed; nvcc cross-compiles without a GPU)."""
+    from mixture_experts_ffn_gemm_gb300 import build, binding
+    build.build()
+    return binding.load_library()
+
+
+@pytest.fixture(scope="session")
+def cuda_device():
+    import torch
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from mixture_experts_ffn_gemm_gb300 import build
+    build.build()
+    return torch.device("cuda:0")

@@ -1,0 +1,155 @@
+"""Helpers for the GPU parity tests: run the layer through the C ABI (stage by stage and as one
+moe_forward), and compare with the fp64 oracle on the same seeded inputs.
+
+Tolerances (max |GPU - oracle| over the compared outputs, relative to the oracle's rms):
+  fp32 layer 1e-4, bf16 layer 2e-2.  Routing: the oracle's selection rule fed the GPU's own fp32
+logits must give bit-identical expert indices, except tokens whose k-th / (k+1)-th key margin is
+below 1e-5 (near ties, counted and reported, not compared).
+"""
+from __future__ import annotations
+
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+import oracle
+from oracle import torch_bridge as OB
+from mixture_experts_ffn_gemm_gb300 import binding as B
+
+TOL = {"f32": 1e-4, "bf16": 2e-2}
+NEAR_TIE = 1e-5
+NTHREADS = os.cpu_count() or 4
+
+
+@dataclass
+class GpuRun:
+    logits: torch.Tensor
+    idx: torch.Tensor
+    weight: torch.Tensor
+    counts: torch.Tensor
+    offsets: torch.Tensor
+    perm_src: torch.Tensor
+    perm_dst: torch.Tensor
+    y_perm: torch.Tensor
+    out: torch.Tensor       # stage by stage
+    out_fwd: torch.Tensor   # moe_forward
+    status: int
+    status_fwd: int
+
+
+def run_gpu(layer, flags: int = 0) -> GpuRun:
+    w = layer.w
+    cfg = B.config_for(w, T=layer.x.shape[0], flags=flags)
+    T, E, k, d, de = layer.x.shape[0], w.E, w.k, w.d, w.d_expert
+    dev = layer.x.device
+    act = layer.x.dtype
+    ws = B.alloc_workspace(cfg, dev)
+    logits = torch.full((T, E), float("nan"), dtype=torch.float32, device=dev)
+    idx = torch.full((T, k), -7, dtype=torch.int32, device=dev)
+    wgt = torch.full((T, k), float("nan"), dtype=torch.float32, device=dev)
+    B.moe_router(cfg, layer.x, layer.W_r, layer.b, logits, idx, wgt, ws)
+    counts = torch.full((E + 1,), -7, dtype=torch.int32, device=dev)
+    offsets = torch.full((E + 2,), -7, dtype=torch.int32, device=dev)
+    perm_src = torch.full((T * k,), -7, dtype=torch.int32, device=dev)
+    perm_dst = torch.full((T * k,), -7, dtype=torch.int32, device=dev)
+    B.moe_permute(cfg, idx, counts, offsets, perm_src, perm_dst, ws)
+    y_perm = torch.full((T * k * de + T * w.n_shared * d,), float("nan"), dtype=act, device=dev)
+    B.moe_experts(cfg, layer.x, offsets, perm_src, layer.W13, layer.W2, layer.W13_scale,
+                  layer.W2_scale, layer.Ws13, layer.Ws2, layer.Ws13_scale, layer.Ws2_scale,
+                  layer.W_down, y_perm, ws)
+    out = torch.full((T, d), float("nan"), dtype=act, device=dev)
+    B.moe_combine(cfg, y_perm, perm_dst, wgt, layer.W_up, out, ws)
+    status = B.moe_device_status(ws)
+    out_fwd = torch.full((T, d), float("nan"), dtype=act, device=dev)
+    B.moe_forward(cfg, layer.x, *B.layer_weights(layer), out_fwd, ws)
+    status_fwd = B.moe_device_status(ws)
+    return GpuRun(logits, idx, wgt, counts, offsets, perm_src, perm_dst, y_perm, out, out_fwd,
+                  status, status_fwd)
+
+
+def check_routing(layer, g: GpuRun) -> dict:
+    """Bit-exact indices (near ties excepted) and gates against the oracle's rule on the GPU's
+    logits.  Returns counts for reporting."""
+    cfg = OB.config(layer, layer.x.shape[0])
+    z = g.logits.cpu().numpy()
+    assert np.isfinite(z).all(), "router logits not written"
+    idx_o, gates_o, margin = oracle.route_from_logits(cfg, z, layer.b.cpu().numpy())
+    near = margin < NEAR_TIE
+    idx_g = g.idx.cpu().numpy()
+    mism = (idx_g != idx_o).any(1)
+    assert not (mism & ~near).any(), \
+        f"{int((mism & ~near).sum())} tokens routed differently away from a near tie"
+    wg = g.weight.cpu().numpy().astype(np.float64)
+    ok = ~near
+    assert np.allclose(wg[ok], gates_o[ok], rtol=2e-6, atol=2e-6)
+    assert np.allclose(wg.sum(1), layer.w.gate_scale, rtol=0, atol=2e-5)
+    return {"near_ties": int(near.sum()), "tokens": int(len(near))}
+
+
+def check_permutation(layer, g: GpuRun):
+    """counts / offsets / permutation bit-exact against a stable sort of the expert ids."""
+    T, E, k = layer.x.shape[0], layer.w.E, layer.w.k
+    idx = g.idx.cpu().numpy().reshape(-1)
+    counts = g.counts.cpu().numpy()
+    offsets = g.offsets.cpu().numpy()
+    assert np.array_equal(counts[:E], np.bincount(idx, minlength=E))
+    assert counts[E] == T * layer.w.n_shared
+    assert np.array_equal(offsets, np.concatenate([[0], np.cumsum(counts)]))
+    perm_src = g.perm_src.cpu().numpy()
+    perm_dst = g.perm_dst.cpu().numpy()
+    assert np.array_equal(perm_src, np.argsort(idx, kind="stable"))
+    assert np.array_equal(perm_dst[perm_src], np.arange(T * k))
+
+
+def rel_err(a: np.ndarray, ref: np.ndarray) -> float:
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    return float(np.max(np.abs(a - ref))) / max(rms, 1e-30)
+
+
+def check_outputs(layer, g: GpuRun, rows=None, tol=None) -> dict:
+    """Layer outputs (and the shared expert rows of y_perm) against the oracle on `rows`
+    (all rows by default), near-tie tokens excluded and counted."""
+    T = layer.x.shape[0]
+    tol = tol if tol is not None else TOL[layer.w.act]
+    rows_t = torch.arange(T) if rows is None else torch.as_tensor(rows)
+    ref = OB.forward(layer, rows=rows_t, nthreads=NTHREADS)
+    keep = ref["margin"] >= NEAR_TIE
+    out = g.out.float().cpu().numpy()[rows_t.numpy()]
+    out_fwd = g.out_fwd.float().cpu().numpy()[rows_t.numpy()]
+    assert np.isfinite(out).all() and np.isfinite(out_fwd).all()
+    assert np.array_equal(out, out_fwd), "moe_forward differs from the stage-by-stage path"
+    err = rel_err(out[keep], ref["out"][keep]) if keep.any() else 0.0
+    assert err <= tol, f"max err / rms = {err:.3e} > {tol}"
+    res = {"err": err, "compared": int(keep.sum()), "near_ties": int((~keep).sum())}
+    w = layer.w
+    if w.n_shared:
+        P, de, d = T * w.k, w.d_expert, w.d
+        ysh = g.y_perm[P * de:].view(T, d).float().cpu().numpy()[rows_t.numpy()]
+        e_sh = rel_err(ysh, ref["shared"])
+        assert e_sh <= tol, f"shared expert err {e_sh:.3e}"
+        res["shared_err"] = e_sh
+    return res
+
+
+def check_expert_rows(layer, g: GpuRun, nrows: int = 6, seed: int = 0, tol=None):
+    """Sampled permuted rows of y_perm against one oracle SwiGLU of that row's token and expert
+    (K2 path): isolates the grouped GEMMs from the combine."""
+    w = layer.w
+    if w.d_latent:
+        return
+    tol = tol if tol is not None else TOL[w.act]
+    T, k, d = layer.x.shape[0], w.k, w.d
+    P = T * k
+    rng = np.random.default_rng(seed)
+    perm_src = g.perm_src.cpu().numpy()
+    idx = g.idx.cpu().numpy().reshape(-1)
+    y = g.y_perm[: P * d].view(P, d)
+    for r in rng.choice(P, size=min(nrows, P), replace=False):
+        p = int(perm_src[r])
+        t, e = p // k, int(idx[p])
+        xr = layer.x[t].double().cpu().numpy()
+        ref = oracle.swiglu_row(xr, OB.mat(layer.W13[e]), OB.mat(layer.W2[e]), I=w.I)
+        got = y[r].float().cpu().numpy()
+        assert rel_err(got, ref) <= tol, f"row {r} (token {t}, expert {e})"

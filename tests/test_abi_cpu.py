@@ -1,0 +1,122 @@
+"""The C ABI without a GPU: the library loads, exports every entry point that include/moe.h
+declares, and rejects bad arguments on the host (nothing is launched, no CUDA call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from mixture_experts_ffn_gemm_gb300 import binding as B
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z_]+)\s*\(", src)))
+
+
+def test_every_declared_entry_point_is_exported(moelib):
+    names = _declared()
+    assert "moe_forward" in names and len(names) >= 12
+    for n in names:
+        assert hasattr(moelib, n), n
+    assert set(names) == set(B.EXPORTED)
+
+
+def test_config_struct_matches_header_size(moelib):
+    # int64 + 12 x int32 + 2 x float + int32 = 8 + 48 + 8 + 4 -> 72 with 8-byte alignment
+    assert ctypes.sizeof(B.moe_config_t) == 72
+
+
+def _cfg(**kw):
+    base = dict(T=128, d=7168, E=384, k=8, I=2048, act_dtype=B.torch.bfloat16)
+    base.update(kw)
+    return B.make_config(**base)
+
+
+def test_workspace_size_of_the_workloads(moelib):
+    from mixture_experts_ffn_gemm_gb300 import synthetic as S
+    for name, w in S.WORKLOADS.items():
+        n = B.moe_workspace_size(B.config_for(w))
+        if w.fp8:
+            assert n == 0, "fp8 experts are not in this build yet"
+        else:
+            assert n > 0, name
+    # the prefill workspace holds the permuted activations, h and the expert outputs
+    n = B.moe_workspace_size(B.config_for(S.WORKLOADS["k2_prefill_bf16"]))
+    P = 16384 * 8
+    assert n >= (P * 7168 + (P + 16384) * 2048 + (P + 16384) * 7168) * 2
+
+
+@pytest.mark.parametrize("bad", [dict(k=0), dict(k=385), dict(E=0), dict(d=0), dict(T=-1),
+                                 dict(n_shared=2), dict(I=0)])
+def test_invalid_configs_have_no_workspace(moelib, bad):
+    assert B.moe_workspace_size(_cfg(**bad)) == 0
+
+
+@pytest.mark.parametrize("bad", [dict(d=7000), dict(I=2000), dict(k=33, E=64),
+                                 dict(I_shared=4096)])
+def test_unsupported_shapes_are_refused(moelib, bad):
+    cfg = _cfg(**bad)
+    assert B.moe_workspace_size(cfg) == 0
+    st = moelib.moe_forward(ctypes.byref(cfg), *([0x1000] * 14), 0x1000, 1 << 40, None)
+    assert st in (B.MOE_ERR_UNSUPPORTED, B.MOE_ERR_INVALID_ARG)
+
+
+def test_host_validation_codes(moelib):
+    cfg = _cfg()
+    need = B.moe_workspace_size(cfg)
+    p = 0x10000  # an aligned stand-in address: validation fails before anything dereferences it
+
+    def fwd(c, ws=p, nbytes=need, **override):
+        # x, W_r, b, W13, W2, W13_s, W2_s, Ws13, Ws2, Ws13_s, Ws2_s, W_down, W_up, out
+        names = ["x", "W_r", "b", "W13", "W2", "W13_s", "W2_s", "Ws13", "Ws2", "Ws13_s",
+                 "Ws2_s", "W_down", "W_up", "out"]
+        ptrs = [override.get(n, p) for n in names]
+        return moelib.moe_forward(c, *ptrs, ws, nbytes, None)
+
+    c = ctypes.byref(cfg)
+    assert fwd(c, nbytes=need - 1) == B.MOE_ERR_WORKSPACE
+    assert fwd(c, ws=None) == B.MOE_ERR_WORKSPACE
+    assert fwd(c, x=None) == B.MOE_ERR_INVALID_ARG
+    assert fwd(c, out=None) == B.MOE_ERR_INVALID_ARG
+    assert fwd(c, Ws13=None) == B.MOE_ERR_INVALID_ARG       # n_shared = 1 needs the shared expert
+    assert fwd(c, W13=p + 2) == B.MOE_ERR_INVALID_ARG       # misaligned weight
+    assert fwd(c, ws=p + 8) == B.MOE_ERR_INVALID_ARG        # misaligned workspace
+    cfg.reserved_ = 1
+    assert fwd(c) == B.MOE_ERR_INVALID_ARG
+    assert fwd(None) == B.MOE_ERR_INVALID_ARG
+
+
+def test_stage_entry_points_validate(moelib):
+    cfg = _cfg()
+    need = B.moe_workspace_size(cfg)
+    p = 0x10000
+    assert moelib.moe_router(ctypes.byref(cfg), p, p, p, None, None, p, p, need, None) == \
+        B.MOE_ERR_INVALID_ARG
+    assert moelib.moe_permute(ctypes.byref(cfg), p, p, p, None, p, p, need, None) == \
+        B.MOE_ERR_INVALID_ARG
+    assert moelib.moe_experts(ctypes.byref(cfg), p, p, p, p, None, *([None] * 7), p, p, need,
+                              None) == B.MOE_ERR_INVALID_ARG
+    assert moelib.moe_combine(ctypes.byref(cfg), p, p, p, None, None, p, need, None) == \
+        B.MOE_ERR_INVALID_ARG
+    lat = _cfg(d_latent=3584, latent_norm=1)
+    need_l = B.moe_workspace_size(lat)
+    assert moelib.moe_combine(ctypes.byref(lat), p, p, p, None, p, p, need_l, None) == \
+        B.MOE_ERR_INVALID_ARG  # the latent path needs W_up
+    assert moelib.moe_device_status(None, 0, None) == B.MOE_ERR_WORKSPACE
+    assert moelib.moe_reset_device_status(None, 0, None) == B.MOE_ERR_WORKSPACE
+
+
+def test_status_strings(moelib):
+    for code in range(7):
+        assert B.status_string(code).startswith("MOE_")
+    assert B.status_string(99) == "MOE_ERR_UNKNOWN"
+
+
+def test_missing_library_fails_loudly(monkeypatch, tmp_path):
+    monkeypatch.setattr(B, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(B, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        B.load_library()

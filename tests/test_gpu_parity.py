@@ -1,0 +1,218 @@
+"""GPU parity: the CUDA path through the C ABI against the fp64 oracle, element by element.
+
+Small shapes compare every token; the full workloads (K2 decode 128 tokens, K2 prefill 16384,
+K3 latent 8192) compare all routing decisions and a seeded sample of tokens, in the launch
+configuration the benchmark times.  Ragged token counts, empty experts, one expert taking every
+token, k == E and T == 0 are covered.
+"""
+from dataclasses import replace
+
+import numpy as np
+import pytest
+import torch
+
+from mixture_experts_ffn_gemm_gb300 import binding as B
+from mixture_experts_ffn_gemm_gb300 import synthetic as S
+
+pytestmark = pytest.mark.gpu
+
+ROWS = B.MOE_FLAG_GEMM_ROWS_MAJOR
+SWAP = B.MOE_FLAG_GEMM_SWAP_AB
+
+
+def _lib():
+    import parity_lib as L
+    return L
+
+
+def _layer(w, seed=0):
+    return S.make_layer(w, seed=seed, device="cuda")
+
+
+def _full_check(layer, flags=0, rows=None):
+    L = _lib()
+    g = L.run_gpu(layer, flags)
+    assert g.status == B.MOE_OK and g.status_fwd == B.MOE_OK
+    L.check_permutation(layer, g)
+    r = L.check_routing(layer, g)
+    L.check_expert_rows(layer, g)
+    o = L.check_outputs(layer, g, rows=rows)
+    return {**r, **o}
+
+
+# ---------------------------------------------------------------------------------------------
+# fp32 tiny layer (CUDA-core GEMMs)
+# ---------------------------------------------------------------------------------------------
+
+def test_tiny_fp32_all_tokens(cuda_device):
+    res = _full_check(_layer(S.WORKLOADS["tiny_fp32"]))
+    assert res["err"] <= 1e-4
+
+
+@pytest.mark.parametrize("T", [1, 3, 17, 200])
+def test_tiny_fp32_ragged_tokens(cuda_device, T):
+    _full_check(_layer(S.WORKLOADS["tiny_fp32"].with_tokens(T), seed=T))
+
+
+def test_zero_tokens_is_a_no_op(cuda_device):
+    w = S.WORKLOADS["tiny_fp32"].with_tokens(0)
+    layer = _layer(w)
+    cfg = B.config_for(w)
+    ws = B.alloc_workspace(cfg)
+    out = torch.empty(0, w.d, device="cuda")
+    B.moe_forward(cfg, layer.x, *B.layer_weights(layer), out, ws)
+    assert B.moe_device_status(ws) == B.MOE_OK
+
+
+# ---------------------------------------------------------------------------------------------
+# bf16, tensor-core GEMMs, small widths (many tiles, ragged groups)
+# ---------------------------------------------------------------------------------------------
+
+SMALL_BF16 = replace(S.WORKLOADS["tiny_fp32"], name="small_bf16", act="bf16", T=300)
+
+
+@pytest.mark.parametrize("flags", [ROWS, SWAP], ids=["rows", "swap"])
+def test_bf16_small_all_tokens(cuda_device, flags):
+    _full_check(_layer(SMALL_BF16, seed=1), flags)
+
+
+@pytest.mark.parametrize("flags", [ROWS, SWAP], ids=["rows", "swap"])
+def test_bf16_one_expert_takes_every_token(cuda_device, flags):
+    """k = 1 and a bias that forces expert 5: one group of T rows, every other group empty."""
+    w = replace(SMALL_BF16, k=1, T=333)
+    layer = _layer(w, seed=2)
+    layer.b.zero_()
+    layer.b[5] = 10.0
+    g = _lib().run_gpu(layer, flags)
+    assert (g.idx.cpu() == 5).all()
+    assert int(g.counts[5]) == 333 and int(g.counts[:5].sum() + g.counts[6:16].sum()) == 0
+    _full_check(layer, flags)
+
+
+@pytest.mark.parametrize("flags", [ROWS, SWAP], ids=["rows", "swap"])
+def test_bf16_every_expert_selected(cuda_device, flags):
+    """k == E: every token visits every expert."""
+    w = replace(SMALL_BF16, E=4, k=4, T=130)
+    _full_check(_layer(w, seed=3), flags)
+
+
+def test_bf16_tensor_core_router(cuda_device):
+    """E = 128 with more than 1024 tokens takes the 3 x bf16 split router on the tensor cores."""
+    w = replace(SMALL_BF16, E=128, k=8, T=1100)
+    res = _full_check(_layer(w, seed=4), ROWS | B.MOE_FLAG_ROUTER_TC,
+                      rows=np.arange(0, 1100, 7))
+    assert res["compared"] > 100
+
+
+def test_bf16_router_paths_agree(cuda_device):
+    """The CUDA-core split-K router and the tensor-core split router give the same selections
+    (away from near ties) and logits within fp32 accumulation error."""
+    w = replace(SMALL_BF16, E=128, k=8, T=257, d=512)
+    layer = _layer(w, seed=5)
+    L = _lib()
+    a = L.run_gpu(layer, B.MOE_FLAG_ROUTER_SIMT)
+    b = L.run_gpu(layer, B.MOE_FLAG_ROUTER_TC)
+    za, zb = a.logits.cpu().double(), b.logits.cpu().double()
+    assert float((za - zb).abs().max()) <= 1e-5 * float(za.abs().max())
+    L.check_routing(layer, a)
+    L.check_routing(layer, b)
+
+
+def test_latent_small_all_tokens(cuda_device):
+    w = replace(SMALL_BF16, name="latent_small", d=512, d_latent=256, latent_norm=1, T=300,
+                w_init="fan_in")
+    _full_check(_layer(w, seed=6), ROWS)
+
+
+def test_latent_small_without_norm(cuda_device):
+    w = replace(SMALL_BF16, name="latent_small", d=512, d_latent=256, latent_norm=0, T=70,
+                w_init="fan_in")
+    _full_check(_layer(w, seed=7), SWAP)
+
+
+# ---------------------------------------------------------------------------------------------
+# K2 widths (d = 7168, I = 2048) with fewer experts: every token checked
+# ---------------------------------------------------------------------------------------------
+
+@pytest.mark.parametrize("flags", [ROWS, SWAP], ids=["rows", "swap"])
+def test_k2_widths_32_experts(cuda_device, flags):
+    w = replace(S.WORKLOADS["k2_decode_bf16"], name="k2_e32", E=32, T=72)
+    _full_check(_layer(w, seed=8), flags)
+
+
+# ---------------------------------------------------------------------------------------------
+# Full workloads, in the launch configuration of the benchmark (automatic flags)
+# ---------------------------------------------------------------------------------------------
+
+def _sample(T, n=6, seed=1):
+    return S.subset_rows(T, n, seed=seed).numpy()
+
+
+def _full_workload(name):
+    w = S.WORKLOADS[name]
+    layer = _layer(w)
+    res = _full_check(layer, 0, rows=_sample(w.T))
+    del layer
+    torch.cuda.empty_cache()
+    return res
+
+
+def test_full_k2_decode(cuda_device):
+    res = _full_workload("k2_decode_bf16")
+    print("k2_decode", res)
+
+
+def test_full_k2_prefill(cuda_device):
+    res = _full_workload("k2_prefill_bf16")
+    print("k2_prefill", res)
+
+
+def test_full_k3_latent(cuda_device):
+    res = _full_workload("k3_latent_bf16")
+    print("k3_latent", res)
+
+
+# ---------------------------------------------------------------------------------------------
+# Boundary behaviour on the GPU
+# ---------------------------------------------------------------------------------------------
+
+def test_host_io_entry_point_matches_device_path(cuda_device):
+    w = SMALL_BF16
+    layer = _layer(w, seed=9)
+    cfg = B.config_for(w)
+    ws = B.alloc_workspace(cfg)
+    out_dev = torch.empty(w.T, w.d, dtype=torch.bfloat16, device="cuda")
+    B.moe_forward(cfg, layer.x, *B.layer_weights(layer), out_dev, ws)
+    x_host = layer.x.cpu().pin_memory()
+    out_host = torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory()
+    B.moe_forward_host_io(cfg, x_host, *B.layer_weights(layer), out_host, ws)
+    assert torch.equal(out_host, out_dev.cpu())
+
+
+def test_out_of_range_expert_index_is_flagged(cuda_device):
+    """An index outside [0, E) handed to moe_permute is skipped and reported, not followed."""
+    w = SMALL_BF16
+    cfg = B.config_for(w)
+    ws = B.alloc_workspace(cfg)
+    B.moe_reset_device_status(ws)
+    idx = torch.randint(0, w.E, (w.T, w.k), dtype=torch.int32, device="cuda")
+    idx[7, 1] = w.E + 3
+    counts = torch.empty(w.E + 1, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(w.E + 2, dtype=torch.int32, device="cuda")
+    ps = torch.empty(w.T * w.k, dtype=torch.int32, device="cuda")
+    pd = torch.empty(w.T * w.k, dtype=torch.int32, device="cuda")
+    B.moe_permute(cfg, idx, counts, offsets, ps, pd, ws)
+    assert B.moe_device_status(ws) == B.MOE_ERR_DEVICE_CHECK
+    assert int(counts[: w.E].sum()) == w.T * w.k - 1
+    assert int(pd[7 * w.k + 1]) == -1
+
+
+def test_launch_counter_counts_kernels(cuda_device):
+    w = SMALL_BF16
+    layer = _layer(w, seed=10)
+    B.moe_reset_launch_count()
+    B.forward_layer(layer)
+    torch.cuda.synchronize()
+    n = B.moe_launch_count()
+    # router GEMM + top-k, count + scan + scatter, gather, two grouped GEMMs, combine
+    assert n >= 8
