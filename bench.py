@@ -1,0 +1,417 @@
+#!/usr/bin/env python
+"""Benchmark of the GB300 MoE FFN layer: tokens/s and the roofline fraction.
+
+One step = one pass of the whole layer (router -> permute -> experts -> combine) over one batch of
+synthetic tokens, through the C ABI (moe_forward).  Default workload: the Kimi K2 layer in the
+decode regime (128 tokens, d=7168, 384 experts top-8, expert intermediate 2048, one shared expert,
+bf16 with fp32 router logits).  Other workloads: --workload k2_prefill_bf16 | k3_latent_bf16 |
+tiny_fp32.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Multi-GPU (torchrun, one rank per GPU): every rank runs an independent replica of the layer on its
+own batch (the layer has no exchange step); value = tokens of all ranks / max-over-ranks time.
+`--impl reference` times the fp64 CPU oracle (the only reference there is) on the host cores.
+Prints one JSON line (rank 0).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "MoE-layer tokens/s (d=7168, 384 experts top-8) and % of roofline (HBM or TC)"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="k2_decode_bf16")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=50)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-sample", type=int, default=0,
+                    help="tokens in the oracle's timed sample (0 = automatic)")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg")
+    ap.add_argument("--experts", type=int, default=0,
+                    help="override the routed expert count (small profiling cases)")
+    ap.add_argument("--tokens", type=int, default=0, help="override the token count")
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------------------------
+# helpers
+# ----------------------------------------------------------------------------------------------
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return {k: float(p[k]) for k in FALLBACK_PEAKS if k in p}, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons every 200 ms while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.tmp = None
+
+    def start(self):
+        try:
+            self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except (OSError, ValueError):
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        self.tmp.seek(0)
+        rows = [ln.split(", ") for ln in self.tmp.read().strip().splitlines() if ln.strip()]
+        os.unlink(self.tmp.name)
+        sm, mx, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            if len(r) < 9:
+                continue
+            try:
+                sm.append(float(r[1]))
+                mx.append(float(r[2]))
+                power.append(float(r[3]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, r[5:9]):
+                if v.strip().lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power) if power else None}
+
+
+def touched_bytes(w, idx: np.ndarray) -> dict:
+    """Algorithmic bytes of one layer pass: the expert weights the routing touches (each once),
+    the shared expert, the router weight, the input read and the output write."""
+    touched = np.unique(idx)
+    ab = 4 if w.act == "f32" else 2
+    de = w.d_expert
+    T, P = idx.shape[0], idx.size
+    w13 = 2 * w.I * de * ab
+    w2 = de * w.I * ab
+    sh13 = 2 * w.I_shared * w.d * ab if w.n_shared else 0
+    sh2 = w.d * w.I_shared * ab if w.n_shared else 0
+    lat = 2 * w.d_latent * w.d * ab if w.d_latent else 0
+    rows_sh = T * w.n_shared
+    return {
+        "touched_experts": int(touched.size),
+        # gemm13: W1|W3 of the touched experts + shared, activations in, h out
+        "gemm13": len(touched) * w13 + (0 if w.d_latent else sh13) + P * de * ab
+        + (0 if w.d_latent else T * w.d * ab) + (P + (0 if w.d_latent else rows_sh)) * w.I * ab,
+        # gemm2: W2 of the touched experts + shared, h in, y out
+        "gemm2": len(touched) * w2 + (0 if w.d_latent else sh2)
+        + (P + (0 if w.d_latent else rows_sh)) * (w.I + de) * ab,
+        "layer": len(touched) * (w13 + w2) + sh13 + sh2 + lat + w.E * w.d * 4
+        + 2 * T * w.d * ab,
+    }
+
+
+def flops(w, T: int) -> dict:
+    """Algorithmic FLOPs: the router, the k selected experts and the shared expert per token."""
+    de = w.d_expert
+    P = T * w.k
+    rows13 = P + (0 if w.d_latent else T * w.n_shared)
+    f = {
+        "gemm13": 2 * rows13 * de * 2 * w.I,
+        "gemm2": 2 * rows13 * w.I * de,
+        "router": 2 * T * w.d * w.E,
+    }
+    f["layer"] = (2 * T * w.d * w.E + P * 6 * de * w.I + T * w.n_shared * 6 * w.d * w.I_shared
+                  + (4 * T * w.d * w.d_latent if w.d_latent else 0))
+    return f
+
+
+def prepare_oracle(layer, rows):
+    """Host inputs of the fp64 oracle for `rows` of the layer: the rows, the router and the
+    weights of the experts those rows select (copied once, outside any timed part)."""
+    import oracle
+    from oracle import torch_bridge as OB
+    x, W_r, b = OB.route_inputs(layer, rows)
+    cfg = OB.config(layer, x.data.shape[0])
+    experts = np.unique(oracle.route(cfg, x, W_r, b)["idx"])
+    W13, W2 = OB.expert_mats(layer, experts)
+    sh = (OB.mat(layer.Ws13, layer.Ws13_scale), OB.mat(layer.Ws2, layer.Ws2_scale),
+          OB.mat(layer.W_down), OB.mat(layer.W_up))
+    return cfg, (x, W_r, b, W13, W2, *sh)
+
+
+def time_oracle(prep, nthreads: int) -> float:
+    """Seconds of one oracle pass (as it stands) over the prepared rows."""
+    import oracle
+    cfg, args = prep
+    t0 = time.perf_counter()
+    oracle.forward(cfg, *args, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+# ----------------------------------------------------------------------------------------------
+# reference arm: the oracle on the host cores
+# ----------------------------------------------------------------------------------------------
+def run_reference(args, w, rank: int):
+    if rank != 0:
+        return
+    import torch
+    from mixture_experts_ffn_gemm_gb300 import synthetic as S
+    cores = os.cpu_count() or 1
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    layer = S.make_layer(w, seed=0, device=dev)
+    # a step is a bounded sample of the batch, sized so that the whole run stays within minutes
+    core_s_per_token = time_oracle(prepare_oracle(layer, S.subset_rows(w.T, 1, seed=2)), 1)
+    budget_s = 150.0 / max(1, args.steps + args.warmup)
+    n = args.cpu_sample or int(max(1, min(w.T, budget_s * cores / max(core_s_per_token, 1e-9))))
+    prep = prepare_oracle(layer, S.subset_rows(w.T, n, seed=1))
+    for _ in range(args.warmup):
+        time_oracle(prep, cores)
+    secs = [time_oracle(prep, cores) for _ in range(args.steps)]
+    tps = n / statistics.mean(secs)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tps, "unit": "tokens/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1000.0 * statistics.mean(secs), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.T, "d": w.d, "experts": w.E, "top_k": w.k,
+                   "expert_intermediate": w.I, "d_latent": w.d_latent, "parallelism": "replicas"},
+        "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} of {w.T} tokens (seed 1) per step, fp64 C oracle, "
+                                   f"{cores} threads"},
+        "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------------------------
+# our arm
+# ----------------------------------------------------------------------------------------------
+def run_ours(args, w, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+    from mixture_experts_ffn_gemm_gb300 import binding as B
+    from mixture_experts_ffn_gemm_gb300 import build as BLD
+    from mixture_experts_ffn_gemm_gb300 import synthetic as S
+
+    if rank == 0:
+        BLD.build()
+    if world > 1:
+        dist.barrier()
+    B.load_library()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    layer = S.make_layer(w, seed=0, device=dev)
+    cfg = B.config_for(w)
+    ws = B.alloc_workspace(cfg, dev)
+    out = torch.empty(w.T, w.d, dtype=layer.x.dtype, device=dev)
+    weights = B.layer_weights(layer)
+    stream = torch.cuda.current_stream(dev)
+
+    # the routing of this batch (deterministic; same as inside every timed step)
+    idx = torch.empty(w.T, w.k, dtype=torch.int32, device=dev)
+    wgt = torch.empty(w.T, w.k, dtype=torch.float32, device=dev)
+    B.moe_router(cfg, layer.x, layer.W_r, layer.b, None, idx, wgt, ws)
+    idx_np = idx.cpu().numpy()
+
+    def step():
+        B.moe_forward(cfg, layer.x, *weights, out, ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    status = B.moe_device_status(ws)
+    if status != B.MOE_OK:
+        raise RuntimeError(f"device status after warm-up: {B.status_string(status)}")
+
+    gpu_id = str(getattr(torch.cuda.get_device_properties(dev), "uuid", local_rank))
+    if not gpu_id.startswith("GPU-") and len(gpu_id) > 8:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    B.moe_profile_enable(True)
+    B.moe_profile_read()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = B.moe_launch_count()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    launches = B.moe_launch_count() - launches0
+    ms_total = ev0.elapsed_time(ev1)
+    prof = B.moe_profile_read()
+    B.moe_profile_enable(False)
+    clocks = sampler.stop()
+    status = B.moe_device_status(ws)
+    if status != B.MOE_OK:
+        raise RuntimeError(f"device status after the timed steps: {B.status_string(status)}")
+
+    t_ms = torch.tensor([ms_total], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_ms, op=dist.ReduceOp.MAX)
+    ms_total = float(t_ms.item())
+    ms_step = ms_total / args.steps
+    value = world * w.T / (ms_step / 1000.0)
+
+    # ------------------------------------------------------------- end to end (host buffers)
+    io_bytes = w.T * w.d * layer.x.element_size()
+    e2e = None
+    if not args.no_e2e:
+        x_host = layer.x.cpu().pin_memory()
+        out_host = torch.empty(w.T, w.d, dtype=layer.x.dtype).pin_memory()
+        for _ in range(3):
+            B.moe_forward_host_io(cfg, x_host, *weights, out_host, ws, stream=stream)
+        if world > 1:
+            dist.barrier()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            B.moe_forward_host_io(cfg, x_host, *weights, out_host, ws, stream=stream)
+        e2e_s = time.perf_counter() - t0
+        e2e_t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
+        if world > 1:
+            dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
+        e2e = {"value": world * w.T * args.e2e_steps / float(e2e_t.item()), "unit": "tokens/s",
+               "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
+               "path": "moe_forward_host_io (pinned host x / out, synchronised per step)"}
+
+    if rank != 0:
+        return
+
+    # ------------------------------------------------------------- roofline
+    peaks, peak_src = load_peaks()
+    by = touched_bytes(w, idx_np)
+    fl = flops(w, w.T)
+    kernels = {k: {"ms_per_launch": v[0] / max(v[1], 1), "launches": v[1]} for k, v in prof.items()}
+    dom = max(prof.items(), key=lambda kv: kv[1][0])[0] if prof else None
+    if dom is not None:
+        ms_launch = kernels[dom]["ms_per_launch"]
+        unit_key = "gemm2" if dom.startswith("gemm2") else "gemm13"
+        # the kernel's bound: the larger of its algorithmic time at tensor peak and at HBM peak
+        t_tc_k = fl.get(unit_key, 0) / (peaks["bf16_tflops_sustained"] * 1e12)
+        t_hbm_k = by[unit_key] / (peaks["hbm_gbs"] * 1e9)
+        if t_tc_k > t_hbm_k:
+            achieved = fl.get(unit_key, 0) / (ms_launch / 1000.0) / 1e12
+            peak = peaks["bf16_tflops_sustained"]
+            roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
+                    "unit": "TFLOP/s", "frac": achieved / peak,
+                    "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a "
+                                   f"long step loop)",
+                    "work_per_launch": fl.get(unit_key, 0)}
+        else:
+            achieved = by[unit_key] / (ms_launch / 1000.0) / 1e9
+            peak = peaks["hbm_gbs"]
+            roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
+                    "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs",
+                    "work_per_launch": by[unit_key]}
+        roof["traffic"] = None
+    else:
+        roof = None
+    t_tc = fl["layer"] / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_hbm = by["layer"] / (peaks["hbm_gbs"] * 1e9)
+    layer_roof = {"t_roof_ms": 1000 * max(t_tc, t_hbm), "bound": "tensor" if t_tc > t_hbm else "hbm",
+                  "frac": 1000 * max(t_tc, t_hbm) / ms_step, "algorithmic_bytes": by["layer"],
+                  "algorithmic_flops": fl["layer"], "touched_experts": by["touched_experts"]}
+
+    # ------------------------------------------------------------- CPU baseline (oracle)
+    cpu = None
+    if not args.no_cpu_baseline:
+        cores = os.cpu_count() or 1
+        n = args.cpu_sample or min(w.T, 512 if w.d >= 4096 else w.T)
+        sec = time_oracle(prepare_oracle(layer, S.subset_rows(w.T, n, seed=1)), cores)
+        cpu = {"value": n / sec, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} of {w.T} tokens (seed 1), fp64 C oracle, one pass, {sec:.1f} s"}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if w.act == "f32" else "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.T, "d": w.d, "experts": w.E, "top_k": w.k,
+                   "expert_intermediate": w.I, "shared_intermediate": w.I_shared,
+                   "d_latent": w.d_latent, "router": "fp32 logits",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (expert weights stream from HBM every step; "
+                         "no flush)"},
+        "roofline": roof,
+        "layer_roofline": layer_roof,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": int(launches),
+        "kernels": kernels,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    from mixture_experts_ffn_gemm_gb300 import synthetic as S
+    w = S.WORKLOADS[args.workload]
+    if args.experts or args.tokens:
+        from dataclasses import replace
+        w = replace(w, name=f"{w.name}_E{args.experts or w.E}_T{args.tokens or w.T}",
+                    E=args.experts or w.E, T=args.tokens or w.T)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    try:
+        run_ours(args, w, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -31,6 +31,8 @@
  *     holds the weight output by input"), i.e. K-contiguous.
  *   - Every pointer must be 16-byte aligned; every row pitch is the row's width (no padding).
  *   - Errors are return codes; nothing is launched when host validation fails.
+ *   - T == 0 is valid: once the configuration and workspace pass validation every entry point
+ *     returns MOE_OK without touching any other pointer (empty tensors may be NULL).
  *   - The functions hold no state between calls other than cached kernel attributes and the
  *     driver entry point of cuTensorMapEncodeTiled; they are safe to call from several threads on
  *     distinct workspaces.
@@ -130,8 +132,9 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, int32
  *   Ws13      [2 I_shared][d], Ws2 [d][I_shared] (+ Ws13_scale, Ws2_scale for fp8); NULL when
  *             n_shared == 0
  *   W_down    [d_latent][d] act_dtype, K3 only (else NULL)
- *   y_perm    out, act_dtype: [T*k][d_e] un-weighted expert outputs in permuted row order,
- *             followed by [T*n_shared][d] shared-expert outputs in token order.
+ *   y_perm    out, fp32: [T*k][d_e] un-weighted expert outputs in permuted row order, followed
+ *             by [T*n_shared][d] shared-expert outputs in token order (kept in fp32 so that the
+ *             gate-weighted sum in moe_combine rounds only once).
  * fp8 (w_dtype MOE_FP8_E4M3): the activations entering both GEMMs are quantised per token per
  * quant_block channels to e4m3 with scale = amax/448 (1 for an all-zero group), accumulation in
  * fp32. */
@@ -189,6 +192,16 @@ const char* moe_status_string(moe_status_t status);
  * counter for benchmarks), and its reset. */
 uint64_t moe_launch_count(void);
 void moe_reset_launch_count(void);
+
+/* Launch profiler (the trace of the layer's kernels; off by default).  While enabled, every kernel
+ * this library enqueues is bracketed by a CUDA event pair recorded on its own stream (events are
+ * created once and reused; no device memory is allocated).  moe_profile_read() synchronises on
+ * the recorded events, sums the elapsed time and the launch count per kernel name, writes at most
+ * max_entries entries (names as NUL-terminated strings in slots of name_len bytes) and clears the
+ * totals; it returns the number of entries written. */
+moe_status_t moe_profile_enable(int on);
+int moe_profile_read(int max_entries, char* names, size_t name_len, double* total_ms,
+                     uint64_t* launches);
 
 #ifdef __cplusplus
 }

@@ -25,7 +25,8 @@ MOE_FLAG_ROUTER_SIMT, MOE_FLAG_ROUTER_TC = 0x4, 0x8
 
 EXPORTED = ("moe_workspace_size", "moe_router", "moe_permute", "moe_experts", "moe_combine",
             "moe_forward", "moe_forward_host_io", "moe_reset_device_status", "moe_device_status",
-            "moe_status_string", "moe_launch_count", "moe_reset_launch_count")
+            "moe_status_string", "moe_launch_count", "moe_reset_launch_count",
+            "moe_profile_enable", "moe_profile_read")
 
 
 class MoEError(RuntimeError):
@@ -85,6 +86,10 @@ def load_library():
             lib.moe_launch_count.argtypes = []
             lib.moe_reset_launch_count.restype = None
             lib.moe_reset_launch_count.argtypes = []
+            lib.moe_profile_enable.restype = S
+            lib.moe_profile_enable.argtypes = [S]
+            lib.moe_profile_read.restype = S
+            lib.moe_profile_read.argtypes = [S, P, ctypes.c_size_t, P, P]
             _lib = lib
     return _lib
 
@@ -230,6 +235,26 @@ def moe_launch_count() -> int:
 
 def moe_reset_launch_count():
     load_library().moe_reset_launch_count()
+
+
+def moe_profile_enable(on: bool = True):
+    _check(load_library().moe_profile_enable(1 if on else 0), "moe_profile_enable")
+
+
+def moe_profile_read(max_entries: int = 64) -> dict:
+    """{kernel name: (total ms, launches)} since the last read (synchronises on the events)."""
+    name_len = 48
+    names = ctypes.create_string_buffer(max_entries * name_len)
+    ms = (ctypes.c_double * max_entries)()
+    n_l = (ctypes.c_uint64 * max_entries)()
+    n = load_library().moe_profile_read(max_entries, ctypes.cast(names, ctypes.c_void_p),
+                                        name_len, ctypes.cast(ms, ctypes.c_void_p),
+                                        ctypes.cast(n_l, ctypes.c_void_p))
+    out = {}
+    for i in range(n):
+        nm = names.raw[i * name_len:(i + 1) * name_len].split(b"\0", 1)[0].decode()
+        out[nm] = (float(ms[i]), int(n_l[i]))
+    return out
 
 
 # ----------------------------------------------------------------------------------------------

@@ -164,6 +164,7 @@ cudaError_t launch_gemm_simt(const GroupedGemm& g, int num_sms, cudaStream_t st)
   p.err = g.err;
   dim3 grid(num_sms * 4, g.k_splits);
   const bool swiglu = g.epi == EPI_SWIGLU;
+  LaunchScope ls(g.label, st);
   if (g.act_dtype == MOE_F32 && g.w_dtype == MOE_F32) {
     if (swiglu)
       moe_gemm_simt_kernel<float, float, true><<<grid, kSimtThreads, 0, st>>>(p);
@@ -182,7 +183,6 @@ cudaError_t launch_gemm_simt(const GroupedGemm& g, int num_sms, cudaStream_t st)
   } else {
     return cudaErrorInvalidValue;
   }
-  count_launch();
   return cudaGetLastError();
 }
 

@@ -51,7 +51,7 @@ struct TcParams {
   void* out;
   int64_t ldo;
   int32_t out_f32;
-  const __nv_bfloat16* addend;
+  const float* addend;  // EPI_STORE_ADD: fp32 [rows][ld_add]
   int64_t ld_add;
   uint32_t* err;
 };
@@ -298,18 +298,15 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
 #pragma unroll
                 for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
                 if (kEpi == EPI_STORE_ADD) {
-                  const uint4* a4 =
-                      reinterpret_cast<const uint4*>(p.addend + orow * p.ld_add + col0 + c);
+                  const float4* a4 =
+                      reinterpret_cast<const float4*>(p.addend + orow * p.ld_add + col0 + c);
 #pragma unroll
-                  for (int h = 0; h < 2; ++h) {
-                    const uint4 raw = __ldg(a4 + h);
-                    const __nv_bfloat162* b2 = reinterpret_cast<const __nv_bfloat162*>(&raw);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                      const float2 af = __bfloat1622float2(b2[i]);
-                      f[8 * h + 2 * i] += af.x;
-                      f[8 * h + 2 * i + 1] += af.y;
-                    }
+                  for (int h = 0; h < 4; ++h) {
+                    const float4 av = __ldg(a4 + h);
+                    f[4 * h] += av.x;
+                    f[4 * h + 1] += av.y;
+                    f[4 * h + 2] += av.z;
+                    f[4 * h + 3] += av.w;
                   }
                 }
                 uint32_t pk[8];
@@ -340,7 +337,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
               if (p.out_f32) {
                 ((float*)p.out)[orow * p.ldo + feat] = v;
               } else {
-                if (kEpi == EPI_STORE_ADD) v += __bfloat162float(p.addend[orow * p.ld_add + feat]);
+                if (kEpi == EPI_STORE_ADD) v += p.addend[orow * p.ld_add + feat];
                 ((__nv_bfloat16*)p.out)[orow * p.ldo + feat] = __float2bfloat16_rn(v);
               }
             }
@@ -401,7 +398,7 @@ static bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_
 }
 
 template <bool kSwap, int kBN, int kEpi>
-static cudaError_t launch_variant(const TcParams& p, int grid, cudaStream_t st) {
+static cudaError_t launch_variant(const TcParams& p, int grid, cudaStream_t st, const char* label) {
   using S = TcShape<kSwap, kBN, kEpi>;
   auto kern = moe_gemm_tc_kernel<kSwap, kBN, kEpi>;
   static int attr_set_device = -1;  // the attribute is per device; refreshed when it changes
@@ -413,8 +410,8 @@ static cudaError_t launch_variant(const TcParams& p, int grid, cudaStream_t st) 
     if (e != cudaSuccess) return e;
     attr_set_device = dev;
   }
+  LaunchScope ls(label, st);
   kern<<<grid, kTcThreads, S::SMEM, st>>>(p);
-  count_launch();
   return cudaGetLastError();
 }
 
@@ -432,7 +429,7 @@ bool gemm_tc_supported(const GroupedGemm& g, int swap) {
       return false;
   }
   if (g.ldo % 8) return false;
-  if (g.epi == EPI_STORE_ADD && (!g.addend || g.ld_add % 8 || g.out_dtype != MOE_BF16))
+  if (g.epi == EPI_STORE_ADD && (!g.addend || g.ld_add % 4 || g.out_dtype != MOE_BF16))
     return false;
   return true;
 }
@@ -475,19 +472,19 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
   p.out = g.out;
   p.ldo = g.ldo;
   p.out_f32 = g.out_dtype == MOE_F32;
-  p.addend = (const __nv_bfloat16*)g.addend;
+  p.addend = (const float*)g.addend;
   p.ld_add = g.ld_add;
   p.err = g.err;
   const int grid = num_sms;
   if (!swap) {
-    if (g.epi == EPI_SWIGLU) return launch_variant<false, 256, EPI_SWIGLU>(p, grid, st);
-    if (f32_router) return launch_variant<false, 128, EPI_STORE>(p, grid, st);
-    if (g.epi == EPI_STORE) return launch_variant<false, 256, EPI_STORE>(p, grid, st);
-    return launch_variant<false, 256, EPI_STORE_ADD>(p, grid, st);
+    if (g.epi == EPI_SWIGLU) return launch_variant<false, 256, EPI_SWIGLU>(p, grid, st, g.label);
+    if (f32_router) return launch_variant<false, 128, EPI_STORE>(p, grid, st, g.label);
+    if (g.epi == EPI_STORE) return launch_variant<false, 256, EPI_STORE>(p, grid, st, g.label);
+    return launch_variant<false, 256, EPI_STORE_ADD>(p, grid, st, g.label);
   }
-  if (g.epi == EPI_SWIGLU) return launch_variant<true, 32, EPI_SWIGLU>(p, grid, st);
-  if (g.epi == EPI_STORE) return launch_variant<true, 32, EPI_STORE>(p, grid, st);
-  return launch_variant<true, 32, EPI_STORE_ADD>(p, grid, st);
+  if (g.epi == EPI_SWIGLU) return launch_variant<true, 32, EPI_SWIGLU>(p, grid, st, g.label);
+  if (g.epi == EPI_STORE) return launch_variant<true, 32, EPI_STORE>(p, grid, st, g.label);
+  return launch_variant<true, 32, EPI_STORE_ADD>(p, grid, st, g.label);
 }
 
 }  // namespace moe

@@ -52,12 +52,13 @@ struct GroupedGemm {
   void* out = nullptr;
   int64_t ldo = 0;
   int out_dtype = MOE_BF16;
-  const void* addend = nullptr;  // EPI_STORE_ADD: bf16 [rows][ld_add], indexed like out
+  const void* addend = nullptr;  // EPI_STORE_ADD: fp32 [rows][ld_add], indexed like out
   int64_t ld_add = 0;
   // split-K (SIMT router only): out slice s at out + s * split_stride elements
   int k_splits = 1;
   int64_t split_stride = 0;
   uint32_t* err = nullptr;
+  const char* label = "gemm";  // kernel name for the launch profiler
 };
 
 // Tensor-core grouped GEMM (tcgen05 + TMA), bf16 operands, fp32 accumulation in TMEM.
@@ -88,16 +89,29 @@ cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int E, int n_sh
 cudaError_t launch_gather_rows(const void* src, const int32_t* perm_src, int64_t P, int k,
                                int width, int elem_bytes, void* dst, int num_sms, cudaStream_t st);
 
-// Combine: out[t] = sum_j w[t,j] * y[perm_dst[t*k+j]] + y_shared[t]  (fp32 sum, one rounding).
+// Combine: out[t] = sum_j w[t,j] * y[perm_dst[t*k+j]] + y_shared[t]; y fp32, fp32 sum, one
+// rounding to act_dtype.
 cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* y_shared,
                            const int32_t* perm_dst, const float* weight, int64_t T, int k, int d,
                            void* out, int num_sms, cudaStream_t st);
-// K3: u_hat[t] = RMSNorm?( sum_j w[t,j] * y[perm_dst[t*k+j]] ) in bf16, width L.
+// K3: u_hat[t] = RMSNorm?( sum_j w[t,j] * y[perm_dst[t*k+j]] ) in bf16, width L, y fp32.
 cudaError_t launch_latent_combine(const void* y_perm, const int32_t* perm_dst,
                                   const float* weight, int64_t T, int k, int L, int norm,
                                   float eps, void* u_hat, int num_sms, cudaStream_t st);
 
-// Launch counter (per host thread).
-void count_launch(int n = 1);
+// Brackets one kernel launch: counts it (per host thread) and, while profiling is enabled
+// (moe_profile_enable), records a CUDA event pair around it on the launch stream.
+class LaunchScope {
+ public:
+  LaunchScope(const char* name, cudaStream_t st);
+  ~LaunchScope();
+  LaunchScope(const LaunchScope&) = delete;
+  LaunchScope& operator=(const LaunchScope&) = delete;
+
+ private:
+  const char* name_;
+  cudaStream_t st_;
+  cudaEvent_t start_ = nullptr;
+};
 
 }  // namespace moe

@@ -1,13 +1,67 @@
 // moe_api.cu -- the C ABI of include/moe.h: host validation, workspace layout and the order of
 // kernel launches for each entry point.  No allocation, no host synchronisation on the layer path.
 #include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
 
 #include "internal.h"
 
 namespace moe {
 
+// ---------------------------------------------------------------------------------------------
+// Launch counter and launch profiler
+// ---------------------------------------------------------------------------------------------
 static thread_local uint64_t g_launches = 0;
-void count_launch(int n) { g_launches += (uint64_t)n; }
+
+struct ProfRecord {
+  const char* name;
+  cudaEvent_t start, stop;
+};
+struct ProfTotal {
+  std::string name;
+  double ms;
+  uint64_t launches;
+};
+static std::mutex g_prof_mu;
+static bool g_prof_on = false;
+static std::vector<ProfRecord> g_prof_pending;
+static std::vector<cudaEvent_t> g_prof_pool;
+static std::vector<ProfTotal> g_prof_totals;
+
+static cudaEvent_t prof_event() {  // caller holds g_prof_mu
+  if (!g_prof_pool.empty()) {
+    cudaEvent_t e = g_prof_pool.back();
+    g_prof_pool.pop_back();
+    return e;
+  }
+  cudaEvent_t e = nullptr;
+  if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+  return e;
+}
+
+LaunchScope::LaunchScope(const char* name, cudaStream_t st) : name_(name), st_(st) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  if (!g_prof_on) return;
+  start_ = prof_event();
+  if (start_ && cudaEventRecord(start_, st_) != cudaSuccess) {
+    g_prof_pool.push_back(start_);
+    start_ = nullptr;
+  }
+}
+
+LaunchScope::~LaunchScope() {
+  ++g_launches;
+  if (!start_) return;
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  cudaEvent_t stop = prof_event();
+  if (stop && cudaEventRecord(stop, st_) == cudaSuccess) {
+    g_prof_pending.push_back({name_, start_, stop});
+  } else {
+    g_prof_pool.push_back(start_);
+    if (stop) g_prof_pool.push_back(stop);
+  }
+}
 
 static int num_sms() {
   static int cache[64] = {0};
@@ -120,7 +174,7 @@ static Layout make_layout(const moe_config_t* c, const Plan& pl) {
   L.x_lat = take(pl.latent ? (size_t)T * c->d_latent * ab : 0);
   L.x_perm = take((size_t)P * pl.de * ab);
   L.h = take((size_t)(P + shared_rows) * I * ab);
-  L.y_perm = take(((size_t)P * pl.de + (size_t)shared_rows * d) * ab);
+  L.y_perm = take(((size_t)P * pl.de + (size_t)shared_rows * d) * 4);  // fp32 expert outputs
   L.u_hat = take(pl.latent ? (size_t)T * c->d_latent * 2 : 0);
   L.x_io = take((size_t)T * d * ab);
   L.out_io = take((size_t)T * d * ab);
@@ -161,6 +215,13 @@ static moe_status_t begin(Ctx& x, const moe_config_t* c, void* ws, size_t ws_byt
   return MOE_OK;
 }
 
+// T == 0: every entry point is a no-op once the configuration and workspace are valid (empty
+// tensors may come with NULL data pointers).
+#define MOE_RETURN_IF_EMPTY(cfg) \
+  do {                           \
+    if ((cfg)->T == 0) return MOE_OK; \
+  } while (0)
+
 // First CUDA runtime calls of an entry point, made only after every host-side check passed.
 static void ready(Ctx& x) {
   x.sms = num_sms();
@@ -194,6 +255,7 @@ static moe_status_t run_router(Ctx& x, const void* xin, const float* W_r, const 
     g.ldo = c->E;
     g.out_dtype = MOE_F32;
     g.err = x.err;
+    g.label = "router_gemm_tc";
     e = launch_gemm_tc(g, 0, x.sms, x.st);
     if (e != cudaSuccess) return from_cuda(e);
     e = launch_router_topk(z, 1, 0, c->T, c->E, c->k, b, c->gate_scale, nullptr, idx, weight,
@@ -219,6 +281,7 @@ static moe_status_t run_router(Ctx& x, const void* xin, const float* W_r, const 
   g.k_splits = x.pl.router_splits;
   g.split_stride = c->T * c->E;
   g.err = x.err;
+  g.label = "router_gemm_simt";
   e = launch_gemm_simt(g, x.sms, x.st);
   if (e != cudaSuccess) return from_cuda(e);
   e = launch_router_topk(zp, x.pl.router_splits, c->T * c->E, c->T, c->E, c->k, b,
@@ -270,6 +333,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.ldo = de;
     g.out_dtype = c->act_dtype;
     g.err = x.err;
+    g.label = "down_proj";
     e = launch_gemm_tc(g, 0, x.sms, x.st);
     if (e != cudaSuccess) return from_cuda(e);
     route_src = x_lat;
@@ -307,6 +371,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.ldo = I;
     g.out_dtype = c->act_dtype;
     g.err = x.err;
+    g.label = "gemm13_swiglu";
     e = gemm(x, g);
     if (e != cudaSuccess) return from_cuda(e);
   }
@@ -336,14 +401,15 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.act_dtype = g.w_dtype = c->act_dtype;
     g.out = y_perm;
     g.ldo = de;
-    g.out_dtype = c->act_dtype;
+    g.out_dtype = MOE_F32;
     g.err = x.err;
+    g.label = "gemm2";
     e = gemm(x, g);
     if (e != cudaSuccess) return from_cuda(e);
   }
   if (c->n_shared && x.pl.latent) {  // shared expert on the full-width input
     void* h_sh = static_cast<uint8_t*>(h) + (size_t)P * I * ab;
-    void* y_sh = static_cast<uint8_t*>(y_perm) + (size_t)P * de * ab;
+    void* y_sh = static_cast<uint8_t*>(y_perm) + (size_t)P * de * 4;
     GroupedGemm g;
     g.act_d = xin;
     g.act_d_rows = T;
@@ -360,6 +426,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.ldo = I;
     g.out_dtype = c->act_dtype;
     g.err = x.err;
+    g.label = "shared_gemm13_swiglu";
     e = launch_gemm_tc(g, 0, x.sms, x.st);
     if (e != cudaSuccess) return from_cuda(e);
     GroupedGemm g2;
@@ -375,8 +442,9 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g2.act_dtype = g2.w_dtype = c->act_dtype;
     g2.out = y_sh;
     g2.ldo = d;
-    g2.out_dtype = c->act_dtype;
+    g2.out_dtype = MOE_F32;
     g2.err = x.err;
+    g2.label = "shared_gemm2";
     e = launch_gemm_tc(g2, 0, x.sms, x.st);
     if (e != cudaSuccess) return from_cuda(e);
   }
@@ -388,10 +456,9 @@ static moe_status_t run_combine(Ctx& x, const void* y_perm, const int32_t* perm_
   const moe_config_t* c = x.c;
   if (c->T == 0) return MOE_OK;
   const int64_t T = c->T, P = T * c->k;
-  const size_t ab = dtype_bytes(c->act_dtype);
   const int de = x.pl.de, d = c->d;
   const void* y_sh =
-      c->n_shared ? static_cast<const uint8_t*>(y_perm) + (size_t)P * de * ab : nullptr;
+      c->n_shared ? static_cast<const uint8_t*>(y_perm) + (size_t)P * de * 4 : nullptr;
   if (!x.pl.latent)
     return from_cuda(
         launch_combine(c->act_dtype, y_perm, y_sh, perm_dst, weight, T, c->k, d, out, x.sms, x.st));
@@ -416,6 +483,7 @@ static moe_status_t run_combine(Ctx& x, const void* y_perm, const int32_t* perm_
   g.addend = y_sh;
   g.ld_add = d;
   g.err = x.err;
+  g.label = "up_proj";
   return from_cuda(launch_gemm_tc(g, 0, x.sms, x.st));
 }
 
@@ -439,6 +507,7 @@ moe_status_t moe_router(const moe_config_t* cfg, const void* x, const float* W_r
   Ctx c;
   moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
   if (s != MOE_OK) return s;
+  MOE_RETURN_IF_EMPTY(cfg);
   if (!x || !W_r || !b || !topk_idx || !topk_weight) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(W_r) || (logits && !aligned16(logits)))
     return MOE_ERR_INVALID_ARG;
@@ -452,6 +521,7 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, int32
   Ctx c;
   moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
   if (s != MOE_OK) return s;
+  MOE_RETURN_IF_EMPTY(cfg);
   if (!topk_idx || !counts || !offsets || !perm_src || !perm_dst) return MOE_ERR_INVALID_ARG;
   ready(c);
   return run_permute(c, topk_idx, counts, offsets, perm_src, perm_dst);
@@ -470,6 +540,7 @@ moe_status_t moe_experts(const moe_config_t* cfg, const void* x, const int32_t* 
   Ctx c;
   moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
   if (s != MOE_OK) return s;
+  MOE_RETURN_IF_EMPTY(cfg);
   if (!x || !offsets || !perm_src || !W13 || !W2 || !y_perm) return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared && (!Ws13 || !Ws2)) return MOE_ERR_INVALID_ARG;
   if (cfg->d_latent > 0 && !W_down) return MOE_ERR_INVALID_ARG;
@@ -486,6 +557,7 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int3
   Ctx c;
   moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
   if (s != MOE_OK) return s;
+  MOE_RETURN_IF_EMPTY(cfg);
   if (!y_perm || !perm_dst || !topk_weight || !out) return MOE_ERR_INVALID_ARG;
   if (cfg->d_latent > 0 && !W_up) return MOE_ERR_INVALID_ARG;
   if (!aligned16(y_perm) || !aligned16(out) || (W_up && !aligned16(W_up)))
@@ -506,6 +578,7 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const float* W_
   Ctx c;
   moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
   if (s != MOE_OK) return s;
+  MOE_RETURN_IF_EMPTY(cfg);
   if (!x || !W_r || !b || !W13 || !W2 || !out) return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared && (!Ws13 || !Ws2)) return MOE_ERR_INVALID_ARG;
   if (cfg->d_latent > 0 && (!W_down || !W_up)) return MOE_ERR_INVALID_ARG;
@@ -538,6 +611,7 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
   Ctx c;
   moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
   if (s != MOE_OK) return s;
+  MOE_RETURN_IF_EMPTY(cfg);
   if (!x_host || !out_host) return MOE_ERR_INVALID_ARG;
   if (!W_r || !b || !W13 || !W2) return MOE_ERR_INVALID_ARG;
   ready(c);
@@ -587,5 +661,47 @@ const char* moe_status_string(moe_status_t s) {
 
 uint64_t moe_launch_count(void) { return g_launches; }
 void moe_reset_launch_count(void) { g_launches = 0; }
+
+moe_status_t moe_profile_enable(int on) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  g_prof_on = on != 0;
+  return MOE_OK;
+}
+
+int moe_profile_read(int max_entries, char* names, size_t name_len, double* total_ms,
+                     uint64_t* launches) {
+  std::lock_guard<std::mutex> lk(g_prof_mu);
+  for (const ProfRecord& r : g_prof_pending) {
+    float ms = 0.0f;
+    if (cudaEventSynchronize(r.stop) == cudaSuccess &&
+        cudaEventElapsedTime(&ms, r.start, r.stop) == cudaSuccess) {
+      bool found = false;
+      for (ProfTotal& t : g_prof_totals)
+        if (t.name == r.name) {
+          t.ms += ms;
+          ++t.launches;
+          found = true;
+          break;
+        }
+      if (!found) g_prof_totals.push_back({r.name, (double)ms, 1});
+    }
+    g_prof_pool.push_back(r.start);
+    g_prof_pool.push_back(r.stop);
+  }
+  g_prof_pending.clear();
+  int n = 0;
+  for (const ProfTotal& t : g_prof_totals) {
+    if (n >= max_entries) break;
+    if (names && name_len > 0) {
+      std::strncpy(names + (size_t)n * name_len, t.name.c_str(), name_len - 1);
+      names[(size_t)n * name_len + name_len - 1] = '\0';
+    }
+    if (total_ms) total_ms[n] = t.ms;
+    if (launches) launches[n] = t.launches;
+    ++n;
+  }
+  g_prof_totals.clear();
+  return n;
+}
 
 }  // extern "C"

@@ -117,16 +117,18 @@ cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int E, int n_sh
   const int64_t P = T * k;
   const int nchunks = permute_chunks(P);
   if (nchunks > 0) {
+    LaunchScope ls("permute_count", st);
     permute_count_kernel<<<nchunks, 256, 0, st>>>(idx, P, E, chunk_counts, err);
-    count_launch();
   }
-  permute_scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, nchunks, E, P, T * n_shared, counts,
-                                          offsets);
-  count_launch();
+  {
+    LaunchScope ls("permute_scan", st);
+    permute_scan_kernel<<<1, 1024, 0, st>>>(chunk_counts, nchunks, E, P, T * n_shared, counts,
+                                            offsets);
+  }
   if (nchunks > 0) {
+    LaunchScope ls("permute_scatter", st);
     permute_scatter_kernel<<<nchunks, 32, 0, st>>>(idx, P, E, chunk_counts, offsets, perm_src,
                                                    perm_dst);
-    count_launch();
   }
   return cudaGetLastError();
 }
@@ -154,9 +156,9 @@ cudaError_t launch_gather_rows(const void* src, const int32_t* perm_src, int64_t
   const int64_t row_bytes = (int64_t)width * elem_bytes;
   if (row_bytes % 16) return cudaErrorInvalidValue;
   const int64_t blocks = P < (int64_t)num_sms * 16 ? P : (int64_t)num_sms * 16;
+  LaunchScope ls("gather_rows", st);
   gather_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(
       (const uint4*)src, perm_src, P, k, (int)(row_bytes / 16), (uint4*)dst);
-  count_launch();
   return cudaGetLastError();
 }
 

@@ -93,9 +93,9 @@ cudaError_t launch_router_topk(const float* partial, int S, int64_t split_stride
   if (T <= 0) return cudaSuccess;
   if (E > 32 * kMaxExpertsPerLane || k > 32 || k > E) return cudaErrorInvalidValue;
   const int64_t blocks = (T + kTopkWarps - 1) / kTopkWarps;
+  LaunchScope ls("router_topk", st);
   router_topk_kernel<<<(unsigned)blocks, kTopkWarps * 32, 0, st>>>(
       partial, S, split_stride, T, E, k, b, gate_scale, logits_out, idx, weight);
-  count_launch();
   return cudaGetLastError();
 }
 
@@ -127,8 +127,8 @@ cudaError_t launch_split_router_weights(const float* W_r, int E, int d, __nv_bfl
                                         cudaStream_t st) {
   const int64_t n = (int64_t)E * d;
   const int blocks = (int)((n + 255) / 256 < 4096 ? (n + 255) / 256 : 4096);
+  LaunchScope ls("split_router_weights", st);
   split_router_weights_kernel<<<blocks, 256, 0, st>>>(W_r, E, d, out);
-  count_launch();
   return cudaGetLastError();
 }
 

@@ -1,10 +1,13 @@
 """Helpers for the GPU parity tests: run the layer through the C ABI (stage by stage and as one
 moe_forward), and compare with the fp64 oracle on the same seeded inputs.
 
-Tolerances (max |GPU - oracle| over the compared outputs, relative to the oracle's rms):
-  fp32 layer 1e-4, bf16 layer 2e-2.  Routing: the oracle's selection rule fed the GPU's own fp32
-logits must give bit-identical expert indices, except tokens whose k-th / (k+1)-th key margin is
-below 1e-5 (near ties, counted and reported, not compared).
+Tolerances: max |GPU - oracle| over the compared outputs <= tol * rms(oracle), with tol 1e-4 for
+the fp32 layer and 2e-2 for the bf16 layer, against the unrounded fp64 oracle; in addition the rms
+of the error must stay below 1e-5 (fp32) / 5e-3 (bf16) of rms(oracle), which catches a systematic
+error the max bound could hide.
+Routing: the oracle's selection rule fed the GPU's own fp32 logits must give bit-identical expert
+indices, except tokens whose k-th / (k+1)-th key margin is below 1e-5 (near ties, counted and
+reported, not compared).
 """
 from __future__ import annotations
 
@@ -19,6 +22,7 @@ from oracle import torch_bridge as OB
 from mixture_experts_ffn_gemm_gb300 import binding as B
 
 TOL = {"f32": 1e-4, "bf16": 2e-2}
+RMS_TOL = {"f32": 1e-5, "bf16": 5e-3}
 NEAR_TIE = 1e-5
 NTHREADS = os.cpu_count() or 4
 
@@ -55,7 +59,8 @@ def run_gpu(layer, flags: int = 0) -> GpuRun:
     perm_src = torch.full((T * k,), -7, dtype=torch.int32, device=dev)
     perm_dst = torch.full((T * k,), -7, dtype=torch.int32, device=dev)
     B.moe_permute(cfg, idx, counts, offsets, perm_src, perm_dst, ws)
-    y_perm = torch.full((T * k * de + T * w.n_shared * d,), float("nan"), dtype=act, device=dev)
+    y_perm = torch.full((T * k * de + T * w.n_shared * d,), float("nan"), dtype=torch.float32,
+                        device=dev)
     B.moe_experts(cfg, layer.x, offsets, perm_src, layer.W13, layer.W2, layer.W13_scale,
                   layer.W2_scale, layer.Ws13, layer.Ws2, layer.Ws13_scale, layer.Ws2_scale,
                   layer.W_down, y_perm, ws)
@@ -108,11 +113,34 @@ def rel_err(a: np.ndarray, ref: np.ndarray) -> float:
     return float(np.max(np.abs(a - ref))) / max(rms, 1e-30)
 
 
-def check_outputs(layer, g: GpuRun, rows=None, tol=None) -> dict:
+def rms_err(a: np.ndarray, ref: np.ndarray) -> float:
+    rms = float(np.sqrt(np.mean(ref * ref)))
+    return float(np.sqrt(np.mean((a - ref) ** 2))) / max(rms, 1e-30)
+
+
+def compare(got: np.ndarray, ref: np.ndarray, act: str, tol=None,
+            output_rounding: bool = False) -> dict:
+    """max |got - ref| / rms(ref) <= tol and rms(got - ref) / rms(ref) <= RMS_TOL.
+
+    output_rounding: subtract the result's own bf16 rounding, 2^-8 |ref| per element, before the
+    max bound (used only where every output is one gate-amplified expert, k = 1, so that no
+    bf16 implementation can meet the plain bound; the derivation is in the test)."""
+    tol = tol if tol is not None else TOL[act]
+    if output_rounding and act == "bf16":
+        rms = float(np.sqrt(np.mean(ref * ref)))
+        e_max = float(np.max(np.abs(got - ref) - 2.0 ** -8 * np.abs(ref))) / max(rms, 1e-30)
+    else:
+        e_max = rel_err(got, ref)
+    e_rms = rms_err(got, ref)
+    assert e_max <= tol, f"max err / rms = {e_max:.3e} > {tol}"
+    assert e_rms <= RMS_TOL[act], f"rms err = {e_rms:.3e} > {RMS_TOL[act]}"
+    return {"err": e_max, "rms_err": e_rms}
+
+
+def check_outputs(layer, g: GpuRun, rows=None, tol=None, output_rounding=False) -> dict:
     """Layer outputs (and the shared expert rows of y_perm) against the oracle on `rows`
     (all rows by default), near-tie tokens excluded and counted."""
     T = layer.x.shape[0]
-    tol = tol if tol is not None else TOL[layer.w.act]
     rows_t = torch.arange(T) if rows is None else torch.as_tensor(rows)
     ref = OB.forward(layer, rows=rows_t, nthreads=NTHREADS)
     keep = ref["margin"] >= NEAR_TIE
@@ -120,16 +148,14 @@ def check_outputs(layer, g: GpuRun, rows=None, tol=None) -> dict:
     out_fwd = g.out_fwd.float().cpu().numpy()[rows_t.numpy()]
     assert np.isfinite(out).all() and np.isfinite(out_fwd).all()
     assert np.array_equal(out, out_fwd), "moe_forward differs from the stage-by-stage path"
-    err = rel_err(out[keep], ref["out"][keep]) if keep.any() else 0.0
-    assert err <= tol, f"max err / rms = {err:.3e} > {tol}"
-    res = {"err": err, "compared": int(keep.sum()), "near_ties": int((~keep).sum())}
+    res = {"compared": int(keep.sum()), "near_ties": int((~keep).sum())}
+    if keep.any():
+        res.update(compare(out[keep], ref["out"][keep], layer.w.act, tol, output_rounding))
     w = layer.w
     if w.n_shared:
         P, de, d = T * w.k, w.d_expert, w.d
         ysh = g.y_perm[P * de:].view(T, d).float().cpu().numpy()[rows_t.numpy()]
-        e_sh = rel_err(ysh, ref["shared"])
-        assert e_sh <= tol, f"shared expert err {e_sh:.3e}"
-        res["shared_err"] = e_sh
+        res["shared_err"] = compare(ysh, ref["shared"], w.act, tol)["err"]
     return res
 
 
@@ -139,7 +165,6 @@ def check_expert_rows(layer, g: GpuRun, nrows: int = 6, seed: int = 0, tol=None)
     w = layer.w
     if w.d_latent:
         return
-    tol = tol if tol is not None else TOL[w.act]
     T, k, d = layer.x.shape[0], w.k, w.d
     P = T * k
     rng = np.random.default_rng(seed)
@@ -152,4 +177,4 @@ def check_expert_rows(layer, g: GpuRun, nrows: int = 6, seed: int = 0, tol=None)
         xr = layer.x[t].double().cpu().numpy()
         ref = oracle.swiglu_row(xr, OB.mat(layer.W13[e]), OB.mat(layer.W2[e]), I=w.I)
         got = y[r].float().cpu().numpy()
-        assert rel_err(got, ref) <= tol, f"row {r} (token {t}, expert {e})"
+        compare(got, ref, w.act, tol)

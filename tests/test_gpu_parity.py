@@ -29,14 +29,14 @@ def _layer(w, seed=0):
     return S.make_layer(w, seed=seed, device="cuda")
 
 
-def _full_check(layer, flags=0, rows=None):
+def _full_check(layer, flags=0, rows=None, output_rounding=False, expert_rows=6):
     L = _lib()
     g = L.run_gpu(layer, flags)
     assert g.status == B.MOE_OK and g.status_fwd == B.MOE_OK
     L.check_permutation(layer, g)
     r = L.check_routing(layer, g)
-    L.check_expert_rows(layer, g)
-    o = L.check_outputs(layer, g, rows=rows)
+    L.check_expert_rows(layer, g, nrows=expert_rows)
+    o = L.check_outputs(layer, g, rows=rows, output_rounding=output_rounding)
     return {**r, **o}
 
 
@@ -78,7 +78,13 @@ def test_bf16_small_all_tokens(cuda_device, flags):
 
 @pytest.mark.parametrize("flags", [ROWS, SWAP], ids=["rows", "swap"])
 def test_bf16_one_expert_takes_every_token(cuda_device, flags):
-    """k = 1 and a bias that forces expert 5: one group of T rows, every other group empty."""
+    """k = 1 and a bias that forces expert 5: one group of T rows, every other group empty.
+
+    Every output is 2.827 x one expert's output plus the shared expert, with no averaging over
+    the k slots, so the bf16 rounding of h and of the output enter unaveraged: an ideal pipeline
+    that rounds only h and the output to bf16 (all else exact) already reaches 2.16e-2 of the rms
+    on these inputs.  The fp32 expert rows are held to the plain 2e-2 bound (all 64 sampled);
+    the final bf16 output is held to 2e-2 after subtracting its own rounding, 2^-8 |ref|."""
     w = replace(SMALL_BF16, k=1, T=333)
     layer = _layer(w, seed=2)
     layer.b.zero_()
@@ -86,7 +92,7 @@ def test_bf16_one_expert_takes_every_token(cuda_device, flags):
     g = _lib().run_gpu(layer, flags)
     assert (g.idx.cpu() == 5).all()
     assert int(g.counts[5]) == 333 and int(g.counts[:5].sum() + g.counts[6:16].sum()) == 0
-    _full_check(layer, flags)
+    _full_check(layer, flags, output_rounding=True, expert_rows=64)
 
 
 @pytest.mark.parametrize("flags", [ROWS, SWAP], ids=["rows", "swap"])
