@@ -32,6 +32,13 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "MoE-layer tokens/s (d=7168, 384 experts top-8) and % of roofline (HBM or TC)"
+# DRAM traffic / algorithmic bytes per kernel variant, from the committed ncu captures under
+# profiles/ (dram__bytes_read.sum + dram__bytes_write.sum of one launch over the algorithmic bytes
+# of that launch).  A kernel changed since its capture must be dropped from this table.
+MEASURED_TRAFFIC_RATIO = {
+    "gemm13_swiglu_swap": (1.003, "profiles/gemm_tc_swap_decode_E32.md"),
+    "gemm2_swap": (0.994, "profiles/gemm_tc_swap_decode_E32.md"),
+}
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -346,7 +353,11 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
             roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
                     "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs",
                     "work_per_launch": by[unit_key]}
-        roof["traffic"] = None
+        ratio = MEASURED_TRAFFIC_RATIO.get(dom)
+        roof["traffic"] = ratio[0] * by[unit_key] if ratio else None
+        if ratio:
+            roof["traffic_source"] = (f"{ratio[1]}: ncu DRAM bytes / algorithmic bytes = "
+                                      f"{ratio[0]} on a 32-expert capture, scaled to this launch")
     else:
         roof = None
     t_tc = fl["layer"] / (peaks["bf16_tflops_sustained"] * 1e12)

@@ -297,8 +297,15 @@ static moe_status_t run_permute(Ctx& x, const int32_t* idx, int32_t* counts, int
                                   perm_dst, x.err, x.st));
 }
 
-static cudaError_t gemm(Ctx& x, const GroupedGemm& g) {
-  if (x.pl.tc) return launch_gemm_tc(g, x.pl.swap, x.sms, x.st);
+// The routed expert GEMMs: tensor cores (token-rows or swap-AB tiles) for bf16, CUDA cores for
+// fp32.  The profiler name carries the variant ("<label>_rows" / "_swap" / "_simt").
+static cudaError_t gemm(Ctx& x, GroupedGemm g, const char* rows_label, const char* swap_label,
+                        const char* simt_label) {
+  if (x.pl.tc) {
+    g.label = x.pl.swap ? swap_label : rows_label;
+    return launch_gemm_tc(g, x.pl.swap, x.sms, x.st);
+  }
+  g.label = simt_label;
   return launch_gemm_simt(g, x.sms, x.st);
 }
 
@@ -371,8 +378,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.ldo = I;
     g.out_dtype = c->act_dtype;
     g.err = x.err;
-    g.label = "gemm13_swiglu";
-    e = gemm(x, g);
+    e = gemm(x, g, "gemm13_swiglu_rows", "gemm13_swiglu_swap", "gemm13_swiglu_simt");
     if (e != cudaSuccess) return from_cuda(e);
   }
   // W2 -> y_perm [P][de] (+ shared rows [T][d])
@@ -403,8 +409,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.ldo = de;
     g.out_dtype = MOE_F32;
     g.err = x.err;
-    g.label = "gemm2";
-    e = gemm(x, g);
+    e = gemm(x, g, "gemm2_rows", "gemm2_swap", "gemm2_simt");
     if (e != cudaSuccess) return from_cuda(e);
   }
   if (c->n_shared && x.pl.latent) {  // shared expert on the full-width input
