@@ -120,6 +120,24 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, int32
                          int32_t* offsets, int32_t* perm_src, int32_t* perm_dst, void* ws,
                          size_t ws_bytes, void* stream);
 
+/* moe_permute for callers that cannot allocate device memory.  The pages have no counterpart:
+ * this is a deployment variant of the dispatch bookkeeping above, with the same arguments and
+ * results except the workspace.  Callers that cannot call cudaMalloc at routing time need it: a
+ * serving process that gave the GPU's free memory to its own pool at start-up, or a
+ * latency-critical loop where cudaMalloc may synchronise the device.  Its scratch (the per-chunk
+ * expert counts) is a fixed 1 MiB array of device global memory inside the library, held by every
+ * GPU that loads the library until the process exits; no memory is allocated.
+ *   Limits: T*k <= 262144 and E <= 1023; larger sizes return MOE_ERR_UNSUPPORTED and enqueue
+ *   nothing.  There is no status word: an expert index outside [0, E) is skipped (not counted)
+ *   and its perm_dst entry is set to -1.
+ *   The first call on each device looks up the array's device address (cudaGetSymbolAddress)
+ *   with that device current; make that first call before any stream capture.
+ *   Every call on a device shares the one array: calls whose GPU work overlaps (for example on
+ *   two streams at once) race on it and produce wrong results, so serialise them. */
+moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_idx,
+                                 int32_t* counts, int32_t* offsets, int32_t* perm_src,
+                                 int32_t* perm_dst, void* stream);
+
 /* Expert MLPs [K2-MoE] steps g, u, a, h, E_i and y_shared; the per-expert loop of `moe_infer`
  * [K3-UP] as grouped GEMMs over the permuted rows; on the K3 path the down-projection
  * x_lat = x W_down^T first [K3-UP].

@@ -26,7 +26,7 @@ MOE_FLAG_ROUTER_SIMT, MOE_FLAG_ROUTER_TC = 0x4, 0x8
 EXPORTED = ("moe_workspace_size", "moe_router", "moe_permute", "moe_experts", "moe_combine",
             "moe_forward", "moe_forward_host_io", "moe_reset_device_status", "moe_device_status",
             "moe_status_string", "moe_launch_count", "moe_reset_launch_count",
-            "moe_profile_enable", "moe_profile_read")
+            "moe_profile_enable", "moe_profile_read", "moe_permute_noalloc")
 
 
 class MoEError(RuntimeError):
@@ -86,6 +86,8 @@ def load_library():
             lib.moe_launch_count.argtypes = []
             lib.moe_reset_launch_count.restype = None
             lib.moe_reset_launch_count.argtypes = []
+            lib.moe_permute_noalloc.restype = S
+            lib.moe_permute_noalloc.argtypes = [C, P, P, P, P, P, P]
             lib.moe_profile_enable.restype = S
             lib.moe_profile_enable.argtypes = [S]
             lib.moe_profile_read.restype = S
@@ -182,6 +184,13 @@ def moe_permute(cfg, topk_idx, counts, offsets, perm_src, perm_dst, ws, stream=N
     _check(load_library().moe_permute(ctypes.byref(cfg), _dev(topk_idx), _dev(counts),
                                       _dev(offsets), _dev(perm_src), _dev(perm_dst), _dev(ws),
                                       ws.numel(), _stream(stream)), "moe_permute")
+
+
+def moe_permute_noalloc(cfg, topk_idx, counts, offsets, perm_src, perm_dst, stream=None):
+    """moe_permute for callers that cannot allocate: no workspace, fixed in-library scratch."""
+    _check(load_library().moe_permute_noalloc(ctypes.byref(cfg), _dev(topk_idx), _dev(counts),
+                                              _dev(offsets), _dev(perm_src), _dev(perm_dst),
+                                              _stream(stream)), "moe_permute_noalloc")
 
 
 def moe_experts(cfg, x, offsets, perm_src, W13, W2, W13_scale, W2_scale, Ws13, Ws2, Ws13_scale,
