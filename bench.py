@@ -128,25 +128,30 @@ class ClockSampler:
 
 def touched_bytes(w, idx: np.ndarray) -> dict:
     """Algorithmic bytes of one layer pass: the expert weights the routing touches (each once),
-    the shared expert, the router weight, the input read and the output write."""
+    the shared expert, the router weight, the input read and the output write; per kernel also the
+    activations it reads and writes (h in the activation type, or e4m3 + scales for fp8 experts;
+    expert outputs in fp32)."""
     touched = np.unique(idx)
     ab = 4 if w.act == "f32" else 2
+    wb = 1 if w.fp8 else ab                       # bytes per expert weight
+    sb = 4.0 / (128 * 128) if w.fp8 else 0.0      # block-scale bytes per weight
+    hb = 1 + 4.0 / 128 if w.fp8 else ab           # bytes per activation entering a GEMM
     de = w.d_expert
     T, P = idx.shape[0], idx.size
-    w13 = 2 * w.I * de * ab
-    w2 = de * w.I * ab
-    sh13 = 2 * w.I_shared * w.d * ab if w.n_shared else 0
-    sh2 = w.d * w.I_shared * ab if w.n_shared else 0
+    w13 = 2 * w.I * de * (wb + sb)
+    w2 = de * w.I * (wb + sb)
+    sh13 = 2 * w.I_shared * w.d * (wb + sb) if w.n_shared else 0
+    sh2 = w.d * w.I_shared * (wb + sb) if w.n_shared else 0
     lat = 2 * w.d_latent * w.d * ab if w.d_latent else 0
-    rows_sh = T * w.n_shared
+    rows_sh = 0 if w.d_latent else T * w.n_shared
     return {
         "touched_experts": int(touched.size),
-        # gemm13: W1|W3 of the touched experts + shared, activations in, h out
-        "gemm13": len(touched) * w13 + (0 if w.d_latent else sh13) + P * de * ab
-        + (0 if w.d_latent else T * w.d * ab) + (P + (0 if w.d_latent else rows_sh)) * w.I * ab,
-        # gemm2: W2 of the touched experts + shared, h in, y out
-        "gemm2": len(touched) * w2 + (0 if w.d_latent else sh2)
-        + (P + (0 if w.d_latent else rows_sh)) * (w.I + de) * ab,
+        # gemm13: W1|W3 of the touched experts (+ shared), activations in, h out
+        "gemm13": len(touched) * w13 + (0 if w.d_latent else sh13) + P * de * hb
+        + rows_sh * w.d * hb + (P + rows_sh) * w.I * hb,
+        # gemm2: W2 of the touched experts (+ shared), h in, fp32 y out
+        "gemm2": len(touched) * w2 + (0 if w.d_latent else sh2) + (P + rows_sh) * w.I * hb
+        + (P + rows_sh) * de * 4,
         "layer": len(touched) * (w13 + w2) + sh13 + sh2 + lat + w.E * w.d * 4
         + 2 * T * w.d * ab,
     }
@@ -332,20 +337,25 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
     by = touched_bytes(w, idx_np)
     fl = flops(w, w.T)
     kernels = {k: {"ms_per_launch": v[0] / max(v[1], 1), "launches": v[1]} for k, v in prof.items()}
+    if w.fp8:  # an fp8 contraction: the measured bf16 peak times the nominal fp8 / bf16 ratio (2)
+        tc_peak = 2.0 * peaks["bf16_tflops_sustained"]
+        tc_src = (f"{peak_src} bf16_tflops_sustained x 2 (nominal dense fp8 / bf16 ratio 4.5 / "
+                  f"2.25); kernel timed inside a long step loop")
+    else:
+        tc_peak = peaks["bf16_tflops_sustained"]
+        tc_src = f"{peak_src} bf16_tflops_sustained (kernel timed inside a long step loop)"
     dom = max(prof.items(), key=lambda kv: kv[1][0])[0] if prof else None
     if dom is not None:
         ms_launch = kernels[dom]["ms_per_launch"]
         unit_key = "gemm2" if dom.startswith("gemm2") else "gemm13"
         # the kernel's bound: the larger of its algorithmic time at tensor peak and at HBM peak
-        t_tc_k = fl.get(unit_key, 0) / (peaks["bf16_tflops_sustained"] * 1e12)
+        t_tc_k = fl.get(unit_key, 0) / (tc_peak * 1e12)
         t_hbm_k = by[unit_key] / (peaks["hbm_gbs"] * 1e9)
         if t_tc_k > t_hbm_k:
             achieved = fl.get(unit_key, 0) / (ms_launch / 1000.0) / 1e12
-            peak = peaks["bf16_tflops_sustained"]
+            peak = tc_peak
             roof = {"kernel": dom, "bound": "tensor", "achieved": achieved, "peak": peak,
-                    "unit": "TFLOP/s", "frac": achieved / peak,
-                    "peak_source": f"{peak_src} bf16_tflops_sustained (kernel timed inside a "
-                                   f"long step loop)",
+                    "unit": "TFLOP/s", "frac": achieved / peak, "peak_source": tc_src,
                     "work_per_launch": fl.get(unit_key, 0)}
         else:
             achieved = by[unit_key] / (ms_launch / 1000.0) / 1e9
@@ -360,7 +370,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
                                       f"{ratio[0]} on a 32-expert capture, scaled to this launch")
     else:
         roof = None
-    t_tc = fl["layer"] / (peaks["bf16_tflops_sustained"] * 1e12)
+    t_tc = fl["layer"] / (tc_peak * 1e12)
     t_hbm = by["layer"] / (peaks["hbm_gbs"] * 1e9)
     layer_roof = {"t_roof_ms": 1000 * max(t_tc, t_hbm), "bound": "tensor" if t_tc > t_hbm else "hbm",
                   "frac": 1000 * max(t_tc, t_hbm) / ms_step, "algorithmic_bytes": by["layer"],
@@ -379,7 +389,8 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if w.act == "f32" else "bf16", "data": "synthetic",
+        "dtype": "f32" if w.act == "f32" else ("e4m3" if w.fp8 else "bf16"),
+        "data": "synthetic",
         "config": {"workload": w.name, "tokens": w.T, "d": w.d, "experts": w.E, "top_k": w.k,
                    "expert_intermediate": w.I, "shared_intermediate": w.I_shared,
                    "d_latent": w.d_latent, "router": "fp32 logits",

@@ -206,6 +206,10 @@ moe_status_t moe_device_status(const void* ws, size_t ws_bytes, void* stream);
 /* A static, human-readable name of a status code. */
 const char* moe_status_string(moe_status_t status);
 
+/* Name and message of the CUDA error behind the calling thread's last MOE_ERR_CUDA ("" if none);
+ * valid until the thread's next call into the library. */
+const char* moe_last_error_string(void);
+
 /* Number of this library's kernels enqueued by the calling thread since the last reset (a launch
  * counter for benchmarks), and its reset. */
 uint64_t moe_launch_count(void);

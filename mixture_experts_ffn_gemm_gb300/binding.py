@@ -26,13 +26,17 @@ MOE_FLAG_ROUTER_SIMT, MOE_FLAG_ROUTER_TC = 0x4, 0x8
 EXPORTED = ("moe_workspace_size", "moe_router", "moe_permute", "moe_experts", "moe_combine",
             "moe_forward", "moe_forward_host_io", "moe_reset_device_status", "moe_device_status",
             "moe_status_string", "moe_launch_count", "moe_reset_launch_count",
-            "moe_profile_enable", "moe_profile_read", "moe_permute_noalloc")
+            "moe_profile_enable", "moe_profile_read", "moe_permute_noalloc",
+            "moe_last_error_string")
 
 
 class MoEError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {status_string(status)} ({status})")
+        detail = ""
+        if status == MOE_ERR_CUDA:
+            detail = " [" + load_library().moe_last_error_string().decode() + "]"
+        super().__init__(f"{where}: {status_string(status)} ({status}){detail}")
 
 
 class moe_config_t(ctypes.Structure):
@@ -86,6 +90,8 @@ def load_library():
             lib.moe_launch_count.argtypes = []
             lib.moe_reset_launch_count.restype = None
             lib.moe_reset_launch_count.argtypes = []
+            lib.moe_last_error_string.restype = ctypes.c_char_p
+            lib.moe_last_error_string.argtypes = []
             lib.moe_permute_noalloc.restype = S
             lib.moe_permute_noalloc.argtypes = [C, P, P, P, P, P, P]
             lib.moe_profile_enable.restype = S

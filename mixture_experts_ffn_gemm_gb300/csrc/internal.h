@@ -69,6 +69,53 @@ struct GroupedGemm {
 cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStream_t st);
 bool gemm_tc_supported(const GroupedGemm& g, int swap);
 
+// Grouped GEMM with e4m3 operands and fp32 block scales (tcgen05 kind::f8f6f4), token-rows tiles
+// M = 128 x 256 weight rows.  Activation scales per row per 128 channels, stored [K/128][ld];
+// weight scales per 128 x 128 block, [rows/128][K/128].  swiglu: out = e4m3 h [rows][ldo] with
+// scales out_sT [F/128][out_s_ld]; else fp32 out [rows][ldo].
+struct Fp8Gemm {
+  const void* act = nullptr;
+  int64_t act_rows = 0;
+  const float* act_sT = nullptr;
+  int64_t act_s_ld = 0;
+  const void* w = nullptr;
+  int64_t w_rows = 0;
+  const float* w_s = nullptr;
+  const int32_t* offsets = nullptr;
+  int n_routed = 0;
+  int w_group_rows = 0;
+  int u_off = 0;
+  const void* act_d = nullptr;
+  int64_t act_d_rows = 0;
+  const float* act_sT_d = nullptr;
+  int64_t act_s_ld_d = 0;
+  int dense_act_row0 = 0;
+  const void* w_d = nullptr;
+  int64_t w_d_rows = 0;
+  const float* w_s_d = nullptr;
+  int dense_rows = 0;
+  int dense_out_row0 = 0;
+  int u_off_d = 0;
+  int K = 0;
+  int F = 0;
+  bool swiglu = false;
+  void* out = nullptr;
+  int64_t ldo = 0;
+  float* out_sT = nullptr;
+  int64_t out_s_ld = 0;
+  uint32_t* err = nullptr;
+  const char* label = "gemm_fp8";
+};
+cudaError_t launch_gemm_fp8(const Fp8Gemm& g, int num_sms, cudaStream_t st);
+
+// x bf16 [rows][d] -> e4m3 codes [rows][d] and scales sT [d/128][rows] (amax / 448 per 128).
+cudaError_t launch_quantize_rows(const void* x, int64_t rows, int d, uint8_t* q, float* sT,
+                                 cudaStream_t st);
+// dst[r] = src[perm_src[r] / k] for e4m3 rows of d bytes, with their scales (transposed layout).
+cudaError_t launch_gather_q(const uint8_t* src, const float* src_sT, int64_t src_rows,
+                            const int32_t* perm_src, int64_t P, int k, int d, uint8_t* dst,
+                            float* dst_sT, int num_sms, cudaStream_t st);
+
 // CUDA-core grouped GEMM (fp32 or bf16 operands, fp32 accumulation), 64x64 tiles.
 cudaError_t launch_gemm_simt(const GroupedGemm& g, int num_sms, cudaStream_t st);
 

@@ -1,5 +1,6 @@
 // moe_api.cu -- the C ABI of include/moe.h: host validation, workspace layout and the order of
 // kernel launches for each entry point.  No allocation, no host synchronisation on the layer path.
+#include <cstdio>
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -86,11 +87,14 @@ struct Plan {
   int router_splits;  // split-K slices of the CUDA-core router
   int swap;           // 1: weight-rows-as-M tensor-core tiles
   bool tc;            // tensor-core expert GEMMs
+  bool fp8;           // e4m3 experts with block scales
 };
 
 struct Layout {
   size_t status, zbuf, wsplit, idx, weight, chunk_counts, counts, offsets, perm_src, perm_dst,
-      x_lat, x_perm, h, y_perm, u_hat, x_io, out_io, total;
+      x_lat, x_perm, h, y_perm, u_hat, x_io, out_io;
+  size_t xq, xq_s, xpq, xpq_s, hq, hq_s;  // fp8 experts: e4m3 activations + [K/128][rows] scales
+  size_t total;
 };
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -107,7 +111,13 @@ static moe_status_t validate(const moe_config_t* c) {
   if (c->k > 32 || c->E > 1023) return MOE_ERR_UNSUPPORTED;
   if (c->n_shared && c->I_shared != c->I) return MOE_ERR_UNSUPPORTED;
   if (c->T * c->k + c->T >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
-  if (c->w_dtype == MOE_FP8_E4M3) return MOE_ERR_UNSUPPORTED;
+  if (c->w_dtype == MOE_FP8_E4M3) {
+    // e4m3 experts: bf16 activations, 128 x 128 weight blocks, K2 path only
+    if (c->act_dtype != MOE_BF16 || c->quant_block != 128 || c->d_latent > 0)
+      return MOE_ERR_UNSUPPORTED;
+    if (c->d % 256 || c->I % 128) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+  }
   if (c->w_dtype != c->act_dtype) return MOE_ERR_UNSUPPORTED;
   if (c->act_dtype == MOE_F32) {
     if (c->d % 16 || c->I % 16 || c->d % 4) return MOE_ERR_UNSUPPORTED;
@@ -124,6 +134,7 @@ static Plan make_plan(const moe_config_t* c) {
   p.latent = c->d_latent > 0;
   p.de = p.latent ? c->d_latent : c->d;
   p.tc = c->act_dtype == MOE_BF16;
+  p.fp8 = c->w_dtype == MOE_FP8_E4M3;
   // router
   const bool tc_ok = c->act_dtype == MOE_BF16 && c->E % 128 == 0 && c->d % 64 == 0;
   if (c->flags & MOE_FLAG_ROUTER_SIMT)
@@ -172,8 +183,14 @@ static Layout make_layout(const moe_config_t* c, const Plan& pl) {
   L.perm_src = take((size_t)P * 4);
   L.perm_dst = take((size_t)P * 4);
   L.x_lat = take(pl.latent ? (size_t)T * c->d_latent * ab : 0);
-  L.x_perm = take((size_t)P * pl.de * ab);
-  L.h = take((size_t)(P + shared_rows) * I * ab);
+  L.x_perm = take(pl.fp8 ? 0 : (size_t)P * pl.de * ab);
+  L.h = take(pl.fp8 ? 0 : (size_t)(P + shared_rows) * I * ab);
+  L.xq = take(pl.fp8 ? (size_t)T * d : 0);
+  L.xq_s = take(pl.fp8 ? (size_t)(d / 128) * T * 4 : 0);
+  L.xpq = take(pl.fp8 ? (size_t)P * d : 0);
+  L.xpq_s = take(pl.fp8 ? (size_t)(d / 128) * P * 4 : 0);
+  L.hq = take(pl.fp8 ? (size_t)(P + shared_rows) * I : 0);
+  L.hq_s = take(pl.fp8 ? (size_t)(I / 128) * (P + shared_rows) * 4 : 0);
   L.y_perm = take(((size_t)P * pl.de + (size_t)shared_rows * d) * 4);  // fp32 expert outputs
   L.u_hat = take(pl.latent ? (size_t)T * c->d_latent * 2 : 0);
   L.x_io = take((size_t)T * d * ab);
@@ -182,7 +199,14 @@ static Layout make_layout(const moe_config_t* c, const Plan& pl) {
   return L;
 }
 
-static moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+static thread_local char g_last_error[256] = "";
+
+static moe_status_t from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return MOE_OK;
+  snprintf(g_last_error, sizeof g_last_error, "%s: %s", cudaGetErrorName(e),
+           cudaGetErrorString(e));
+  return MOE_ERR_CUDA;
+}
 
 template <typename T>
 static T* at(void* ws, size_t off) {
@@ -311,8 +335,9 @@ static cudaError_t gemm(Ctx& x, GroupedGemm g, const char* rows_label, const cha
 
 static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
                                 const int32_t* perm_src, const void* W13, const void* W2,
-                                const void* Ws13, const void* Ws2, const void* W_down,
-                                void* y_perm) {
+                                const float* W13_scale, const float* W2_scale, const void* Ws13,
+                                const void* Ws2, const float* Ws13_scale, const float* Ws2_scale,
+                                const void* W_down, void* y_perm) {
   const moe_config_t* c = x.c;
   if (c->T == 0) return MOE_OK;
   const int64_t T = c->T, P = T * c->k;
@@ -321,6 +346,86 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
   void* h = at<void>(x.ws, x.L.h);
   void* x_perm = at<void>(x.ws, x.L.x_perm);
   cudaError_t e;
+
+  if (x.pl.fp8) {  // e4m3 experts: quantise x once, gather codes + scales, two fp8 GEMMs
+    uint8_t* xq = at<uint8_t>(x.ws, x.L.xq);
+    float* xq_s = at<float>(x.ws, x.L.xq_s);
+    uint8_t* xpq = at<uint8_t>(x.ws, x.L.xpq);
+    float* xpq_s = at<float>(x.ws, x.L.xpq_s);
+    uint8_t* hq = at<uint8_t>(x.ws, x.L.hq);
+    float* hq_s = at<float>(x.ws, x.L.hq_s);
+    const int64_t rows_h = P + (c->n_shared ? T : 0);
+    e = launch_quantize_rows(xin, T, d, xq, xq_s, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+    e = launch_gather_q(xq, xq_s, T, perm_src, P, c->k, d, xpq, xpq_s, x.sms, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+    Fp8Gemm g;
+    g.act = xpq;
+    g.act_rows = P;
+    g.act_sT = xpq_s;
+    g.act_s_ld = P;
+    g.w = W13;
+    g.w_rows = (int64_t)E * 2 * I;
+    g.w_s = W13_scale;
+    g.offsets = offsets;
+    g.n_routed = E;
+    g.w_group_rows = 2 * I;
+    g.u_off = I;
+    if (c->n_shared) {
+      g.act_d = xq;
+      g.act_d_rows = T;
+      g.act_sT_d = xq_s;
+      g.act_s_ld_d = T;
+      g.w_d = Ws13;
+      g.w_d_rows = 2 * I;
+      g.w_s_d = Ws13_scale;
+      g.dense_rows = (int)T;
+      g.dense_out_row0 = (int)P;
+      g.u_off_d = I;
+    }
+    g.K = d;
+    g.F = I;
+    g.swiglu = true;
+    g.out = hq;
+    g.ldo = I;
+    g.out_sT = hq_s;
+    g.out_s_ld = rows_h;
+    g.err = x.err;
+    g.label = "gemm13_swiglu_fp8";
+    e = launch_gemm_fp8(g, x.sms, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+    Fp8Gemm g2;
+    g2.act = hq;
+    g2.act_rows = rows_h;
+    g2.act_sT = hq_s;
+    g2.act_s_ld = rows_h;
+    g2.w = W2;
+    g2.w_rows = (int64_t)E * d;
+    g2.w_s = W2_scale;
+    g2.offsets = offsets;
+    g2.n_routed = E;
+    g2.w_group_rows = d;
+    if (c->n_shared) {
+      g2.act_d = hq;
+      g2.act_d_rows = rows_h;
+      g2.act_sT_d = hq_s;
+      g2.act_s_ld_d = rows_h;
+      g2.dense_act_row0 = (int)P;
+      g2.w_d = Ws2;
+      g2.w_d_rows = d;
+      g2.w_s_d = Ws2_scale;
+      g2.dense_rows = (int)T;
+      g2.dense_out_row0 = (int)P;
+    }
+    g2.K = I;
+    g2.F = d;
+    g2.swiglu = false;
+    g2.out = y_perm;
+    g2.ldo = d;
+    g2.err = x.err;
+    g2.label = "gemm2_fp8";
+    return from_cuda(launch_gemm_fp8(g2, x.sms, x.st));
+  }
 
   const void* route_src = xin;
   if (x.pl.latent) {  // x_lat = x W_down^T on every token (the router saw the full width)
@@ -538,22 +643,22 @@ moe_status_t moe_experts(const moe_config_t* cfg, const void* x, const int32_t* 
                          const void* Ws2, const float* Ws13_scale, const float* Ws2_scale,
                          const void* W_down, void* y_perm, void* ws, size_t ws_bytes,
                          void* stream) {
-  (void)W13_scale;
-  (void)W2_scale;
-  (void)Ws13_scale;
-  (void)Ws2_scale;
   Ctx c;
   moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
   if (s != MOE_OK) return s;
   MOE_RETURN_IF_EMPTY(cfg);
   if (!x || !offsets || !perm_src || !W13 || !W2 || !y_perm) return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared && (!Ws13 || !Ws2)) return MOE_ERR_INVALID_ARG;
+  if (cfg->w_dtype == MOE_FP8_E4M3 &&
+      (!W13_scale || !W2_scale || (cfg->n_shared && (!Ws13_scale || !Ws2_scale))))
+    return MOE_ERR_INVALID_ARG;
   if (cfg->d_latent > 0 && !W_down) return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {x, W13, W2, Ws13, Ws2, W_down, y_perm};
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
   ready(c);
-  return run_experts(c, x, offsets, perm_src, W13, W2, Ws13, Ws2, W_down, y_perm);
+  return run_experts(c, x, offsets, perm_src, W13, W2, W13_scale, W2_scale, Ws13, Ws2,
+                     Ws13_scale, Ws2_scale, W_down, y_perm);
 }
 
 moe_status_t moe_combine(const moe_config_t* cfg, const void* y_perm, const int32_t* perm_dst,
@@ -576,16 +681,15 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const float* W_
                          const float* W2_scale, const void* Ws13, const void* Ws2,
                          const float* Ws13_scale, const float* Ws2_scale, const void* W_down,
                          const void* W_up, void* out, void* ws, size_t ws_bytes, void* stream) {
-  (void)W13_scale;
-  (void)W2_scale;
-  (void)Ws13_scale;
-  (void)Ws2_scale;
   Ctx c;
   moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
   if (s != MOE_OK) return s;
   MOE_RETURN_IF_EMPTY(cfg);
   if (!x || !W_r || !b || !W13 || !W2 || !out) return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared && (!Ws13 || !Ws2)) return MOE_ERR_INVALID_ARG;
+  if (cfg->w_dtype == MOE_FP8_E4M3 &&
+      (!W13_scale || !W2_scale || (cfg->n_shared && (!Ws13_scale || !Ws2_scale))))
+    return MOE_ERR_INVALID_ARG;
   if (cfg->d_latent > 0 && (!W_down || !W_up)) return MOE_ERR_INVALID_ARG;
   const void* ptrs[] = {x, W_r, W13, W2, Ws13, Ws2, W_down, W_up, out};
   for (const void* p : ptrs)
@@ -602,7 +706,8 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const float* W_
   if ((s = run_router(c, x, W_r, b, nullptr, idx, wgt)) != MOE_OK) return s;
   if ((s = run_permute(c, idx, at<int32_t>(ws, L.counts), offsets, perm_src, perm_dst)) != MOE_OK)
     return s;
-  if ((s = run_experts(c, x, offsets, perm_src, W13, W2, Ws13, Ws2, W_down, y_perm)) != MOE_OK)
+  if ((s = run_experts(c, x, offsets, perm_src, W13, W2, W13_scale, W2_scale, Ws13, Ws2,
+                       Ws13_scale, Ws2_scale, W_down, y_perm)) != MOE_OK)
     return s;
   return run_combine(c, y_perm, perm_dst, wgt, W_up, out);
 }
@@ -663,6 +768,8 @@ const char* moe_status_string(moe_status_t s) {
   }
   return "MOE_ERR_UNKNOWN";
 }
+
+const char* moe_last_error_string(void) { return g_last_error; }
 
 uint64_t moe_launch_count(void) { return g_launches; }
 void moe_reset_launch_count(void) { g_launches = 0; }

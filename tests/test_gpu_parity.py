@@ -137,6 +137,35 @@ def test_latent_small_without_norm(cuda_device):
 
 
 # ---------------------------------------------------------------------------------------------
+# fp8 experts: e4m3 weights with 128 x 128 block scales, activations per token per 128 channels
+# ---------------------------------------------------------------------------------------------
+
+SMALL_FP8 = replace(S.WORKLOADS["tiny_fp32"], name="small_fp8", act="bf16", fp8=True, T=300,
+                    x_dist="clusters16", w_init="std0.02", bias_range=0.05)
+
+
+def test_fp8_small_all_tokens(cuda_device):
+    _full_check(_layer(SMALL_FP8, seed=21))
+
+
+@pytest.mark.parametrize("T", [1, 17, 129])
+def test_fp8_ragged_tokens(cuda_device, T):
+    _full_check(_layer(SMALL_FP8.with_tokens(T), seed=22 + T))
+
+
+def test_fp8_k2_widths_32_experts(cuda_device):
+    w = replace(S.WORKLOADS["k2_fp8"], name="k2_fp8_e32", E=32, T=72)
+    _full_check(_layer(w, seed=23))
+
+
+def test_fp8_zero_activation_group_gets_unit_scale(cuda_device):
+    """An all-zero 128-channel group of x quantises with scale 1 (no 0/0) and contributes 0."""
+    layer = _layer(replace(SMALL_FP8, T=64), seed=24)
+    layer.x[:, :128] = 0.0
+    _full_check(layer)
+
+
+# ---------------------------------------------------------------------------------------------
 # K2 widths (d = 7168, I = 2048) with fewer experts: every token checked
 # ---------------------------------------------------------------------------------------------
 
@@ -176,6 +205,11 @@ def test_full_k2_prefill(cuda_device):
 def test_full_k3_latent(cuda_device):
     res = _full_workload("k3_latent_bf16")
     print("k3_latent", res)
+
+
+def test_full_k2_fp8(cuda_device):
+    res = _full_workload("k2_fp8")
+    print("k2_fp8", res)
 
 
 # ---------------------------------------------------------------------------------------------
