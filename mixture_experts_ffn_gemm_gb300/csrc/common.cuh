@@ -226,6 +226,16 @@ __device__ __forceinline__ void tmem_ld_wait() {
 // ---------------------------------------------------------------------------------------------
 // Numerics
 // ---------------------------------------------------------------------------------------------
+// acc[0..1] += s * v[0..1] with one paired fp32 FMA (fma.rn.f32x2, sm_100 and later).
+__device__ __forceinline__ void fma2(float& a0, float& a1, float s, uint32_t v0, uint32_t v1) {
+  uint64_t acc, sv, vv;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(acc) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(sv) : "f"(s));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(vv) : "r"(v0), "r"(v1));
+  asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(sv), "l"(vv));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
+}
+
 __device__ __forceinline__ float silu_fast(float g) { return g / (1.0f + __expf(-g)); }
 __device__ __forceinline__ float silu_accurate(float g) { return g / (1.0f + expf(-g)); }
 

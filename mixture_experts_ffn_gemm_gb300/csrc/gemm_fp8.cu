@@ -237,7 +237,18 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
       float acc[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+      // the scales of K-block kb + 1 are loaded while block kb is promoted (their global-memory
+      // latency then hides behind the MMA instead of stalling every block)
+      const float* sx_ptr = sx_col + act_row;
+      float sx_n = valid ? __ldg(sx_ptr) : 0.0f;
+      float w0_n = __ldg(ws0), w1_n = __ldg(ws1);
       for (int kb = 0; kb < nkb; ++kb, ++kbg) {
+        const float sx = sx_n, w0 = w0_n, w1 = w1_n;
+        if (kb + 1 < nkb) {
+          sx_n = valid ? __ldg(sx_ptr + (int64_t)(kb + 1) * sx_ld) : 0.0f;
+          w0_n = __ldg(ws0 + kb + 1);
+          w1_n = __ldg(ws1 + kb + 1);
+        }
         const uint32_t buf = kbg & 1u, bph = (kbg >> 1) & 1u;
         int w_ok = 1;
         if (lane == 0) w_ok = mbar_wait(&pfull[buf], bph, abort_flag, p.err) ? 1 : 0;
@@ -247,9 +258,8 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
           break;
         }
         tc_fence_after();
-        const float sx = valid ? __ldg(sx_col + (int64_t)kb * sx_ld + act_row) : 0.0f;
-        const float s0 = sx * __ldg(ws0 + kb);
-        const float s1 = sx * __ldg(ws1 + kb);
+        const float s0 = sx * w0;
+        const float s1 = sx * w1;
         const uint32_t tb = tmem_base + buf * kF8BN + ((uint32_t)(quarter * 32) << 16);
         if (kSwiGLU) {
 #pragma unroll
@@ -259,19 +269,23 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
             tmem_ld16(tb + 128 + half * 64 + c, u);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              acc[c + i] = fmaf(s0, __uint_as_float(g[i]), acc[c + i]);
-              acc[64 + c + i] = fmaf(s1, __uint_as_float(u[i]), acc[64 + c + i]);
+            for (int i = 0; i < 16; i += 2) {
+              fma2(acc[c + i], acc[c + i + 1], s0, g[i], g[i + 1]);
+              fma2(acc[64 + c + i], acc[64 + c + i + 1], s1, u[i], u[i + 1]);
             }
           }
         } else {
 #pragma unroll
           for (int c = 0; c < 128; c += 32) {
-            uint32_t v[32];
-            tmem_ld32(tb + half * 128 + c, v);
+            uint32_t v0[16], v1[16];
+            tmem_ld16(tb + half * 128 + c, v0);
+            tmem_ld16(tb + half * 128 + c + 16, v1);
             tmem_ld_wait();
 #pragma unroll
-            for (int i = 0; i < 32; ++i) acc[c + i] = fmaf(s0, __uint_as_float(v[i]), acc[c + i]);
+            for (int i = 0; i < 16; i += 2) {
+              fma2(acc[c + i], acc[c + i + 1], s0, v0[i], v0[i + 1]);
+              fma2(acc[c + 16 + i], acc[c + 16 + i + 1], s0, v1[i], v1[i + 1]);
+            }
           }
         }
         tc_fence_before();

@@ -162,7 +162,13 @@ cudaError_t launch_gemm_simt(const GroupedGemm& g, int num_sms, cudaStream_t st)
   p.ldo = g.ldo;
   p.out_f32 = g.out_dtype == MOE_F32;
   p.err = g.err;
-  dim3 grid(num_sms * 4, g.k_splits);
+  // at most as many CTAs as tiles can exist: routed groups have at most P/64 + n_routed row
+  // tiles in total, the dense group ceil(rows/64)
+  const int64_t ftiles = (g.F + kSimtTile - 1) / kSimtTile;
+  const int64_t rtiles = (g.n_routed > 0 ? g.act_rows / kSimtTile + g.n_routed : 0) +
+                         (g.dense_rows + kSimtTile - 1) / kSimtTile;
+  const int64_t bound = rtiles * ftiles;
+  dim3 grid((unsigned)(bound < num_sms * 4 ? (bound > 0 ? bound : 1) : num_sms * 4), g.k_splits);
   const bool swiglu = g.epi == EPI_SWIGLU;
   LaunchScope ls(g.label, st);
   if (g.act_dtype == MOE_F32 && g.w_dtype == MOE_F32) {

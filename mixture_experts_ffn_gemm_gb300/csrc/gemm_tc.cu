@@ -54,6 +54,8 @@ struct TcParams {
   const float* addend;  // EPI_STORE_ADD: fp32 [rows][ld_add]
   int64_t ld_add;
   uint32_t* err;
+  uint64_t wait_ns;     // limit of every mbarrier wait
+  int32_t test_stall;   // test hook: the producer issues no copy, so the MMA's wait expires
 };
 
 template <bool kSwap, int kBN, int kEpi>
@@ -140,7 +142,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
+    if (lane == 0 && !p.test_stall) {
       uint32_t stage = 0, phase = 0;
       int armed = 0;
       bool ok = true;
@@ -153,7 +155,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
         const int w_y = (ti.dense ? 0 : ti.g * p.w_group_rows) + ti.ft * S::FPT;
         const int u_off = ti.dense ? p.u_off_d : p.u_off;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -203,11 +205,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) break;
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * S::ACC_COLS;
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.err, p.wait_ns)) {
             ok = false;
             break;
           }
@@ -247,7 +249,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
       const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
                                       p.dense_rows, p.dense_act_row0, S::RPT);
       int ok = 1;
-      if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err) ? 1 : 0;
+      if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err, p.wait_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       tc_fence_after();
@@ -475,6 +477,8 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
   p.addend = (const float*)g.addend;
   p.ld_add = g.ld_add;
   p.err = g.err;
+  p.test_stall = g.test_stall ? 1 : 0;
+  p.wait_ns = g.test_stall ? 50000000ull : kWaitLimitNs;
   const int grid = num_sms;
   if (!swap) {
     if (g.epi == EPI_SWIGLU) return launch_variant<false, 256, EPI_SWIGLU>(p, grid, st, g.label);

@@ -59,6 +59,7 @@ struct GroupedGemm {
   int64_t split_stride = 0;
   uint32_t* err = nullptr;
   const char* label = "gemm";  // kernel name for the launch profiler
+  bool test_stall = false;     // test hook (MOE_FLAG_TEST_STALL_EXPERTS): see moe.h
 };
 
 // Tensor-core grouped GEMM (tcgen05 + TMA), bf16 operands, fp32 accumulation in TMEM.

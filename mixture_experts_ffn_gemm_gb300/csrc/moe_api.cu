@@ -483,6 +483,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.ldo = I;
     g.out_dtype = c->act_dtype;
     g.err = x.err;
+    g.test_stall = (c->flags & MOE_FLAG_TEST_STALL_EXPERTS) != 0;
     e = gemm(x, g, "gemm13_swiglu_rows", "gemm13_swiglu_swap", "gemm13_swiglu_simt");
     if (e != cudaSuccess) return from_cuda(e);
   }

@@ -19,6 +19,8 @@ namespace moe {
 constexpr int kTopkWarps = 8;
 constexpr int kMaxExpertsPerLane = 32;  // E <= 1024
 
+// EPL = experts per lane (ceil(E / 32)), a compile-time bound so that only real slots are kept.
+template <int EPL>
 __global__ void __launch_bounds__(kTopkWarps * 32)
     router_topk_kernel(const float* __restrict__ partial, int S, int64_t split_stride, int64_t T,
                        int E, int k, const float* __restrict__ b, float gate_scale,
@@ -28,10 +30,10 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
   const int64_t t = (int64_t)blockIdx.x * kTopkWarps + (threadIdx.x >> 5);
   if (t >= T) return;  // warp-uniform
 
-  float key[kMaxExpertsPerLane];
-  float sig[kMaxExpertsPerLane];
+  float key[EPL];
+  float sig[EPL];
 #pragma unroll
-  for (int j = 0; j < kMaxExpertsPerLane; ++j) {
+  for (int j = 0; j < EPL; ++j) {
     const int e = lane + 32 * j;
     key[j] = -INFINITY;
     sig[j] = 0.0f;
@@ -55,7 +57,7 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
     int be = 0x7fffffff;
     float bs = 0.0f;
 #pragma unroll
-    for (int j = 0; j < kMaxExpertsPerLane; ++j) {
+    for (int j = 0; j < EPL; ++j) {
       const int e = lane + 32 * j;
       if (e < E && !((taken >> j) & 1u) && (key[j] > bk || (key[j] == bk && e < be))) {
         bk = key[j];
@@ -93,10 +95,24 @@ cudaError_t launch_router_topk(const float* partial, int S, int64_t split_stride
   if (T <= 0) return cudaSuccess;
   if (E > 32 * kMaxExpertsPerLane || k > 32 || k > E) return cudaErrorInvalidValue;
   const int64_t blocks = (T + kTopkWarps - 1) / kTopkWarps;
+  const int epl = (E + 31) / 32;
   LaunchScope ls("router_topk", st);
-  router_topk_kernel<<<(unsigned)blocks, kTopkWarps * 32, 0, st>>>(
-      partial, S, split_stride, T, E, k, b, gate_scale, logits_out, idx, weight);
-  return cudaGetLastError();
+#define MOE_TOPK_CASE(N)                                                               \
+  if (epl <= N) {                                                                      \
+    router_topk_kernel<N><<<(unsigned)blocks, kTopkWarps * 32, 0, st>>>(               \
+        partial, S, split_stride, T, E, k, b, gate_scale, logits_out, idx, weight);    \
+    return cudaGetLastError();                                                         \
+  }
+  MOE_TOPK_CASE(1)
+  MOE_TOPK_CASE(2)
+  MOE_TOPK_CASE(4)
+  MOE_TOPK_CASE(8)
+  MOE_TOPK_CASE(12)
+  MOE_TOPK_CASE(16)
+  MOE_TOPK_CASE(24)
+  MOE_TOPK_CASE(32)
+#undef MOE_TOPK_CASE
+  return cudaErrorInvalidValue;
 }
 
 // W [E][d] fp32 -> [E][3d] bf16: hi = bf16(w), mid = bf16(w - hi), lo = bf16(w - hi - mid).  Each

@@ -23,8 +23,9 @@ struct TileInfo {
 };
 
 // Block-wide: fills tile_start[0..G] (exclusive prefix of tiles per group) and row_start[0..G]
-// (first row of each group).  Ends with __syncthreads().  Returns nothing; tile_start[G] is the
-// total number of tiles.
+// (row_start[g] = offsets[g] for the routed groups g <= n_routed, so that a routed group's row count
+// is row_start[g+1] - row_start[g] without touching global memory again).  Ends with
+// __syncthreads(); tile_start[G] is the total number of tiles.
 __device__ __forceinline__ void build_tile_table(int* tile_start, int* row_start,
                                                  int* scratch /* blockDim.x ints */,
                                                  const int32_t* offsets, int n_routed,
@@ -45,7 +46,8 @@ __device__ __forceinline__ void build_tile_table(int* tile_start, int* row_start
       rows = dense_rows;
     }
     rows = rows < 0 ? 0 : rows;
-    row_start[g] = r0;
+    if (g < n_routed) row_start[g] = r0;  // the dense group's entry is never read
+    if (g == n_routed - 1) row_start[n_routed] = offsets[n_routed];
     const int t = ((rows + rpt - 1) / rpt) * feat_tiles;
     tile_start[g] = t;  // count for now
     local += t;
@@ -90,7 +92,7 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int* tile_start,
     ti.grp_row0 = dense_row0;
   } else {
     ti.grp_row0 = row_start[lo];
-    ti.rows = offsets[lo + 1] - ti.grp_row0;
+    ti.rows = row_start[lo + 1] - ti.grp_row0;
   }
   const int nrt = (ti.rows + rpt - 1) / rpt;
   const int local = tile - tile_start[lo];

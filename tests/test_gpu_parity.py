@@ -247,6 +247,20 @@ def test_out_of_range_expert_index_is_flagged(cuda_device):
     assert int(pd[7 * w.k + 1]) == -1
 
 
+def test_expired_wait_is_reported_and_the_context_survives(cuda_device):
+    """The failure path without a GPU fault: the test flag withholds the expert GEMM's copies, its
+    bounded wait (50 ms) expires, the kernel returns with MOE_ERR_TIMEOUT in the device status;
+    the next normal call on the same context gives correct results."""
+    w = SMALL_BF16
+    layer = _layer(w, seed=11)
+    cfg = B.config_for(w, flags=ROWS | B.MOE_FLAG_TEST_STALL_EXPERTS)
+    ws = B.alloc_workspace(cfg)
+    out = torch.empty(w.T, w.d, dtype=torch.bfloat16, device="cuda")
+    B.moe_forward(cfg, layer.x, *B.layer_weights(layer), out, ws)
+    assert B.moe_device_status(ws) == B.MOE_ERR_TIMEOUT
+    _full_check(layer, ROWS)
+
+
 def test_launch_counter_counts_kernels(cuda_device):
     w = SMALL_BF16
     layer = _layer(w, seed=10)
