@@ -47,9 +47,12 @@ struct TcParams {
   const int32_t* offsets;
   int32_t n_routed, w_group_rows, u_off, u_off_d;
   int32_t dense_rows, dense_act_row0, dense_out_row0;
-  int32_t K, k_wrap, F;
+  int32_t K, k_wrap, F;          // routed groups
+  int32_t K_d, k_wrap_d, F_d;    // the dense group (its own reduction length and features)
   void* out;
   int64_t ldo;
+  void* out_d;                   // the dense group's output and row pitch
+  int64_t ldo_d;
   int32_t out_f32;
   const float* addend;  // EPI_STORE_ADD: fp32 [rows][ld_add]
   int64_t ld_add;
@@ -67,7 +70,9 @@ struct TcShape {
   static constexpr int OPB = kBN * 128;                                       // B bytes / stage
   static constexpr int STAGE = OPA + OPB;
   static constexpr int ACC_COLS = (kSwap && kSwiGLU) ? 2 * kBN : kBN;  // fp32 columns per tile
-  static constexpr int TMEM_NEED = 2 * ACC_COLS;
+  // two accumulators (the epilogue of tile i overlaps the mainloop of tile i+1) when they fit
+  static constexpr int NACC = 2 * ACC_COLS <= 512 ? 2 : 1;
+  static constexpr int TMEM_NEED = NACC * ACC_COLS;
   static constexpr int TMEM_COLS = TMEM_NEED <= 32    ? 32
                                    : TMEM_NEED <= 64  ? 64
                                    : TMEM_NEED <= 128 ? 128
@@ -131,14 +136,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
     tmem_relinquish();
   }
   build_tile_table(tile_start, row_start, scratch, p.offsets, p.n_routed, p.dense_rows, S::RPT,
-                   p.F / S::FPT);  // ends with __syncthreads
+                   p.F / S::FPT, p.F_d / S::FPT);  // ends with __syncthreads
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int G = p.n_routed + (p.dense_rows > 0 ? 1 : 0);
   const int total = tile_start[G];
-  const int nkb = p.K / kBK;
+  const int nkb_r = p.K / kBK, nkb_d = p.K_d / kBK;
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -154,6 +159,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
         const int act_y = ti.grp_row0 + ti.rt * S::RPT;
         const int w_y = (ti.dense ? 0 : ti.g * p.w_group_rows) + ti.ft * S::FPT;
         const int u_off = ti.dense ? p.u_off_d : p.u_off;
+        const int nkb = ti.dense ? nkb_d : nkb_r;
+        const int kwrap = ti.dense ? p.k_wrap_d : p.k_wrap;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, p.wait_ns)) {
             ok = false;
@@ -163,7 +170,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
           uint8_t* sb = sa + S::OPA;
           mbar_arrive_expect_tx(&full[stage], S::STAGE);
           const int kx = kb * kBK;
-          const int ax = kx % p.k_wrap;
+          const int ax = kx % kwrap;
           if (!kSwap) {
             tma_load_2d(sa, ma, &full[stage], ax, act_y);
             if (S::kSwiGLU) {
@@ -201,10 +208,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t kIdesc = idesc_bf16_f32<128, kBN>();
+      constexpr uint32_t kIdesc = idesc_bf16_f32<128, (kBN > 256 ? 256 : kBN)>();
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+        const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
+                                        p.dense_rows, p.dense_act_row0, S::RPT);
+        const int nkb = ti.dense ? nkb_d : nkb_r;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * S::ACC_COLS;
@@ -220,6 +230,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
           for (int k16 = 0; k16 < kBK / 16; ++k16) {
             const uint32_t accum = (kb | k16) != 0;
             const uint64_t bdesc = sw128_kmajor_desc(sb + k16 * 32);
+            if constexpr (kBN > 256) {  // N = 384: an N = 256 and an N = 128 MMA side by side
+              const uint64_t adesc = sw128_kmajor_desc(sa + k16 * 32);
+              mma_bf16(d0, adesc, bdesc, idesc_bf16_f32<128, 256>(), accum);
+              mma_bf16(d0 + 256, adesc, sw128_kmajor_desc(sb + 2 * kBoxBytes + k16 * 32),
+                       idesc_bf16_f32<128, kBN - 256>(), accum);
+              continue;
+            }
             mma_bf16(d0, sw128_kmajor_desc(sa + k16 * 32), bdesc, kIdesc, accum);
             if (kSwap && S::kSwiGLU)
               mma_bf16(d0 + kBN, sw128_kmajor_desc(sa + kBoxBytes + k16 * 32), bdesc, kIdesc,
@@ -233,7 +250,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
         }
         if (!ok) break;
         mma_commit(&tfull[acc]);
-        acc ^= 1u;
+        if (S::NACC == 2) acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       // every MMA issued above has completed once this commit arrives
@@ -256,11 +273,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
       const uint32_t tb = tmem_base + acc * S::ACC_COLS + ((uint32_t)(quarter * 32) << 16);
       const int64_t out_row0 = (ti.dense ? (int64_t)p.dense_out_row0 : (int64_t)ti.grp_row0) +
                                (int64_t)ti.rt * S::RPT;
+      void* const out = ti.dense ? p.out_d : p.out;
+      const int64_t ldo = ti.dense ? p.ldo_d : p.ldo;
       if (!kSwap) {
         const bool valid = r < ti.valid;
         const int64_t orow = out_row0 + r;
         if (S::kSwiGLU) {
-          __nv_bfloat16* dst = (__nv_bfloat16*)p.out + orow * p.ldo + (int64_t)ti.ft * S::FPT;
+          __nv_bfloat16* dst = (__nv_bfloat16*)out + orow * ldo + (int64_t)ti.ft * S::FPT;
 #pragma unroll 1
           for (int c = 0; c < S::FPT; c += 16) {
             uint32_t g[16], u[16];
@@ -290,7 +309,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
             tmem_ld_wait();
             if (valid) {
               if (p.out_f32) {
-                float4* d4 = reinterpret_cast<float4*>((float*)p.out + orow * p.ldo + col0 + c);
+                float4* d4 = reinterpret_cast<float4*>((float*)out + orow * ldo + col0 + c);
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                   d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
@@ -314,7 +333,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
                 uint32_t pk[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-                uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)p.out + orow * p.ldo + col0 + c);
+                uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)out + orow * ldo + col0 + c);
                 d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
               }
@@ -337,10 +356,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
               float v = __uint_as_float(g[i]);
               if (S::kSwiGLU) v = silu_fast(v) * __uint_as_float(u[i]);
               if (p.out_f32) {
-                ((float*)p.out)[orow * p.ldo + feat] = v;
+                ((float*)out)[orow * ldo + feat] = v;
               } else {
                 if (kEpi == EPI_STORE_ADD) v += p.addend[orow * p.ld_add + feat];
-                ((__nv_bfloat16*)p.out)[orow * p.ldo + feat] = __float2bfloat16_rn(v);
+                ((__nv_bfloat16*)out)[orow * ldo + feat] = __float2bfloat16_rn(v);
               }
             }
           }
@@ -348,7 +367,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
       }
       tc_fence_before();
       mbar_arrive(&tempty[acc]);
-      acc ^= 1u;
+      if (S::NACC == 2) acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
   }
@@ -420,6 +439,8 @@ static cudaError_t launch_variant(const TcParams& p, int grid, cudaStream_t st, 
 bool gemm_tc_supported(const GroupedGemm& g, int swap) {
   if (g.act_dtype != MOE_BF16 || g.w_dtype != MOE_BF16) return false;
   if (g.K <= 0 || g.K % kBK) return false;
+  if (g.K_d % kBK || (g.F_d && g.F_d % (g.epi == EPI_SWIGLU || swap ? 128 : 256))) return false;
+  if (g.out_d && g.ldo_d % 8) return false;
   const int kw = g.k_wrap > 0 ? g.k_wrap : g.K;
   if (kw % kBK || g.K % kw) return false;
   if (g.n_routed > kTcMaxGroups - 1) return false;
@@ -447,10 +468,12 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
     if (!make_map_bf16(&p.map_act, g.act, g.act_rows, kw, act_box)) return cudaErrorInvalidValue;
     if (!make_map_bf16(&p.map_w, g.w, g.w_rows, g.K, 128)) return cudaErrorInvalidValue;
   }
+  const int K_d = g.K_d > 0 ? g.K_d : g.K;
+  const int kw_d = g.k_wrap_d > 0 ? g.k_wrap_d : (g.K_d > 0 ? g.K_d : kw);
   if (g.dense_rows > 0) {
-    if (!make_map_bf16(&p.map_act_d, g.act_d, g.act_d_rows, kw, act_box))
+    if (!make_map_bf16(&p.map_act_d, g.act_d, g.act_d_rows, kw_d, act_box))
       return cudaErrorInvalidValue;
-    if (!make_map_bf16(&p.map_w_d, g.w_d, g.w_d_rows, g.K, 128)) return cudaErrorInvalidValue;
+    if (!make_map_bf16(&p.map_w_d, g.w_d, g.w_d_rows, K_d, 128)) return cudaErrorInvalidValue;
   }
   if (g.n_routed == 0) {  // keep the unused maps valid objects
     p.map_act = p.map_act_d;
@@ -471,8 +494,13 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
   p.K = g.K;
   p.k_wrap = kw;
   p.F = g.F;
+  p.K_d = K_d;
+  p.k_wrap_d = kw_d;
+  p.F_d = g.F_d > 0 ? g.F_d : g.F;
   p.out = g.out;
   p.ldo = g.ldo;
+  p.out_d = g.out_d ? g.out_d : g.out;
+  p.ldo_d = g.out_d ? g.ldo_d : g.ldo;
   p.out_f32 = g.out_dtype == MOE_F32;
   p.addend = (const float*)g.addend;
   p.ld_add = g.ld_add;
@@ -482,6 +510,7 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
   const int grid = num_sms;
   if (!swap) {
     if (g.epi == EPI_SWIGLU) return launch_variant<false, 256, EPI_SWIGLU>(p, grid, st, g.label);
+    if (f32_router && g.F % 384 == 0) return launch_variant<false, 384, EPI_STORE>(p, grid, st, g.label);
     if (f32_router) return launch_variant<false, 128, EPI_STORE>(p, grid, st, g.label);
     if (g.epi == EPI_STORE) return launch_variant<false, 256, EPI_STORE>(p, grid, st, g.label);
     return launch_variant<false, 256, EPI_STORE_ADD>(p, grid, st, g.label);

@@ -45,6 +45,12 @@ struct GroupedGemm {
   int K = 0;
   int k_wrap = 0;  // activation column = k mod k_wrap (3-way split router); K when unused
   int F = 0;       // output features per group
+  // the dense group's own reduction length, features and output (0 / null: as the routed ones)
+  int K_d = 0;
+  int k_wrap_d = 0;
+  int F_d = 0;
+  void* out_d = nullptr;
+  int64_t ldo_d = 0;
   int epi = EPI_STORE;
   int act_dtype = MOE_BF16;
   int w_dtype = MOE_BF16;

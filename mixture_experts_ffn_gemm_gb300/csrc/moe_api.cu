@@ -453,8 +453,11 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
   e = launch_gather_rows(route_src, perm_src, P, c->k, de, (int)ab, x_perm, x.sms, x.st);
   if (e != cudaSuccess) return from_cuda(e);
 
-  // W1 | W3 with the SwiGLU epilogue -> h [P + T][I]
-  const bool fuse_shared = c->n_shared && !x.pl.latent;
+  // W1 | W3 with the SwiGLU epilogue -> h [P + T][I]; the shared expert is the trailing dense
+  // group of the same launch (on the K3 path with its own reduction length d, since it reads the
+  // full-width x while the routed experts read the latent)
+  const bool fuse_shared = c->n_shared && (x.pl.tc || !x.pl.latent);
+  void* y_sh = static_cast<uint8_t*>(y_perm) + (size_t)P * de * 4;
   {
     GroupedGemm g;
     g.act = x_perm;
@@ -473,6 +476,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
       g.dense_rows = (int)T;
       g.dense_out_row0 = (int)P;
       g.u_off_d = I;
+      if (x.pl.latent) g.K_d = d;
     }
     g.K = de;
     g.k_wrap = de;
@@ -505,6 +509,12 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
       g.w_d_rows = d;
       g.dense_rows = (int)T;
       g.dense_out_row0 = (int)P;
+      if (x.pl.latent) {  // shared outputs are full width, in their own region after y_perm
+        g.F_d = d;
+        g.out_d = y_sh;
+        g.ldo_d = d;
+        g.dense_out_row0 = 0;
+      }
     }
     g.K = I;
     g.k_wrap = I;
@@ -516,47 +526,6 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.out_dtype = MOE_F32;
     g.err = x.err;
     e = gemm(x, g, "gemm2_rows", "gemm2_swap", "gemm2_simt");
-    if (e != cudaSuccess) return from_cuda(e);
-  }
-  if (c->n_shared && x.pl.latent) {  // shared expert on the full-width input
-    void* h_sh = static_cast<uint8_t*>(h) + (size_t)P * I * ab;
-    void* y_sh = static_cast<uint8_t*>(y_perm) + (size_t)P * de * 4;
-    GroupedGemm g;
-    g.act_d = xin;
-    g.act_d_rows = T;
-    g.w_d = Ws13;
-    g.w_d_rows = 2 * I;
-    g.dense_rows = (int)T;
-    g.u_off_d = I;
-    g.K = d;
-    g.k_wrap = d;
-    g.F = I;
-    g.epi = EPI_SWIGLU;
-    g.act_dtype = g.w_dtype = c->act_dtype;
-    g.out = h_sh;
-    g.ldo = I;
-    g.out_dtype = c->act_dtype;
-    g.err = x.err;
-    g.label = "shared_gemm13_swiglu";
-    e = launch_gemm_tc(g, 0, x.sms, x.st);
-    if (e != cudaSuccess) return from_cuda(e);
-    GroupedGemm g2;
-    g2.act_d = h_sh;
-    g2.act_d_rows = T;
-    g2.w_d = Ws2;
-    g2.w_d_rows = d;
-    g2.dense_rows = (int)T;
-    g2.K = I;
-    g2.k_wrap = I;
-    g2.F = d;
-    g2.epi = EPI_STORE;
-    g2.act_dtype = g2.w_dtype = c->act_dtype;
-    g2.out = y_sh;
-    g2.ldo = d;
-    g2.out_dtype = MOE_F32;
-    g2.err = x.err;
-    g2.label = "shared_gemm2";
-    e = launch_gemm_tc(g2, 0, x.sms, x.st);
     if (e != cudaSuccess) return from_cuda(e);
   }
   return MOE_OK;

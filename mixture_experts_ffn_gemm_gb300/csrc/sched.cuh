@@ -29,7 +29,8 @@ struct TileInfo {
 __device__ __forceinline__ void build_tile_table(int* tile_start, int* row_start,
                                                  int* scratch /* blockDim.x ints */,
                                                  const int32_t* offsets, int n_routed,
-                                                 int dense_rows, int rpt, int feat_tiles) {
+                                                 int dense_rows, int rpt, int feat_tiles,
+                                                 int feat_tiles_d = -1) {
   const int G = n_routed + (dense_rows > 0 ? 1 : 0);
   const int nt = blockDim.x;
   const int per = (G + nt - 1) / nt;
@@ -48,7 +49,8 @@ __device__ __forceinline__ void build_tile_table(int* tile_start, int* row_start
     rows = rows < 0 ? 0 : rows;
     if (g < n_routed) row_start[g] = r0;  // the dense group's entry is never read
     if (g == n_routed - 1) row_start[n_routed] = offsets[n_routed];
-    const int t = ((rows + rpt - 1) / rpt) * feat_tiles;
+    const int ft = (g < n_routed || feat_tiles_d < 0) ? feat_tiles : feat_tiles_d;
+    const int t = ((rows + rpt - 1) / rpt) * ft;
     tile_start[g] = t;  // count for now
     local += t;
   }
