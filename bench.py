@@ -57,6 +57,8 @@ def parse_args():
     ap.add_argument("--experts", type=int, default=0,
                     help="override the routed expert count (small profiling cases)")
     ap.add_argument("--tokens", type=int, default=0, help="override the token count")
+    ap.add_argument("--flags", type=lambda v: int(v, 0), default=0,
+                    help="moe_config_t.flags tuning overrides (MOE_FLAG_*)")
     return ap.parse_args()
 
 
@@ -249,7 +251,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     layer = S.make_layer(w, seed=0, device=dev)
-    cfg = B.config_for(w)
+    cfg = B.config_for(w, flags=args.flags)
     ws = B.alloc_workspace(cfg, dev)
     out = torch.empty(w.T, w.d, dtype=layer.x.dtype, device=dev)
     weights = B.layer_weights(layer)

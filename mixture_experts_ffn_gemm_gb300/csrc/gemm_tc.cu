@@ -80,14 +80,38 @@ struct TcShape {
                                                       : 512;
   static constexpr int TABLE_BYTES = 2 * (kTcMaxGroups + 1) * 4 + kTcThreads * 4;
   static constexpr int BAR_BYTES = 256 + 64;  // barriers, TMEM base, abort flag
-  static constexpr int STAGES_FIT = (kSmemLimit - 1024 - TABLE_BYTES - BAR_BYTES) / STAGE;
+  // token-rows epilogues stage each warp's 32 rows x 128 bytes through shared memory so that
+  // the global stores are whole rows (4 KB per epilogue warp)
+  static constexpr bool kStaged = !kSwap && kEpi != EPI_STORE_ADD;
+  static constexpr int STAGING = kStaged ? 4 * 4096 : 0;
+  static constexpr int STAGES_FIT =
+      (kSmemLimit - 1024 - TABLE_BYTES - BAR_BYTES - STAGING) / STAGE;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int SMEM = 1024 + STAGES * STAGE + BAR_BYTES + TABLE_BYTES;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + BAR_BYTES + TABLE_BYTES + STAGING;
   static_assert(STAGES >= 2, "not enough shared memory for two stages");
   static_assert(TMEM_NEED <= 512, "accumulators exceed TMEM");
   static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment for SWIZZLE_128B");
   static_assert(2 * STAGES + 5 <= 32, "barrier area too small");
 };
+
+// One epilogue warp writes a chunk of 32 rows x 128 bytes: lane l holds row l's 128 bytes in v.
+// The chunk goes through a 4 KB shared buffer (16-byte pieces XOR-swizzled by row % 8, free of
+// bank conflicts both ways) and leaves as 4 whole 128-byte rows per store instruction.
+__device__ __forceinline__ void store_rows_128B(uint8_t* buf, int lane, const uint4 (&v)[8],
+                                                uint8_t* row0, int64_t pitch, int valid_rows) {
+  __syncwarp();  // the previous chunk's read-back has finished
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = v[j];
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = i * 4 + (lane >> 3);
+    const int j = lane & 7;
+    const uint4 w = *reinterpret_cast<const uint4*>(buf + r * 128 + ((j ^ (r & 7)) << 4));
+    if (r < valid_rows) *reinterpret_cast<uint4*>(row0 + r * pitch + j * 16) = w;
+  }
+}
 
 template <bool kSwap, int kBN, int kEpi>
 __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid_constant__ TcParams p) {
@@ -106,6 +130,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
   int* tile_start = reinterpret_cast<int*>(smem + S::STAGES * S::STAGE + S::BAR_BYTES);
   int* row_start = tile_start + (kTcMaxGroups + 1);
   int* scratch = row_start + (kTcMaxGroups + 1);
+  uint8_t* staging = smem + S::STAGES * S::STAGE + S::BAR_BYTES + S::TABLE_BYTES;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -275,69 +300,110 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
                                (int64_t)ti.rt * S::RPT;
       void* const out = ti.dense ? p.out_d : p.out;
       const int64_t ldo = ti.dense ? p.ldo_d : p.ldo;
-      if (!kSwap) {
-        const bool valid = r < ti.valid;
-        const int64_t orow = out_row0 + r;
-        if (S::kSwiGLU) {
-          __nv_bfloat16* dst = (__nv_bfloat16*)out + orow * ldo + (int64_t)ti.ft * S::FPT;
+      if (!kSwap && S::kStaged) {
+        uint8_t* buf = staging + (warp - 2) * 4096;
+        const int vrows = min(32, max(0, ti.valid - quarter * 32));
+        const int64_t row0 = out_row0 + quarter * 32;
+        if (S::kSwiGLU) {  // h in bf16: chunks of 64 features = 128 bytes per row
 #pragma unroll 1
-          for (int c = 0; c < S::FPT; c += 16) {
-            uint32_t g[16], u[16];
-            tmem_ld16(tb + c, g);
-            tmem_ld16(tb + S::FPT + c, u);
-            tmem_ld_wait();
-            if (valid) {
-              uint32_t pk[8];
+          for (int c = 0; c < S::FPT; c += 64) {
+            uint4 v[8];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              uint32_t g0[16], u0[16], g1[16], u1[16];
+              tmem_ld16(tb + c + 32 * h, g0);
+              tmem_ld16(tb + S::FPT + c + 32 * h, u0);
+              tmem_ld16(tb + c + 32 * h + 16, g1);
+              tmem_ld16(tb + S::FPT + c + 32 * h + 16, u1);
+              tmem_ld_wait();
+              uint32_t pk[16];
 #pragma unroll
               for (int i = 0; i < 8; ++i) {
-                const float h0 = silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
-                const float h1 =
-                    silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-                pk[i] = pack_bf16x2(h0, h1);
+                pk[i] = pack_bf16x2(
+                    silu_fast(__uint_as_float(g0[2 * i])) * __uint_as_float(u0[2 * i]),
+                    silu_fast(__uint_as_float(g0[2 * i + 1])) * __uint_as_float(u0[2 * i + 1]));
+                pk[8 + i] = pack_bf16x2(
+                    silu_fast(__uint_as_float(g1[2 * i])) * __uint_as_float(u1[2 * i]),
+                    silu_fast(__uint_as_float(g1[2 * i + 1])) * __uint_as_float(u1[2 * i + 1]));
               }
-              uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-              d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-              d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                v[4 * h + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
             }
+            uint8_t* dst = (uint8_t*)out + (row0 * ldo + (int64_t)ti.ft * S::FPT + c) * 2;
+            store_rows_128B(buf, lane, v, dst, ldo * 2, vrows);
           }
-        } else {
-          const int64_t col0 = (int64_t)ti.ft * S::FPT;
+        } else if (p.out_f32) {  // fp32: chunks of 32 columns
 #pragma unroll 1
-          for (int c = 0; c < S::FPT; c += 16) {
-            uint32_t v[16];
-            tmem_ld16(tb + c, v);
+          for (int c = 0; c < S::FPT; c += 32) {
+            uint32_t a[16], b[16];
+            tmem_ld16(tb + c, a);
+            tmem_ld16(tb + c + 16, b);
             tmem_ld_wait();
-            if (valid) {
-              if (p.out_f32) {
-                float4* d4 = reinterpret_cast<float4*>((float*)out + orow * ldo + col0 + c);
+            uint4 v[8];
 #pragma unroll
-                for (int i = 0; i < 4; ++i)
-                  d4[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                      __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
-              } else {
-                float f[16];
+            for (int q = 0; q < 4; ++q) {
+              v[q] = make_uint4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+              v[4 + q] = make_uint4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
+            }
+            uint8_t* dst = (uint8_t*)out + (row0 * ldo + (int64_t)ti.ft * S::FPT + c) * 4;
+            store_rows_128B(buf, lane, v, dst, ldo * 4, vrows);
+          }
+        } else {  // bf16: chunks of 64 columns
+#pragma unroll 1
+          for (int c = 0; c < S::FPT; c += 64) {
+            uint4 v[8];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
-                if (kEpi == EPI_STORE_ADD) {
-                  const float4* a4 =
-                      reinterpret_cast<const float4*>(p.addend + orow * p.ld_add + col0 + c);
+            for (int h = 0; h < 2; ++h) {
+              uint32_t a[16], b[16];
+              tmem_ld16(tb + c + 32 * h, a);
+              tmem_ld16(tb + c + 32 * h + 16, b);
+              tmem_ld_wait();
+              uint32_t pk[16];
 #pragma unroll
-                  for (int h = 0; h < 4; ++h) {
-                    const float4 av = __ldg(a4 + h);
-                    f[4 * h] += av.x;
-                    f[4 * h + 1] += av.y;
-                    f[4 * h + 2] += av.z;
-                    f[4 * h + 3] += av.w;
-                  }
-                }
-                uint32_t pk[8];
+              for (int i = 0; i < 8; ++i) {
+                pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+                pk[8 + i] = pack_bf16x2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
+              }
 #pragma unroll
-                for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
-                uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)out + orow * ldo + col0 + c);
-                d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+              for (int q = 0; q < 4; ++q)
+                v[4 * h + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+            }
+            uint8_t* dst = (uint8_t*)out + (row0 * ldo + (int64_t)ti.ft * S::FPT + c) * 2;
+            store_rows_128B(buf, lane, v, dst, ldo * 2, vrows);
+          }
+        }
+      } else if (!kSwap) {
+        // store + fp32 addend (bf16 out): one row per thread
+        const bool valid = r < ti.valid;
+        const int64_t orow = out_row0 + r;
+        const int64_t col0 = (int64_t)ti.ft * S::FPT;
+#pragma unroll 1
+        for (int c = 0; c < S::FPT; c += 16) {
+          uint32_t v[16];
+          tmem_ld16(tb + c, v);
+          tmem_ld_wait();
+          if (valid) {
+            float f[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) f[i] = __uint_as_float(v[i]);
+            if (kEpi == EPI_STORE_ADD) {
+              const float4* a4 = reinterpret_cast<const float4*>(p.addend + orow * p.ld_add + col0 + c);
+#pragma unroll
+              for (int h = 0; h < 4; ++h) {
+                const float4 av = __ldg(a4 + h);
+                f[4 * h] += av.x;
+                f[4 * h + 1] += av.y;
+                f[4 * h + 2] += av.z;
+                f[4 * h + 3] += av.w;
               }
             }
+            uint32_t pk[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) pk[i] = pack_bf16x2(f[2 * i], f[2 * i + 1]);
+            uint4* d4 = reinterpret_cast<uint4*>((__nv_bfloat16*)out + orow * ldo + col0 + c);
+            d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
         }
       } else {
@@ -462,6 +528,8 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
   TcParams p;
   memset(&p, 0, sizeof(p));
   const bool f32_router = !swap && g.epi == EPI_STORE && g.out_dtype == MOE_F32 && g.F % 256;
+  if (g.n128 && g.epi == EPI_STORE && (g.F % 128 || (g.F_d && g.F_d % 128)))
+    return cudaErrorInvalidValue;
   const int act_box = swap ? 32 : 128;
   const int kw = g.k_wrap > 0 ? g.k_wrap : g.K;
   if (g.n_routed > 0) {
@@ -511,7 +579,8 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
   if (!swap) {
     if (g.epi == EPI_SWIGLU) return launch_variant<false, 256, EPI_SWIGLU>(p, grid, st, g.label);
     if (f32_router && g.F % 384 == 0) return launch_variant<false, 384, EPI_STORE>(p, grid, st, g.label);
-    if (f32_router) return launch_variant<false, 128, EPI_STORE>(p, grid, st, g.label);
+    if (f32_router || (g.n128 && g.epi == EPI_STORE))
+      return launch_variant<false, 128, EPI_STORE>(p, grid, st, g.label);
     if (g.epi == EPI_STORE) return launch_variant<false, 256, EPI_STORE>(p, grid, st, g.label);
     return launch_variant<false, 256, EPI_STORE_ADD>(p, grid, st, g.label);
   }

@@ -66,6 +66,7 @@ struct GroupedGemm {
   uint32_t* err = nullptr;
   const char* label = "gemm";  // kernel name for the launch profiler
   bool test_stall = false;     // test hook (MOE_FLAG_TEST_STALL_EXPERTS): see moe.h
+  bool n128 = false;           // token-rows store tiles with N = 128 (MOE_FLAG_GEMM_N128)
 };
 
 // Tensor-core grouped GEMM (tcgen05 + TMA), bf16 operands, fp32 accumulation in TMEM.

@@ -525,6 +525,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.ldo = de;
     g.out_dtype = MOE_F32;
     g.err = x.err;
+    g.n128 = (c->flags & MOE_FLAG_GEMM_N128) != 0;
     e = gemm(x, g, "gemm2_rows", "gemm2_swap", "gemm2_simt");
     if (e != cudaSuccess) return from_cuda(e);
   }
