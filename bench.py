@@ -36,8 +36,15 @@ METRIC = "MoE-layer tokens/s (d=7168, 384 experts top-8) and % of roofline (HBM 
 # profiles/ (dram__bytes_read.sum + dram__bytes_write.sum of one launch over the algorithmic bytes
 # of that launch).  A kernel changed since its capture must be dropped from this table.
 MEASURED_TRAFFIC_RATIO = {
-    "gemm13_swiglu_swap": (1.003, "profiles/gemm_tc_swap_decode_E32.md"),
-    "gemm2_swap": (0.994, "profiles/gemm_tc_swap_decode_E32.md"),
+    "gemm13_swiglu_swap": (1.004, "profiles/gemm_tc_swap_decode_E32.md", "a 32-expert decode capture"),
+    "gemm2_swap": (0.994, "profiles/gemm_tc_swap_decode_E32.md", "a 32-expert decode capture"),
+    "gemm13_swiglu_rows": (1.099, "profiles/gemm_tc_rows_prefill_E64_T4096.md",
+                           "a 64-expert, 4096-token prefill capture"),
+    "gemm2_rows": (0.984, "profiles/gemm_tc_rows_prefill_E64_T4096.md",
+                   "a 64-expert, 4096-token prefill capture"),
+    "gemm13_swiglu_fp8": (1.51, "profiles/gemm_fp8_E64_T4096.md",
+                          "a 64-expert, 4096-token fp8 capture"),
+    "gemm2_fp8": (1.03, "profiles/gemm_fp8_E64_T4096.md", "a 64-expert, 4096-token fp8 capture"),
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -369,7 +376,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         roof["traffic"] = ratio[0] * by[unit_key] if ratio else None
         if ratio:
             roof["traffic_source"] = (f"{ratio[1]}: ncu DRAM bytes / algorithmic bytes = "
-                                      f"{ratio[0]} on a 32-expert capture, scaled to this launch")
+                                      f"{ratio[0]} on {ratio[2]}, scaled to this launch")
     else:
         roof = None
     t_tc = fl["layer"] / (tc_peak * 1e12)
