@@ -9,19 +9,21 @@
 //
 // Kernel shape: persistent, one CTA per SM, 320 threads:
 //   warp 0      TMA producer: one K-block (128 e4m3 = one 128-byte swizzle row) per stage;
-//   warp 1      MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (K = 32 each) per K-block into one of two
-//               TMEM partial buffers (M = 128 rows x N = 256 columns), commit -> partial_full;
-//   warps 2..9  epilogue/promotion: two warps per TMEM lane quarter, each owning 128 of the 256
-//               columns; per K-block they read the partial, multiply by the row's activation
-//               scale times the block's weight scale and add into 128 fp32 registers, then free
-//               the buffer, so the MMA of block kb+1 overlaps the promotion of block kb.
+//   warp 1      MMA issuer: per K-block two products, one per 128-row weight box, each 4 x
+//               tcgen05.mma kind::f8f6f4 (M = 128, N = 128, K = 32) into the next slot of a ring
+//               of four 128-column TMEM partial buffers, commit -> partial_full[slot];
+//   warps 2..9  epilogue/promotion: two warps per TMEM lane quarter; warp half h owns columns
+//               [64h, 64h + 64) of every slot.  Per slot they read the partial, multiply by the
+//               row's activation scale times the box's weight scale and add into fp32 registers,
+//               then free the slot.  With four slots the MMA runs up to two K-blocks ahead of the
+//               promotion, so the two overlap.
 // Tiles are token rows (M = 128) x 256 weight rows, as in the bf16 rows orientation:
-//   SwiGLU: columns 0..127 are the W1 rows of 128 features, 128..255 the W3 rows of the same
+//   SwiGLU: the first box holds the W1 rows of 128 features, the second the W3 rows of the same
 //           features; warp half 0 owns features 0..63 (g and u), half 1 features 64..127.  The
 //           epilogue forms h = SiLU(g) * u and quantises it per row per 128 features -- exactly one
 //           tile -- to e4m3 with scale amax/448 (the two halves exchange their amax).
-//   store:  half 0 owns output features 0..127 (weight block 0), half 1 128..255 (block 1);
-//           fp32 output.
+//   store:  the boxes are weight blocks 2 ft and 2 ft + 1 (output features 0..127 and
+//           128..255 of the tile); fp32 output, written through a per-warp staging buffer.
 // Every wait is bounded as in the bf16 kernel.
 #include <cstring>
 #include <mutex>
@@ -42,7 +44,13 @@ constexpr int kF8Table = 2 * (kF8MaxGroups + 1) * 4 + kF8Threads * 4;
 constexpr int kF8Bars = 256 + 64;
 constexpr int kF8Xchg = 2 * 2 * 128 * 4;  // [tile parity][half][row] amax exchange
 constexpr int kF8Stages = 4;
-constexpr int kF8Smem = 1024 + kF8Stages * kF8Stage + kF8Bars + kF8Xchg + kF8Table;
+// Partial products per K-block: 1 = one N = 256 product into a ring of two 256-column TMEM
+// buffers; 2 = one N = 128 product per 128-row weight box into a ring of four 128-column slots.
+constexpr int kF8SPK = 1;
+constexpr int kF8SlotCols = 256 / kF8SPK;
+constexpr int kF8Slots = 512 / kF8SlotCols;
+constexpr int kF8Staging = 8 * 2048;     // 2 KB per epilogue warp for row-contiguous stores
+constexpr int kF8Smem = 1024 + kF8Stages * kF8Stage + kF8Bars + kF8Xchg + kF8Table + kF8Staging;
 static_assert(kF8Smem <= 232448, "fp8 GEMM shared memory");
 
 struct F8Params {
@@ -71,6 +79,81 @@ __device__ __forceinline__ uint32_t e4m3x4_pack(float a, float b, float c, float
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
+// Warp-cooperative store of 32 rows x 64 bytes (lane l holds row l) through a 2 KB XOR-swizzled
+// shared buffer: each store instruction then writes 8 whole 64-byte row pieces instead of 32
+// scattered 16-byte ones.  Rows >= valid_rows are not written.
+__device__ __forceinline__ void store_rows_64B(uint8_t* buf, int lane, const uint4 (&v)[4],
+                                               uint8_t* row0, int pitch, int valid_rows) {
+  __syncwarp();  // the previous chunk's read-back has finished
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    *reinterpret_cast<uint4*>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) = v[j];
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = i * 8 + (lane >> 2);
+    const int j = lane & 3;
+    const uint4 w = *reinterpret_cast<const uint4*>(buf + r * 64 + ((j ^ ((r >> 1) & 3)) << 4));
+    if (r < valid_rows) *reinterpret_cast<uint4*>(row0 + (r * pitch + j * 16)) = w;
+  }
+}
+
+// RN(x / s) from y = RN(1 / s): q0 = RN(x * y), the exact remainder r = x - s * q0 (one fma), then
+// RN(q0 + r * y).  By Markstein's theorem (P. Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990) this is the correctly rounded
+// quotient whenever the quotient is a normal number, i.e. the same value as an IEEE division.
+__device__ __forceinline__ float div_rn_by_recip(float x, float s, float y) {
+  const float q0 = x * y;
+  const float r = fmaf(-s, q0, x);
+  return fmaf(r, y, q0);
+}
+
+// SiLU for the fp8 epilogue: the quotient with the fast division (h is quantised to e4m3 next)
+__device__ __forceinline__ float silu_fp8(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
+
+// One promotion step of a warp: wait for partial product ks (slot ks % kF8Slots), which holds
+// weight boxes BOX0 .. BOX0 + kF8SlotCols / 128 - 1; add s_box * partial[box column c] into
+// acc[box * 64 + c] for this thread's 64 columns of each box (tq addresses its lane and first
+// column; box 0 is scaled by s0, box 1 by s1), then release the slot.  False when the wait gave
+// up.
+template <int BOX0>
+__device__ __forceinline__ bool promote_slot(float (&acc)[128], float s0, float s1, uint32_t tq,
+                                             uint32_t ks,
+                                             uint64_t* pfull, uint64_t* pempty, int lane,
+                                             volatile int* abort_flag, uint32_t* err) {
+  const uint32_t slot = ks % kF8Slots, sph = (ks / kF8Slots) & 1u;
+  int w_ok = 1;
+  if (lane == 0) w_ok = mbar_wait(&pfull[slot], sph, abort_flag, err) ? 1 : 0;
+  w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+  if (!w_ok) return false;
+  tc_fence_after();
+  const uint32_t tb = tq + slot * kF8SlotCols;
+#pragma unroll
+  for (int j = 0; j < kF8SlotCols / 128; ++j) {  // the weight boxes this slot holds
+    constexpr int kBase = BOX0 * 64;
+    const float sc = (BOX0 + j) ? s1 : s0;
+#pragma unroll
+    for (int c = 0; c < 64; c += 32) {
+      uint32_t v0[16], v1[16];
+      tmem_ld16(tb + j * 128 + c, v0);
+      tmem_ld16(tb + j * 128 + c + 16, v1);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 16; i += 2) {
+        fma2(acc[kBase + j * 64 + c + i], acc[kBase + j * 64 + c + i + 1], sc, v0[i], v0[i + 1]);
+        fma2(acc[kBase + j * 64 + c + 16 + i], acc[kBase + j * 64 + c + 16 + i + 1], sc, v1[i],
+             v1[i + 1]);
+      }
+    }
+  }
+  // every lane's loads of this slot have completed (tcgen05.wait::ld); one arrival per warp
+  // after a warp barrier releases the slot to the MMA issuer
+  tc_fence_before();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&pempty[slot]);
+  return true;
+}
+
 template <bool kSwiGLU>
 __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __grid_constant__ F8Params p) {
   extern __shared__ uint8_t smem_raw[];
@@ -79,9 +162,9 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kF8Stages * kF8Stage);
   uint64_t* full = bars;
   uint64_t* empty = bars + kF8Stages;
-  uint64_t* pfull = bars + 2 * kF8Stages;
-  uint64_t* pempty = pfull + 2;
-  uint64_t* drain = pempty + 2;
+  uint64_t* pfull = bars + 2 * kF8Stages;  // [kF8Slots]
+  uint64_t* pempty = pfull + kF8Slots;     // [kF8Slots]
+  uint64_t* drain = pempty + kF8Slots;
   uint64_t* xbar = drain + 1;  // [2]: amax exchange between the two epilogue halves
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
@@ -89,6 +172,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
   int* tile_start = reinterpret_cast<int*>(smem + kF8Stages * kF8Stage + kF8Bars + kF8Xchg);
   int* row_start = tile_start + (kF8MaxGroups + 1);
   int* scratch = row_start + (kF8MaxGroups + 1);
+  uint8_t* staging = smem + kF8Stages * kF8Stage + kF8Bars + kF8Xchg + kF8Table;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -99,13 +183,13 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < kF8Slots; ++b) {
       mbar_init(&pfull[b], 1);
-      mbar_init(&pempty[b], 256);
+      mbar_init(&pempty[b], 8);  // one arrival per promotion warp
     }
     mbar_init(drain, 1);
-    mbar_init(&xbar[0], 256);
-    mbar_init(&xbar[1], 256);
+    mbar_init(&xbar[0], 8);
+    mbar_init(&xbar[1], 8);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -129,17 +213,25 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------------------ TMA producer
+      // the boxes of (tile, kb): activation rows, then the two 128-row weight boxes
+      auto boxes = [&](const TileInfo& ti, const CUtensorMap*& ma, const CUtensorMap*& mw,
+                       int& act_y, int& w_y0, int& w_y1) {
+        ma = ti.dense ? &p.map_act_d : &p.map_act;
+        mw = ti.dense ? &p.map_w_d : &p.map_w;
+        act_y = ti.grp_row0 + ti.rt * 128;
+        w_y0 = (ti.dense ? 0 : ti.g * p.w_group_rows) + ti.ft * FPT;
+        w_y1 = kSwiGLU ? w_y0 + (ti.dense ? p.u_off_d : p.u_off) : w_y0 + 128;
+      };
       uint32_t stage = 0, phase = 0;
       int armed = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
                                         p.dense_rows, p.dense_act_row0, 128);
-        const CUtensorMap* ma = ti.dense ? &p.map_act_d : &p.map_act;
-        const CUtensorMap* mw = ti.dense ? &p.map_w_d : &p.map_w;
-        const int act_y = ti.grp_row0 + ti.rt * 128;
-        const int w_y = (ti.dense ? 0 : ti.g * p.w_group_rows) + ti.ft * FPT;
-        const int u_off = ti.dense ? p.u_off_d : p.u_off;
+        const CUtensorMap* ma;
+        const CUtensorMap* mw;
+        int act_y, w_y0, w_y1;
+        boxes(ti, ma, mw, act_y, w_y0, w_y1);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err)) {
             ok = false;
@@ -148,10 +240,10 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
           uint8_t* sa = smem + stage * kF8Stage;
           uint8_t* sb = sa + kF8Box;
           mbar_arrive_expect_tx(&full[stage], kF8Stage);
-          const int kx = kb * kF8BK;
+          const int kx = kb * (kF8BK / 8);  // in the maps' 8-byte elements
           tma_load_2d(sa, ma, &full[stage], kx, act_y);
-          tma_load_2d(sb, mw, &full[stage], kx, w_y);
-          tma_load_2d(sb + kF8Box, mw, &full[stage], kx, kSwiGLU ? w_y + u_off : w_y + 128);
+          tma_load_2d(sb, mw, &full[stage], kx, w_y0);
+          tma_load_2d(sb + kF8Box, mw, &full[stage], kx, w_y1);
           if (armed < kF8Stages) ++armed;
           if (++stage == kF8Stages) {
             stage = 0;
@@ -172,28 +264,37 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
     }
   } else if (warp == 1) {
     if (lane == 0) {  // ------------------------------------------------ MMA issuer
-      constexpr uint32_t kIdesc = idesc_e4m3_f32<128, kF8BN>();
+      constexpr uint32_t kIdesc = idesc_e4m3_f32<128, kF8SlotCols>();
       uint32_t stage = 0, phase = 0;
-      uint32_t kbg = 0;  // K-blocks issued so far (all tiles): buffer = kbg & 1
+      uint32_t ks = 0;  // partial products issued so far (all tiles): slot = ks % kF8Slots
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-        for (int kb = 0; kb < nkb; ++kb, ++kbg) {
-          const uint32_t buf = kbg & 1u, bph = (kbg >> 1) & 1u;
-          if (!mbar_wait(&pempty[buf], bph ^ 1u, abort_flag, p.err) ||
-              !mbar_wait(&full[stage], phase, abort_flag, p.err)) {
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+          if (!mbar_wait(&full[stage], phase, abort_flag, p.err)) {
             ok = false;
             break;
           }
-          tc_fence_after();
           const uint32_t sa = smem_u32(smem + stage * kF8Stage);
-          const uint32_t sb = sa + kF8Box;
-          const uint32_t d = tmem_base + buf * kF8BN;
+          // the K-block's two 128-row weight boxes go to two slots, so that the promotion can
+          // free one slot while the MMA fills the next ones
+#pragma unroll 1
+          for (int hb = 0; hb < kF8SPK; ++hb, ++ks) {
+            const uint32_t slot = ks % kF8Slots, sph = (ks / kF8Slots) & 1u;
+            if (!mbar_wait(&pempty[slot], sph ^ 1u, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t sb = sa + kF8Box + hb * (kF8SlotCols / 128) * kF8Box;
+            const uint32_t d = tmem_base + slot * kF8SlotCols;
 #pragma unroll
-          for (int k32 = 0; k32 < kF8BK / 32; ++k32)
-            mma_e4m3(d, sw128_kmajor_desc(sa + k32 * 32), sw128_kmajor_desc(sb + k32 * 32), kIdesc,
-                     k32 != 0);
+            for (int k32 = 0; k32 < kF8BK / 32; ++k32)
+              mma_e4m3(d, sw128_kmajor_desc(sa + k32 * 32), sw128_kmajor_desc(sb + k32 * 32),
+                       kIdesc, k32 != 0);
+            mma_commit(&pfull[slot]);
+          }
+          if (!ok) break;
           mma_commit(&empty[stage]);
-          mma_commit(&pfull[buf]);
           if (++stage == kF8Stages) {
             stage = 0;
             phase ^= 1u;
@@ -208,18 +309,20 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
-    uint32_t kbg = 0;
+    uint8_t* wbuf = staging + (warp - 2) * 2048;
+    uint32_t ks = 0;  // partial products consumed so far (all tiles), as counted by the MMA issuer
     uint32_t it = 0;  // tiles finished by this thread: exchange slot it & 1
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
       const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
                                       p.dense_rows, p.dense_act_row0, 128);
       const bool valid = r < ti.valid;
+      const int vrows = ti.valid - quarter * 32;  // rows of this warp's 32 that are real
       const int64_t act_row = (int64_t)ti.grp_row0 + ti.rt * 128 + r;
       const float* sx_col = ti.dense ? p.act_sT_d : p.act_sT;
       const int64_t sx_ld = ti.dense ? p.act_s_ld_d : p.act_s_ld;
       const int wblocks = p.w_group_rows / 128;
-      // weight scale rows of the two 128-row halves this warp reads
+      // weight-scale rows of the tile's two 128-row weight boxes (slot hb = 0 and hb = 1)
       const float* ws0;
       const float* ws1;
       if (kSwiGLU) {
@@ -229,10 +332,9 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
         ws0 = base + (int64_t)rb_g * nkb;
         ws1 = base + (int64_t)rb_u * nkb;
       } else {
-        const int rb = ti.ft * 2 + half;
         const float* base = ti.dense ? p.w_s_d : p.w_s + (int64_t)ti.g * wblocks * nkb;
-        ws0 = base + (int64_t)rb * nkb;
-        ws1 = ws0;
+        ws0 = base + (int64_t)(ti.ft * 2) * nkb;
+        ws1 = ws0 + nkb;
       }
       float acc[128];
 #pragma unroll
@@ -242,54 +344,24 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
       const float* sx_ptr = sx_col + act_row;
       float sx_n = valid ? __ldg(sx_ptr) : 0.0f;
       float w0_n = __ldg(ws0), w1_n = __ldg(ws1);
-      for (int kb = 0; kb < nkb; ++kb, ++kbg) {
+      for (int kb = 0; kb < nkb && ok; ++kb) {
         const float sx = sx_n, w0 = w0_n, w1 = w1_n;
         if (kb + 1 < nkb) {
           sx_n = valid ? __ldg(sx_ptr + (int64_t)(kb + 1) * sx_ld) : 0.0f;
           w0_n = __ldg(ws0 + kb + 1);
           w1_n = __ldg(ws1 + kb + 1);
         }
-        const uint32_t buf = kbg & 1u, bph = (kbg >> 1) & 1u;
-        int w_ok = 1;
-        if (lane == 0) w_ok = mbar_wait(&pfull[buf], bph, abort_flag, p.err) ? 1 : 0;
-        w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-        if (!w_ok) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const float s0 = sx * w0;
-        const float s1 = sx * w1;
-        const uint32_t tb = tmem_base + buf * kF8BN + ((uint32_t)(quarter * 32) << 16);
-        if (kSwiGLU) {
-#pragma unroll
-          for (int c = 0; c < 64; c += 16) {
-            uint32_t g[16], u[16];
-            tmem_ld16(tb + half * 64 + c, g);
-            tmem_ld16(tb + 128 + half * 64 + c, u);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-              fma2(acc[c + i], acc[c + i + 1], s0, g[i], g[i + 1]);
-              fma2(acc[64 + c + i], acc[64 + c + i + 1], s1, u[i], u[i + 1]);
-            }
-          }
+        // this thread owns columns [half * 64, half * 64 + 64) of both slots of the K-block:
+        // acc[0..63] from the first weight box, acc[64..127] from the second
+        const uint32_t tq = tmem_base + half * 64 + ((uint32_t)(quarter * 32) << 16);
+        const float s0 = sx * w0, s1 = sx * w1;
+        if constexpr (kF8SPK == 1) {
+          ok = promote_slot<0>(acc, s0, s1, tq, ks, pfull, pempty, lane, abort_flag, p.err);
         } else {
-#pragma unroll
-          for (int c = 0; c < 128; c += 32) {
-            uint32_t v0[16], v1[16];
-            tmem_ld16(tb + half * 128 + c, v0);
-            tmem_ld16(tb + half * 128 + c + 16, v1);
-            tmem_ld_wait();
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-              fma2(acc[c + i], acc[c + i + 1], s0, v0[i], v0[i + 1]);
-              fma2(acc[c + 16 + i], acc[c + 16 + i + 1], s0, v1[i], v1[i + 1]);
-            }
-          }
+          ok = promote_slot<0>(acc, s0, s1, tq, ks, pfull, pempty, lane, abort_flag, p.err) &&
+               promote_slot<1>(acc, s0, s1, tq, ks + 1, pfull, pempty, lane, abort_flag, p.err);
         }
-        tc_fence_before();
-        mbar_arrive(&pempty[buf]);
+        ks += kF8SPK;
       }
       if (!ok) break;
       const int64_t orow =
@@ -299,7 +371,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
         float amax = 0.0f;
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
-          acc[j] = silu_fast(acc[j]) * acc[64 + j];
+          acc[j] = silu_fp8(acc[j]) * acc[64 + j];
           amax = fmaxf(amax, fabsf(acc[j]));
         }
         // exchange with the other half through a double-buffered slot and a bounded mbarrier wait:
@@ -307,34 +379,47 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
         // tile in between, i.e. after it read this one
         float* slot = xchg + (it & 1u) * 256;
         slot[half * 128 + r] = amax;
-        mbar_arrive(&xbar[it & 1u]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&xbar[it & 1u]);
         int x_ok = 1;
         if (lane == 0) x_ok = mbar_wait(&xbar[it & 1u], (it >> 1) & 1u, abort_flag, p.err) ? 1 : 0;
         x_ok = __shfl_sync(0xffffffffu, x_ok, 0);
+        __syncwarp();
         if (!x_ok) break;
         amax = fmaxf(amax, slot[(half ^ 1) * 128 + r]);
         const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-        if (valid) {
-          uint8_t* dst = (uint8_t*)p.out + orow * p.ldo + (int64_t)ti.ft * 128 + half * 64;
+        const float rscale = __frcp_rn(scale);
+        uint4 v[4];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t w[4];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t w[4];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int j = v * 16 + q * 4;
-              w[q] = e4m3x4_pack(__fdiv_rn(acc[j], scale), __fdiv_rn(acc[j + 1], scale),
-                                 __fdiv_rn(acc[j + 2], scale), __fdiv_rn(acc[j + 3], scale));
-            }
-            reinterpret_cast<uint4*>(dst)[v] = make_uint4(w[0], w[1], w[2], w[3]);
+          for (int q = 0; q < 4; ++q) {
+            const int j = c * 16 + q * 4;
+            w[q] = e4m3x4_pack(div_rn_by_recip(acc[j], scale, rscale),
+                               div_rn_by_recip(acc[j + 1], scale, rscale),
+                               div_rn_by_recip(acc[j + 2], scale, rscale),
+                               div_rn_by_recip(acc[j + 3], scale, rscale));
           }
-          if (half == 0) p.out_sT[(int64_t)ti.ft * p.out_s_ld + orow] = scale;
+          v[c] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-      } else if (valid) {
-        float* dst = (float*)p.out + orow * p.ldo + (int64_t)ti.ft * kF8BN + half * 128;
+        uint8_t* dst0 = (uint8_t*)p.out + (orow - lane) * p.ldo + (int64_t)ti.ft * 128 + half * 64;
+        store_rows_64B(wbuf, lane, v, dst0, (int)p.ldo, vrows);
+        if (valid && half == 0) p.out_sT[(int64_t)ti.ft * p.out_s_ld + orow] = scale;
+      } else {
+        // acc[0..63] are output columns ft*256 + half*64 + j, acc[64..127] the same + 128
+        uint8_t* dst0 = (uint8_t*)p.out +
+                        ((orow - lane) * p.ldo + (int64_t)ti.ft * kF8BN + half * 64) * 4;
 #pragma unroll
-        for (int j = 0; j < 128; j += 4)
-          reinterpret_cast<float4*>(dst)[j / 4] = make_float4(acc[j], acc[j + 1], acc[j + 2],
-                                                              acc[j + 3]);
+        for (int c = 0; c < 128; c += 16) {
+          uint4 v[4];
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            v[q] = make_uint4(__float_as_uint(acc[c + 4 * q]), __float_as_uint(acc[c + 4 * q + 1]),
+                              __float_as_uint(acc[c + 4 * q + 2]), __float_as_uint(acc[c + 4 * q + 3]));
+          const int col = (c < 64 ? c : 128 + (c - 64));
+          store_rows_64B(wbuf, lane, v, dst0 + col * 4, (int)p.ldo * 4, vrows);
+        }
       }
     }
   }
@@ -369,15 +454,18 @@ static EncodeTiledFnF8 encode_fn_f8() {
   return fn;
 }
 
-// 2D uint8 map over [rows][cols], box {128 bytes, 128 rows}, 128-byte swizzle, zero fill.
+// 2D map over a byte matrix [rows][cols] (cols % 8 == 0), box {128 bytes, 128 rows}, 128-byte
+// swizzle, zero fill.  The copy moves bytes unchanged, so the map describes each row as cols / 8
+// 8-byte elements: a 16 KB box is then 2048 elements instead of 16384 single bytes, which the TMA
+// unit moves faster.  x coordinates passed to the copies are in these 8-byte units.
 static bool make_map_u8(CUtensorMap* m, const void* base, int64_t rows, int64_t cols) {
   EncodeTiledFnF8 enc = encode_fn_f8();
-  if (!enc || !base || rows <= 0 || cols <= 0) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  if (!enc || !base || rows <= 0 || cols <= 0 || cols % 8) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)(cols / 8), (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols};
-  cuuint32_t box[2] = {128, 128};
+  cuuint32_t box[2] = {16, 128};
   cuuint32_t estr[2] = {1, 1};
-  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box,
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT64, 2, const_cast<void*>(base), dims, strides, box,
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
@@ -403,7 +491,7 @@ static cudaError_t launch_f8_variant(const F8Params& p, int grid, cudaStream_t s
 cudaError_t launch_gemm_fp8(const Fp8Gemm& g, int num_sms, cudaStream_t st) {
   if (g.K % kF8BK || g.n_routed > kF8MaxGroups - 1) return cudaErrorInvalidValue;
   if (g.swiglu ? g.F % 128 : g.F % kF8BN) return cudaErrorInvalidValue;
-  if (g.w_group_rows % 128 || g.ldo % 16) return cudaErrorInvalidValue;
+  if (g.w_group_rows % 128 || g.ldo % 16 || g.ldo > (1 << 24)) return cudaErrorInvalidValue;
   F8Params p;
   memset(&p, 0, sizeof(p));
   if (g.n_routed > 0) {
