@@ -42,9 +42,9 @@ MEASURED_TRAFFIC_RATIO = {
                            "a 64-expert, 4096-token prefill capture"),
     "gemm2_rows": (0.984, "profiles/gemm_tc_rows_prefill_E64_T4096.md",
                    "a 64-expert, 4096-token prefill capture"),
-    "gemm13_swiglu_fp8": (1.51, "profiles/gemm_fp8_E64_T4096.md",
+    "gemm13_swiglu_fp8": (1.018, "profiles/gemm_fp8_E64_T4096.md",
                           "a 64-expert, 4096-token fp8 capture"),
-    "gemm2_fp8": (1.03, "profiles/gemm_fp8_E64_T4096.md", "a 64-expert, 4096-token fp8 capture"),
+    "gemm2_fp8": (0.977, "profiles/gemm_fp8_E64_T4096.md", "a 64-expert, 4096-token fp8 capture"),
 }
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 

@@ -236,6 +236,16 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, float s, uint32_t v0,
   asm("mov.b64 {%0, %1}, %2;" : "=f"(a0), "=f"(a1) : "l"(acc));
 }
 
+// RN(x / s) from y = RN(1 / s): q0 = RN(x * y), the exact remainder r = x - s * q0 (one fma), then
+// RN(q0 + r * y).  By Markstein's theorem (P. Markstein, "Computation of elementary functions on
+// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990) this is the correctly rounded
+// quotient whenever the quotient is a normal number, i.e. the same value as an IEEE division.
+__device__ __forceinline__ float div_rn_by_recip(float x, float s, float y) {
+  const float q0 = x * y;
+  const float r = fmaf(-s, q0, x);
+  return fmaf(r, y, q0);
+}
+
 __device__ __forceinline__ float silu_fast(float g) { return g / (1.0f + __expf(-g)); }
 __device__ __forceinline__ float silu_accurate(float g) { return g / (1.0f + expf(-g)); }
 

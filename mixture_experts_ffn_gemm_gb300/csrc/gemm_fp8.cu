@@ -98,16 +98,6 @@ __device__ __forceinline__ void store_rows_64B(uint8_t* buf, int lane, const uin
   }
 }
 
-// RN(x / s) from y = RN(1 / s): q0 = RN(x * y), the exact remainder r = x - s * q0 (one fma), then
-// RN(q0 + r * y).  By Markstein's theorem (P. Markstein, "Computation of elementary functions on
-// the IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990) this is the correctly rounded
-// quotient whenever the quotient is a normal number, i.e. the same value as an IEEE division.
-__device__ __forceinline__ float div_rn_by_recip(float x, float s, float y) {
-  const float q0 = x * y;
-  const float r = fmaf(-s, q0, x);
-  return fmaf(r, y, q0);
-}
-
 // SiLU for the fp8 epilogue: the quotient with the fast division (h is quantised to e4m3 next)
 __device__ __forceinline__ float silu_fp8(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
