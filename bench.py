@@ -5,7 +5,8 @@ One step = one pass of the whole layer (router -> permute -> experts -> combine)
 synthetic tokens, through the C ABI (moe_forward).  Default workload: the Kimi K2 layer in the
 decode regime (128 tokens, d=7168, 384 experts top-8, expert intermediate 2048, one shared expert,
 bf16 with fp32 router logits).  Other workloads: --workload k2_prefill_bf16 | k3_latent_bf16 |
-tiny_fp32.
+k2_fp8 | tiny_fp32, and the dense block-0 MLP (moe_dense_mlp, d=7168, I=18432) as
+k2_dense_decode_bf16 | k2_dense_prefill_bf16 | tiny_dense_fp32.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
@@ -46,6 +47,7 @@ MEASURED_TRAFFIC_RATIO = {
                           "a 64-expert, 4096-token fp8 capture"),
     "gemm2_fp8": (0.977, "profiles/gemm_fp8_E64_T4096.md", "a 64-expert, 4096-token fp8 capture"),
 }
+DENSE_METRIC = "Dense block-0 MLP tokens/s (d=7168, I=18432) and % of roofline (HBM or TC)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
@@ -416,18 +418,210 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
     }
     print(json.dumps(line), flush=True)
 
+# ----------------------------------------------------------------------------------------------
+# the dense block MLP (moe_dense_mlp): a second workload on the same GEMM kernels
+# ----------------------------------------------------------------------------------------------
+def dense_work(w) -> dict:
+    """Algorithmic bytes and FLOPs of the dense MLP per kernel and for the whole MLP: weights once,
+    x in and y out (and h between the two GEMMs, for the kernels)."""
+    T, d, I = w.T, w.d, w.I
+    ab = 4 if w.act == "f32" else 2
+    return {"gemm13": (2 * I * d * ab + T * d * ab + T * I * ab, 2 * T * d * 2 * I),
+            "gemm2": (d * I * ab + T * I * ab + T * d * ab, 2 * T * I * d),
+            "layer": (3 * d * I * ab + 2 * T * d * ab, 6 * T * d * I)}
+
+
+def time_dense_oracle(layer, rows, nthreads: int) -> float:
+    from oracle import torch_bridge as OB
+    t0 = time.perf_counter()
+    OB.dense_mlp(layer, rows=rows, nthreads=nthreads)
+    return time.perf_counter() - t0
+
+
+def run_dense(args, w, rank: int, world: int, local_rank: int):
+    import torch
+    import torch.distributed as dist
+    from mixture_experts_ffn_gemm_gb300 import binding as B
+    from mixture_experts_ffn_gemm_gb300 import build as BLD
+    from mixture_experts_ffn_gemm_gb300 import synthetic as S
+
+    cores = os.cpu_count() or 1
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        dev = "cuda" if torch.cuda.is_available() else "cpu"
+        layer = S.make_dense(w, seed=0, device=dev)
+        per_token = time_dense_oracle(layer, S.subset_rows(w.T, 1, seed=2), 1)
+        budget_s = 150.0 / max(1, args.steps + args.warmup)
+        n = args.cpu_sample or int(max(1, min(w.T, budget_s * cores / max(per_token, 1e-9))))
+        rows = S.subset_rows(w.T, n, seed=1)
+        for _ in range(args.warmup):
+            time_dense_oracle(layer, rows, cores)
+        secs = [time_dense_oracle(layer, rows, cores) for _ in range(args.steps)]
+        tps = n / statistics.mean(secs)
+        print(json.dumps({
+            "impl": "reference", "metric": DENSE_METRIC, "value": tps, "unit": "tokens/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1000.0 * statistics.mean(secs), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "tokens": w.T, "d": w.d, "intermediate": w.I,
+                       "parallelism": "replicas"},
+            "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{n} of {w.T} tokens (seed 1) per step, fp64 C oracle"},
+            "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}), flush=True)
+        return
+
+    if rank == 0:
+        BLD.build()
+    if world > 1:
+        dist.barrier()
+    B.load_library()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    layer = S.make_dense(w, seed=0, device=dev)
+    ws = torch.zeros(B.moe_dense_mlp_workspace_size(w.T, w.d, w.I, layer.x.dtype),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty(w.T, w.d, dtype=layer.x.dtype, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(x=layer.x, y=out):
+        B.moe_dense_mlp(x, layer.W13, layer.W2, y, ws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+    if B.moe_device_status(ws) != B.MOE_OK:
+        raise RuntimeError("device status after warm-up")
+    gpu_id = str(getattr(torch.cuda.get_device_properties(dev), "uuid", local_rank))
+    if not gpu_id.startswith("GPU-") and len(gpu_id) > 8:
+        gpu_id = "GPU-" + gpu_id
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.3)
+    B.moe_profile_enable(True)
+    B.moe_profile_read()
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    launches0 = B.moe_launch_count()
+    ev0 = torch.cuda.Event(enable_timing=True)
+    ev1 = torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    launches = B.moe_launch_count() - launches0
+    prof = B.moe_profile_read()
+    B.moe_profile_enable(False)
+    clocks = sampler.stop()
+    if B.moe_device_status(ws) != B.MOE_OK:
+        raise RuntimeError("device status after the timed steps")
+    t_ms = torch.tensor([ev0.elapsed_time(ev1)], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(t_ms, op=dist.ReduceOp.MAX)
+    ms_step = float(t_ms.item()) / args.steps
+    value = world * w.T / (ms_step / 1000.0)
+
+    e2e = None
+    if not args.no_e2e:  # host x -> device, the MLP, device y -> host, every step
+        io_bytes = w.T * w.d * layer.x.element_size()
+        x_host = layer.x.cpu().pin_memory()
+        y_host = torch.empty(w.T, w.d, dtype=layer.x.dtype).pin_memory()
+        x_dev = torch.empty_like(layer.x)
+
+        def e2e_step():
+            x_dev.copy_(x_host, non_blocking=True)
+            step(x=x_dev)
+            y_host.copy_(out, non_blocking=True)
+            torch.cuda.synchronize(dev)
+
+        for _ in range(3):
+            e2e_step()
+        t0 = time.perf_counter()
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e2e_s = time.perf_counter() - t0
+        e2e = {"value": world * w.T * args.e2e_steps / e2e_s, "unit": "tokens/s",
+               "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
+               "path": "pinned host x -> moe_dense_mlp -> pinned host y, synchronised per step"}
+    if rank != 0:
+        return
+
+    peaks, peak_src = load_peaks()
+    work = dense_work(w)
+    tc_peak = peaks["bf16_tflops_sustained"]
+    kernels = {k: {"ms_per_launch": v[0] / max(v[1], 1), "launches": v[1]} for k, v in prof.items()}
+    dom = max(prof.items(), key=lambda kv: kv[1][0])[0] if prof else None
+    roof = None
+    if dom is not None:
+        by, fl = work["gemm2" if "gemm2" in dom else "gemm13"]
+        sec = kernels[dom]["ms_per_launch"] / 1000.0
+        if fl / (tc_peak * 1e12) > by / (peaks["hbm_gbs"] * 1e9):
+            roof = {"kernel": dom, "bound": "tensor", "achieved": fl / sec / 1e12, "peak": tc_peak,
+                    "unit": "TFLOP/s", "frac": fl / sec / 1e12 / tc_peak,
+                    "peak_source": f"{peak_src} bf16_tflops_sustained", "work_per_launch": fl}
+        else:
+            roof = {"kernel": dom, "bound": "hbm", "achieved": by / sec / 1e9,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": by / sec / 1e9 / peaks["hbm_gbs"],
+                    "peak_source": f"{peak_src} hbm_gbs", "work_per_launch": by}
+        roof["traffic"] = None
+    lb, lf = work["layer"]
+    t_roof = max(lf / (tc_peak * 1e12), lb / (peaks["hbm_gbs"] * 1e9))
+    cpu = None
+    if not args.no_cpu_baseline:
+        n = args.cpu_sample or min(w.T, 64)
+        sec = time_dense_oracle(layer, S.subset_rows(w.T, n, seed=1), cores)
+        cpu = {"value": n / sec, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} of {w.T} tokens (seed 1), fp64 C oracle, one pass, {sec:.1f} s"}
+    print(json.dumps({
+        "metric": DENSE_METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32" if w.act == "f32" else "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.T, "d": w.d, "intermediate": w.I,
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (0.8 GB of weights stream from HBM every step; "
+                         "no flush)"},
+        "roofline": roof,
+        "layer_roofline": {"t_roof_ms": 1000 * t_roof, "frac": 1000 * t_roof / ms_step,
+                           "bound": "tensor" if lf / (tc_peak * 1e12) > lb / (peaks["hbm_gbs"] * 1e9)
+                           else "hbm", "algorithmic_bytes": lb, "algorithmic_flops": lf},
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches), "kernels": kernels,
+        "clocks": clocks}), flush=True)
+
 
 def main():
     args = parse_args()
     from mixture_experts_ffn_gemm_gb300 import synthetic as S
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.workload in S.DENSE_WORKLOADS:
+        w = S.DENSE_WORKLOADS[args.workload]
+        if args.tokens:
+            w = w.with_tokens(args.tokens)
+        if world > 1 and args.impl != "reference":
+            import torch
+            import torch.distributed as dist
+            torch.cuda.set_device(local_rank)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+        try:
+            run_dense(args, w, rank, world, local_rank)
+        finally:
+            if world > 1 and args.impl != "reference":
+                import torch.distributed as dist
+                dist.destroy_process_group()
+        return
     w = S.WORKLOADS[args.workload]
     if args.experts or args.tokens:
         from dataclasses import replace
         w = replace(w, name=f"{w.name}_E{args.experts or w.E}_T{args.tokens or w.T}",
                     E=args.experts or w.E, T=args.tokens or w.T)
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         run_reference(args, w, rank)
         return

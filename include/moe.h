@@ -18,6 +18,10 @@
  *   [K3-UP]    "Kimi K3 · Latent up-projection": equation y_routed = u_hat W_up, parameter table,
  *              and the `__init__`, `forward` and `moe_infer` code excerpts (dispatch by expert,
  *              per-expert MLP, un-permute, gate-weighted sum; latent down/up projections, RMSNorm).
+ *   [NN-PRINT] nnterp "kimi_k2", "Printout": layer 0's `mlp` is a dense DeepseekV3MLP
+ *              (gate_proj, up_proj 7168 -> 18432, down_proj 18432 -> 7168, SiLU).
+ *   [K2-CODE]  "Kimi K2 · Transformer blocks", the modeling_deepseek excerpt that builds the dense
+ *              MLP instead of the MoE for blocks below first_k_dense_replace.
  *
  * Conventions for every entry point
  *   - Pointers named x, W*, b, out, logits, topk_*, counts, offsets, perm_*, y_perm and ws are
@@ -199,6 +203,27 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
                                  const void* Ws2, const float* Ws13_scale, const float* Ws2_scale,
                                  const void* W_down, const void* W_up, void* out_host, void* ws,
                                  size_t ws_bytes, void* stream);
+
+/* The dense SwiGLU MLP of the first block(s), [NN-PRINT] and [K2-CODE]:
+ *   y = (SiLU(x W1^T) * (x W3^T)) W2^T, with no router, experts or gates.
+ * It runs on the same grouped GEMM kernels as the experts, as one dense group.
+ *   T, d, I     tokens, hidden width, intermediate width (d % 256 == 0 and I % 128 == 0 for
+ *               bf16; d % 16 == 0 and I % 16 == 0 for fp32)
+ *   act_dtype   MOE_BF16 (tensor cores, fp32 accumulation, h rounded to bf16) or MOE_F32
+ *               (CUDA cores); x, W13, W2 and out all have this type
+ *   x           [T][d]
+ *   W13         [2I][d]: the I rows of W1 (gate_proj), then the I rows of W3 (up_proj)
+ *   W2          [d][I]   (down_proj)
+ *   out         [T][d]   y, each element rounded once from its fp32 accumulation
+ *   ws          workspace of at least moe_dense_mlp_workspace_size() bytes (holds h [T][I] and the
+ *               status word); ws_bytes its size
+ * Errors: MOE_ERR_INVALID_ARG (null pointer, non-positive width, misalignment),
+ * MOE_ERR_UNSUPPORTED (dtype or width the kernels do not take), MOE_ERR_WORKSPACE (ws too small),
+ * MOE_ERR_CUDA.  T == 0 is a no-op. */
+size_t moe_dense_mlp_workspace_size(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtype);
+moe_status_t moe_dense_mlp(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtype, const void* x,
+                           const void* W13, const void* W2, void* out, void* ws, size_t ws_bytes,
+                           void* stream);
 
 /* Reset the device status word (first 256 bytes of ws) to "no error", enqueued on stream. */
 moe_status_t moe_reset_device_status(void* ws, size_t ws_bytes, void* stream);

@@ -29,7 +29,7 @@ EXPORTED = ("moe_workspace_size", "moe_router", "moe_permute", "moe_experts", "m
             "moe_forward", "moe_forward_host_io", "moe_reset_device_status", "moe_device_status",
             "moe_status_string", "moe_launch_count", "moe_reset_launch_count",
             "moe_profile_enable", "moe_profile_read", "moe_permute_noalloc",
-            "moe_last_error_string")
+            "moe_last_error_string", "moe_dense_mlp_workspace_size", "moe_dense_mlp")
 
 
 class MoEError(RuntimeError):
@@ -96,6 +96,12 @@ def load_library():
             lib.moe_last_error_string.argtypes = []
             lib.moe_permute_noalloc.restype = S
             lib.moe_permute_noalloc.argtypes = [C, P, P, P, P, P, P]
+            lib.moe_dense_mlp_workspace_size.restype = ctypes.c_size_t
+            lib.moe_dense_mlp_workspace_size.argtypes = [ctypes.c_int64, ctypes.c_int32,
+                                                         ctypes.c_int32, S]
+            lib.moe_dense_mlp.restype = S
+            lib.moe_dense_mlp.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, S, P, P,
+                                          P, P, P, ctypes.c_size_t, P]
             lib.moe_profile_enable.restype = S
             lib.moe_profile_enable.argtypes = [S]
             lib.moe_profile_read.restype = S
@@ -234,6 +240,20 @@ def moe_forward_host_io(cfg, x_host, W_r, b, W13, W2, W13_scale, W2_scale, Ws13,
         ctypes.byref(cfg), _p(x_host), _dev(W_r), _dev(b), _dev(W13), _dev(W2), _dev(W13_scale),
         _dev(W2_scale), _dev(Ws13), _dev(Ws2), _dev(Ws13_scale), _dev(Ws2_scale), _dev(W_down),
         _dev(W_up), _p(out_host), _dev(ws), ws.numel(), _stream(stream)), "moe_forward_host_io")
+
+
+def moe_dense_mlp_workspace_size(T: int, d: int, I: int, act_dtype: torch.dtype) -> int:
+    return int(load_library().moe_dense_mlp_workspace_size(int(T), int(d), int(I),
+                                                           _dt(act_dtype)))
+
+
+def moe_dense_mlp(x, W13, W2, out, ws, stream=None):
+    """Dense SwiGLU MLP: x [T][d], W13 [2I][d] (W1 rows then W3 rows), W2 [d][I], out [T][d]."""
+    T, d = x.shape
+    I = W2.shape[1]
+    _check(load_library().moe_dense_mlp(int(T), int(d), int(I), _dt(x.dtype), _dev(x), _dev(W13),
+                                        _dev(W2), _dev(out), _dev(ws), ws.numel(),
+                                        _stream(stream)), "moe_dense_mlp")
 
 
 def moe_reset_device_status(ws, stream=None):

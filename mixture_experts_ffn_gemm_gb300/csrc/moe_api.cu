@@ -710,6 +710,83 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
   return from_cuda(cudaStreamSynchronize(c.st));
 }
 
+// The dense SwiGLU MLP: one dense group through the expert GEMMs (W1|W3 + SwiGLU -> h in the
+// workspace, then W2 straight into `out`).  Token-rows tensor-core tiles for many tokens, swap-AB
+// tiles for few (the decode regime streams the 0.8 GB of weights), CUDA cores for fp32.
+size_t moe_dense_mlp_workspace_size(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtype) {
+  if (T < 0 || d <= 0 || I <= 0 || (act_dtype != MOE_BF16 && act_dtype != MOE_F32)) return 0;
+  return 256 + moe::align256((size_t)T * (size_t)I * moe::dtype_bytes(act_dtype));
+}
+
+moe_status_t moe_dense_mlp(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtype, const void* x,
+                           const void* W13, const void* W2, void* out, void* ws, size_t ws_bytes,
+                           void* stream) {
+  using namespace moe;
+  if (T < 0 || d <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+  if (act_dtype != MOE_BF16 && act_dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
+  const bool tc = act_dtype == MOE_BF16;
+  if (tc && (d % 256 || I % 128)) return MOE_ERR_UNSUPPORTED;
+  if (!tc && (d % 16 || I % 16)) return MOE_ERR_UNSUPPORTED;
+  if (T > INT32_MAX) return MOE_ERR_UNSUPPORTED;
+  if (!ws || !aligned16(ws)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_dense_mlp_workspace_size(T, d, I, act_dtype)) return MOE_ERR_WORKSPACE;
+  if (T == 0) return MOE_OK;
+  const void* ptrs[] = {x, W13, W2, out};
+  for (const void* q : ptrs)
+    if (!q || !aligned16(q)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int sms = num_sms();
+  (void)cudaGetLastError();
+  uint32_t* err = at<uint32_t>(ws, 0);
+  void* h = at<void>(ws, 256);
+  if (cudaMemsetAsync(err, 0, 256, st) != cudaSuccess) return MOE_ERR_CUDA;
+  const bool swap = T <= 512;
+  cudaError_t e;
+  {
+    GroupedGemm g;
+    g.act_d = x;
+    g.act_d_rows = T;
+    g.w_d = W13;
+    g.w_d_rows = 2 * (int64_t)I;
+    g.dense_rows = (int)T;
+    g.u_off_d = I;
+    g.K = d;
+    g.k_wrap = d;
+    g.F = I;
+    g.epi = EPI_SWIGLU;
+    g.act_dtype = g.w_dtype = act_dtype;
+    g.out = h;
+    g.ldo = I;
+    g.out_dtype = act_dtype;
+    g.err = err;
+    g.label = tc ? (swap ? "dense_gemm13_swiglu_swap" : "dense_gemm13_swiglu_rows")
+                 : "dense_gemm13_swiglu_simt";
+    e = tc ? launch_gemm_tc(g, swap, sms, st) : launch_gemm_simt(g, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  {
+    GroupedGemm g;
+    g.act_d = h;
+    g.act_d_rows = T;
+    g.w_d = W2;
+    g.w_d_rows = d;
+    g.dense_rows = (int)T;
+    g.K = I;
+    g.k_wrap = I;
+    g.F = d;
+    g.epi = EPI_STORE;
+    g.act_dtype = g.w_dtype = act_dtype;
+    g.out = out;
+    g.ldo = d;
+    g.out_dtype = act_dtype;
+    g.err = err;
+    g.label = tc ? (swap ? "dense_gemm2_swap" : "dense_gemm2_rows") : "dense_gemm2_simt";
+    e = tc ? launch_gemm_tc(g, swap, sms, st) : launch_gemm_simt(g, sms, st);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return MOE_OK;
+}
+
 moe_status_t moe_reset_device_status(void* ws, size_t ws_bytes, void* stream) {
   if (!ws || ws_bytes < 256) return MOE_ERR_WORKSPACE;
   return from_cuda(cudaMemsetAsync(ws, 0, 256, static_cast<cudaStream_t>(stream)));

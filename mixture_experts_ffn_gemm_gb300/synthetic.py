@@ -23,6 +23,19 @@ k2_fp8             8192    7168   384  8   2048  -       as prefill; expert weig
                                                           fp32 scale (amax/448) per 128x128 block
 =================  ======  =====  ===  ==  ====  ======  =====================================
 
+Dense block MLP workloads (the first block's DeepseekV3MLP, nnterp "kimi_k2" "Printout":
+gate_proj / up_proj 7168 -> 18432, down_proj 18432 -> 7168):
+
+============================  ======  =====  =====  ==========================================
+name                          T       d      I      values
+============================  ======  =====  =====  ==========================================
+tiny_dense_fp32               48      64     96     fp32; x~N(0,1); W~N(0,1/fan_in)
+k2_dense_decode_bf16          128     7168   18432  bf16; x~N(0,1); W~N(0,0.02^2)
+k2_dense_prefill_bf16         16384   7168   18432  bf16; x as k2_prefill_bf16; W~N(0,0.02^2)
+============================  ======  =====  =====  ==========================================
+
+Draw order for a dense workload: x, W13 (W1 rows, then W3 rows), W2.
+
 Readings: "N(0, 1/fan_in)" is a variance (std = fan_in**-0.5); "N(0, 0.02)" is a standard deviation
 (the usual initializer range); the 16 cluster centres are picked uniformly per token.
 
@@ -89,6 +102,38 @@ WORKLOADS: Dict[str, Workload] = {
     "k2_fp8": Workload("k2_fp8", T=8192, d=7168, E=384, k=8, I=2048, I_shared=2048,
                        x_dist="clusters16", fp8=True),
 }
+
+
+@dataclass(frozen=True)
+class DenseWorkload:
+    name: str
+    T: int
+    d: int
+    I: int
+    act: str = "bf16"
+    x_dist: str = "normal"
+    w_init: str = "std0.02"
+
+    def with_tokens(self, T: int) -> "DenseWorkload":
+        return replace(self, T=T)
+
+
+DENSE_WORKLOADS: Dict[str, DenseWorkload] = {
+    "tiny_dense_fp32": DenseWorkload("tiny_dense_fp32", T=48, d=64, I=96, act="f32",
+                                     w_init="fan_in"),
+    "k2_dense_decode_bf16": DenseWorkload("k2_dense_decode_bf16", T=128, d=7168, I=18432),
+    "k2_dense_prefill_bf16": DenseWorkload("k2_dense_prefill_bf16", T=16384, d=7168, I=18432,
+                                           x_dist="clusters16"),
+}
+
+
+@dataclass
+class DenseLayer:
+    """The dense block MLP's input and weights, resident on one device."""
+    w: DenseWorkload
+    x: torch.Tensor
+    W13: torch.Tensor
+    W2: torch.Tensor
 
 
 @dataclass
@@ -191,6 +236,29 @@ def make_layer(w: Workload, seed: int = 0, device="cuda") -> Layer:
         W_up = randn(d, L, std=_std(w, L)).to(adt).contiguous()
     return Layer(w, x, W_r, b, W13, W2, Ws13, Ws2, W_down, W_up, W13_scale, W2_scale,
                  Ws13_scale, Ws2_scale)
+
+
+def make_dense(w: DenseWorkload, seed: int = 0, device="cuda") -> DenseLayer:
+    """Draw the dense MLP's input and weights on ``device`` from ``seed`` (order: x, W13, W2)."""
+    device = torch.device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    adt = torch.float32 if w.act == "f32" else torch.bfloat16
+    std = (lambda fan_in: fan_in ** -0.5) if w.w_init == "fan_in" else (lambda fan_in: 0.02)
+
+    def randn(*shape, s=1.0):
+        return torch.randn(*shape, generator=g, device=device, dtype=torch.float32) * s
+
+    if w.x_dist == "clusters16":
+        centres = randn(16, w.d)
+        member = torch.randint(0, 16, (w.T,), generator=g, device=device)
+        x = centres[member] + 0.5 * randn(w.T, w.d)
+    else:
+        x = randn(w.T, w.d)
+    x = x.to(adt).contiguous()
+    W13 = randn(2 * w.I, w.d, s=std(w.d)).to(adt).contiguous()
+    W2 = randn(w.d, w.I, s=std(w.I)).to(adt).contiguous()
+    return DenseLayer(w, x, W13, W2)
 
 
 def subset_rows(n: int, count: int, seed: int = 1) -> torch.Tensor:

@@ -99,6 +99,9 @@ def _load():
                                            _Tensor, ctypes.c_int, ctypes.c_int, P]
             lib.orc_rmsnorm_unit.restype = None
             lib.orc_rmsnorm_unit.argtypes = [P, ctypes.c_int, ctypes.c_double, P]
+            lib.orc_dense_mlp.restype = ctypes.c_int
+            lib.orc_dense_mlp.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                          _Tensor, _Tensor, _Tensor, P]
             _lib = lib
     return _lib
 
@@ -265,6 +268,19 @@ def swiglu_row(x: np.ndarray, W13: Mat, W2: Mat, I: int, qb: int = 128,
     if st != 0:
         raise RuntimeError(f"orc_swiglu_row failed with status {st}")
     return y
+
+
+def dense_mlp(x: Mat, W13: Mat, W2: Mat, nthreads: int = 1) -> np.ndarray:
+    """The dense block MLP, y = (SiLU(x W1) * (x W3)) W2 per token, fp64 [T][d] (weights
+    [out, in]; W13 holds the W1 rows, then the W3 rows)."""
+    T, d = x.data.shape
+    I = W2.data.shape[1]
+    out = np.zeros((T, d), np.float64)
+    st = _load().orc_dense_mlp(int(T), int(d), int(I), int(nthreads), x._c(), W13._c(), W2._c(),
+                               _ptr(out))
+    if st != 0:
+        raise RuntimeError(f"orc_dense_mlp failed with status {st}")
+    return out
 
 
 def rmsnorm_unit(v: np.ndarray, eps: float) -> np.ndarray:

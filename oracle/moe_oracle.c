@@ -485,3 +485,69 @@ int orc_forward(const orc_config* c, int nthreads, orc_tensor x, const float* W_
   free(th);
   return status;
 }
+
+/* ------------------------------------------------------------------------------------------ */
+/* Dense block MLP (nnterp "kimi_k2", "Printout": layer 0's mlp is a DeepseekV3MLP; the Kimi K2  */
+/* "Transformer blocks" modeling_deepseek excerpt builds it for blocks below                     */
+/* first_k_dense_replace): y = (SiLU(x W1) (.) (x W3)) W2 per token, the expert equations with   */
+/* no routing.                                                                                   */
+/* ------------------------------------------------------------------------------------------ */
+typedef struct {
+  int64_t T;
+  int d, I, tid, nthreads;
+  orc_tensor x, W13, W2;
+  double* out;
+  int status;
+} dense_job;
+
+static void* dense_worker(void* arg) {
+  dense_job* J = (dense_job*)arg;
+  double* xr = (double*)malloc(sizeof(double) * J->d);
+  if (!xr) {
+    J->status = ORC_EINVAL;
+    return NULL;
+  }
+  for (int64_t t = J->tid; t < J->T; t += J->nthreads) {
+    for (int ch = 0; ch < J->d; ++ch) xr[ch] = elem(&J->x, J->d, 1, t, ch);
+    const int st = orc_swiglu_row(xr, J->d, J->I, J->d, J->W13, J->W2, 128, 0,
+                                  J->out + t * (int64_t)J->d);
+    if (st != ORC_OK) {
+      J->status = st;
+      break;
+    }
+  }
+  free(xr);
+  return NULL;
+}
+
+int orc_dense_mlp(int64_t T, int d, int I, int nthreads, orc_tensor x, orc_tensor W13,
+                  orc_tensor W2, double* out) {
+  if (T < 0 || d < 1 || I < 1 || !x.data || !W13.data || !W2.data || !out) return ORC_EINVAL;
+  if (x.dtype == ORC_E4M3 || W13.dtype == ORC_E4M3 || W2.dtype == ORC_E4M3) return ORC_EINVAL;
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > 1024) nthreads = 1024;
+  dense_job* jobs = (dense_job*)calloc((size_t)nthreads, sizeof(dense_job));
+  pthread_t* th = (pthread_t*)calloc((size_t)nthreads, sizeof(pthread_t));
+  char* started = (char*)calloc((size_t)nthreads, 1);
+  if (!jobs || !th || !started) {
+    free(jobs); free(th); free(started);
+    return ORC_EINVAL;
+  }
+  for (int i = 0; i < nthreads; ++i) {
+    dense_job j = {T, d, I, i, nthreads, x, W13, W2, out, ORC_OK};
+    jobs[i] = j;
+  }
+  for (int i = 1; i < nthreads; ++i)
+    started[i] = pthread_create(&th[i], NULL, dense_worker, &jobs[i]) == 0;
+  dense_worker(&jobs[0]);
+  int status = jobs[0].status;
+  for (int i = 1; i < nthreads; ++i) {
+    if (started[i])
+      pthread_join(th[i], NULL);
+    else
+      dense_worker(&jobs[i]);
+    if (!status) status = jobs[i].status;
+  }
+  free(started); free(jobs); free(th);
+  return status;
+}

@@ -108,6 +108,14 @@ void orc_quantize_group_e4m3(const float* v, int64_t n, int qb, uint8_t* q, floa
 int orc_swiglu_row(const double* x, int din, int I, int dout, orc_tensor W13, orc_tensor W2,
                    int qb, int quant_act, double* y);
 
+/* The dense SwiGLU MLP of the first block(s) (nnterp "kimi_k2", "Printout": layer 0's mlp is a
+ * DeepseekV3MLP with gate_proj / up_proj d -> I and down_proj I -> d): per token the expert
+ * equations with no routing, y = (SiLU(x W1) (.) (x W3)) W2, in fp64.
+ *  x [T][d] (ORC_F32 / ORC_BF16 / ORC_F64), W13 [2I][d] (W1 rows then W3 rows), W2 [d][I],
+ *  out [T][d] fp64.  nthreads >= 1 worker threads split the tokens. */
+int orc_dense_mlp(int64_t T, int d, int I, int nthreads, orc_tensor x, orc_tensor W13,
+                  orc_tensor W2, double* out);
+
 /* RMSNorm with unit weight: y = v / sqrt(mean(v^2) + eps). */
 void orc_rmsnorm_unit(const double* v, int n, double eps, double* y);
 

@@ -12,6 +12,7 @@ import numpy as np
 import torch
 
 from . import Config, Mat
+from . import dense_mlp as _dense_mlp
 
 
 def _np_bits(t: torch.Tensor) -> np.ndarray:
@@ -78,3 +79,11 @@ def forward(layer, rows: Optional[torch.Tensor] = None, experts: Optional[Iterab
     return orc_forward(cfg, x, W_r, b, W13, W2, mat(layer.Ws13, layer.Ws13_scale),
                        mat(layer.Ws2, layer.Ws2_scale), mat(layer.W_down), mat(layer.W_up),
                        nthreads=nthreads)
+
+
+def dense_mlp(layer, rows: Optional[torch.Tensor] = None, nthreads: int = 1) -> np.ndarray:
+    """The oracle's dense block MLP on a synthetic DenseLayer (optionally a subset of its rows):
+    fp64 [rows][d]."""
+    x = layer.x if rows is None else layer.x[rows.to(layer.x.device)]
+    return _dense_mlp(mat(x.cpu()), mat(layer.W13.cpu()), mat(layer.W2.cpu()),
+                            nthreads=nthreads)

@@ -105,6 +105,34 @@ def test_stage_entry_points_validate(moelib):
     assert moelib.moe_reset_device_status(None, 0, None) == B.MOE_ERR_WORKSPACE
 
 
+def test_dense_mlp_host_validation(moelib):
+    p = 0x10000  # aligned stand-in address: every call below fails (or returns) before using it
+    bf, f32 = B.MOE_BF16, B.MOE_F32
+    T, d, I = 16, 7168, 18432
+    need = moelib.moe_dense_mlp_workspace_size(T, d, I, bf)
+    assert need == 256 + ((T * I * 2 + 255) // 256) * 256
+    assert moelib.moe_dense_mlp_workspace_size(-1, d, I, bf) == 0
+    assert moelib.moe_dense_mlp_workspace_size(T, d, I, B.MOE_FP8_E4M3) == 0
+    f = moelib.moe_dense_mlp
+
+    def call(T=T, d=d, I=I, dt=bf, x=p, W13=p, W2=p, out=p, ws=p, nbytes=need):
+        return f(T, d, I, dt, x, W13, W2, out, ws, nbytes, None)
+
+    assert call(T=-1) == B.MOE_ERR_INVALID_ARG
+    assert call(I=0) == B.MOE_ERR_INVALID_ARG
+    assert call(dt=B.MOE_FP8_E4M3) == B.MOE_ERR_UNSUPPORTED
+    assert call(d=7000) == B.MOE_ERR_UNSUPPORTED                    # bf16 tiles need d % 256
+    assert call(d=64, I=40, dt=f32, nbytes=1 << 20) == B.MOE_ERR_UNSUPPORTED  # fp32: I % 16
+    assert call(nbytes=need - 1) == B.MOE_ERR_WORKSPACE
+    assert call(ws=None) == B.MOE_ERR_INVALID_ARG
+    assert call(ws=p + 8) == B.MOE_ERR_INVALID_ARG
+    assert call(x=None) == B.MOE_ERR_INVALID_ARG
+    assert call(W2=p + 4) == B.MOE_ERR_INVALID_ARG
+    # T = 0 is a no-op once the widths and the workspace are valid; empty tensors may be NULL
+    need0 = moelib.moe_dense_mlp_workspace_size(0, d, I, bf)
+    assert call(T=0, x=None, W13=None, W2=None, out=None, nbytes=need0) == B.MOE_OK
+
+
 def test_status_strings(moelib):
     for code in range(7):
         assert B.status_string(code).startswith("MOE_")

@@ -227,6 +227,40 @@ def test_swiglu_hand_computed(orc):
     assert np.allclose(y, rows["E"], rtol=0, atol=1e-15)
 
 
+def test_dense_mlp_hand_computed(orc):
+    """The dense block MLP on the hand-computed SwiGLU case, with a zero token beside it:
+    SiLU(0) * 0 = 0, so the second row must be exactly zero."""
+    rows = {r[0]: np.array([float(v) for v in r[1:]]) for r in read_golden("swiglu_hand.txt")}
+    W13 = np.concatenate([rows["W1"].reshape(2, 3), rows["W3"].reshape(2, 3)])
+    W2 = rows["W2"].reshape(3, 2)
+    x = np.stack([rows["x"], np.zeros(3)])
+    y = orc.dense_mlp(orc.Mat(x, "f64"), orc.Mat(W13, "f64"), orc.Mat(W2, "f64"), nthreads=2)
+    assert np.allclose(y[0], rows["E"], rtol=0, atol=1e-15)
+    assert np.all(y[1] == 0.0)
+
+
+def test_dense_mlp_is_one_always_selected_expert(orc):
+    """A MoE layer with one expert, top-1 and no shared expert routes every token to expert 0 with
+    gate 2.827 * s / s = 2.827: its output is 2.827 times the dense MLP with the same weights."""
+    from oracle import torch_bridge as TB
+    layer = _tiny_layer(T=24, E=1, k=1, n_shared=0)
+    res = TB.forward(layer)
+    x = orc.Mat(layer.x.numpy(), "f32")
+    y = orc.dense_mlp(x, orc.Mat(layer.W13[0].numpy(), "f32"), orc.Mat(layer.W2[0].numpy(), "f32"),
+                      nthreads=3)
+    assert np.allclose(res["out"], 2.827 * y, rtol=1e-13, atol=1e-13)
+    ref = dense_swiglu(layer.x.double().numpy(), layer.W13[0].double().numpy(),
+                       layer.W2[0].double().numpy())
+    assert np.allclose(y, ref, rtol=1e-11, atol=1e-12)
+
+
+def test_dense_mlp_threads_do_not_change_the_result(orc):
+    from mixture_experts_ffn_gemm_gb300 import synthetic as S
+    L = S.make_dense(S.DENSE_WORKLOADS["tiny_dense_fp32"], device="cpu")
+    args = (orc.Mat(L.x.numpy(), "f32"), orc.Mat(L.W13.numpy(), "f32"), orc.Mat(L.W2.numpy(), "f32"))
+    assert np.array_equal(orc.dense_mlp(*args, nthreads=1), orc.dense_mlp(*args, nthreads=7))
+
+
 def test_dense_reduction_one_forced_expert(orc):
     """top_k = 1 with a bias that forces expert 5: every gate is 2.827 and the layer is
     2.827 * MLP_5(x) + MLP_shared(x), a pair of dense SwiGLU MLPs."""
