@@ -206,7 +206,8 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
 
 /* The dense SwiGLU MLP of the first block(s), [NN-PRINT] and [K2-CODE]:
  *   y = (SiLU(x W1^T) * (x W3^T)) W2^T, with no router, experts or gates.
- * It runs on the same grouped GEMM kernels as the experts, as one dense group.
+ * It runs on the same grouped GEMM kernels as the experts, as one dense group (token-rows tiles;
+ * at T <= 256 the W2 GEMM uses 128-column tiles so that more CTAs stream its weights).
  *   T, d, I     tokens, hidden width, intermediate width (d % 256 == 0 and I % 128 == 0 for
  *               bf16; d % 16 == 0 and I % 16 == 0 for fp32)
  *   act_dtype   MOE_BF16 (tensor cores, fp32 accumulation, h rounded to bf16) or MOE_F32

@@ -711,8 +711,8 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
 }
 
 // The dense SwiGLU MLP: one dense group through the expert GEMMs (W1|W3 + SwiGLU -> h in the
-// workspace, then W2 straight into `out`).  Token-rows tensor-core tiles for many tokens, swap-AB
-// tiles for few (the decode regime streams the 0.8 GB of weights), CUDA cores for fp32.
+// workspace, then W2 straight into `out`): token-rows tensor-core tiles for bf16, CUDA cores for
+// fp32.
 size_t moe_dense_mlp_workspace_size(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtype) {
   if (T < 0 || d <= 0 || I <= 0 || (act_dtype != MOE_BF16 && act_dtype != MOE_F32)) return 0;
   return 256 + moe::align256((size_t)T * (size_t)I * moe::dtype_bytes(act_dtype));
@@ -740,7 +740,11 @@ moe_status_t moe_dense_mlp(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtyp
   uint32_t* err = at<uint32_t>(ws, 0);
   void* h = at<void>(ws, 256);
   if (cudaMemsetAsync(err, 0, 256, st) != cudaSuccess) return MOE_ERR_CUDA;
-  const bool swap = T <= 512;
+  // Token-rows tiles in every regime: with few tokens one CTA streams each weight tile once
+  // (swap-AB tiles of 32 tokens would have several CTAs stream the same tile, so that only a
+  // fraction of the bytes in flight are distinct and HBM runs latency-bound).  W2 then has only
+  // d / 256 feature tiles; at small T its 128-column variant doubles the CTAs streaming it.
+  const bool n128_2 = T <= 256;
   cudaError_t e;
   {
     GroupedGemm g;
@@ -759,9 +763,8 @@ moe_status_t moe_dense_mlp(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtyp
     g.ldo = I;
     g.out_dtype = act_dtype;
     g.err = err;
-    g.label = tc ? (swap ? "dense_gemm13_swiglu_swap" : "dense_gemm13_swiglu_rows")
-                 : "dense_gemm13_swiglu_simt";
-    e = tc ? launch_gemm_tc(g, swap, sms, st) : launch_gemm_simt(g, sms, st);
+    g.label = tc ? "dense_gemm13_swiglu_rows" : "dense_gemm13_swiglu_simt";
+    e = tc ? launch_gemm_tc(g, 0, sms, st) : launch_gemm_simt(g, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
   }
   {
@@ -780,8 +783,9 @@ moe_status_t moe_dense_mlp(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtyp
     g.ldo = d;
     g.out_dtype = act_dtype;
     g.err = err;
-    g.label = tc ? (swap ? "dense_gemm2_swap" : "dense_gemm2_rows") : "dense_gemm2_simt";
-    e = tc ? launch_gemm_tc(g, swap, sms, st) : launch_gemm_simt(g, sms, st);
+    g.n128 = n128_2;
+    g.label = tc ? "dense_gemm2_rows" : "dense_gemm2_simt";
+    e = tc ? launch_gemm_tc(g, 0, sms, st) : launch_gemm_simt(g, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
   }
   return MOE_OK;

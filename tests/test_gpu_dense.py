@@ -2,7 +2,8 @@
 
 The dense MLP of the first block is y = (SiLU(x W1) * (x W3)) W2 per token (nnterp "kimi_k2",
 "Printout": layer 0's DeepseekV3MLP).  The library runs it as one dense group through the expert
-GEMMs: token-rows tensor-core tiles for many tokens, swap-AB tiles for few, CUDA cores for fp32.
+GEMMs: token-rows tensor-core tiles for bf16 (W2 in 128-column tiles at T <= 256), CUDA cores for
+fp32.
 Bounds as for the layer: max |GPU - oracle| <= tol * rms(oracle), tol 1e-4 (fp32) / 2e-2 (bf16)."""
 from dataclasses import replace
 
@@ -55,15 +56,15 @@ def test_dense_fp32_cuda_cores(cuda_device, T):
     _check(_dense("tiny_dense_fp32", T=T))
 
 
-@pytest.mark.parametrize("T", [1, 33, 200, 512])
-def test_dense_bf16_swap_tiles(cuda_device, T):
-    """T <= 512: swap-AB tiles (weights on the MMA's M side, 32-token tiles, ragged tails)."""
+@pytest.mark.parametrize("T", [1, 33, 200, 256])
+def test_dense_bf16_few_tokens(cuda_device, T):
+    """T <= 256: one or two 128-row token tiles, W2 in 128-column store tiles, ragged tails."""
     _check(_dense("k2_dense_decode_bf16", T=T, d=512, I=384))
 
 
-@pytest.mark.parametrize("T", [513, 700, 1300])
-def test_dense_bf16_token_rows_tiles(cuda_device, T):
-    """T > 512: token-rows tiles (128 rows x 256 weight rows), several tiles and a ragged tail."""
+@pytest.mark.parametrize("T", [257, 700, 1300])
+def test_dense_bf16_many_tokens(cuda_device, T):
+    """T > 256: token-rows tiles (128 rows x 256 weight rows), several tiles and a ragged tail."""
     _check(_dense("k2_dense_prefill_bf16", T=T, d=512, I=384))
 
 
@@ -78,8 +79,8 @@ def test_dense_zero_tokens_is_a_no_op(cuda_device):
 
 
 def test_dense_k2_block0_decode_full_size(cuda_device):
-    """The K2 block-0 widths (d = 7168, I = 18432) at the decode batch (128 tokens, swap-AB
-    tiles), compared on every token."""
+    """The K2 block-0 widths (d = 7168, I = 18432) at the decode batch (128 tokens), compared on
+    every token."""
     _check(_dense("k2_dense_decode_bf16"))
 
 
