@@ -69,6 +69,7 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2 } moe_dtype_t;
 #define MOE_FLAG_ROUTER_SIMT 0x4u     /* force the CUDA-core fp32 router GEMM                    */
 #define MOE_FLAG_ROUTER_TC 0x8u       /* force the tensor-core (3 x bf16 split) router GEMM      */
 #define MOE_FLAG_GEMM_N128 0x10u      /* token-rows tiles of the store GEMMs with N = 128 columns  */
+#define MOE_FLAG_GEMM_SWAP_WIDE 0x20u /* force weight-rows-as-M tiles of 256 tokens (runtime N)  */
 /* Test hook for the failure path: the tensor-core W1|W3 expert GEMM's copy producer issues no
  * copy, so its MMA issuer's bounded wait (shortened to 50 ms under this flag) expires; the kernel
  * flags MOE_ERR_TIMEOUT in the device status, drains, frees its tensor memory and returns, and

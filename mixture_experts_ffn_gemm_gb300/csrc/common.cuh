@@ -152,6 +152,11 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32() {
          ((uint32_t)(M >> 4) << 24);
 }
 
+// The same descriptor with M = 128 and a run-time N (a multiple of 16 in [16, 256]).
+__device__ __forceinline__ uint32_t idesc_bf16_f32_n(int n) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(n >> 3) << 17) | ((128u >> 4) << 24);
+}
+
 // Instruction descriptor, kind::f8f6f4 with e4m3 A and B (format code 0), fp32 accumulator.
 template <int M, int N>
 __host__ __device__ constexpr uint32_t idesc_e4m3_f32() {

@@ -240,6 +240,13 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
         const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
                                         p.dense_rows, p.dense_act_row0, S::RPT);
         const int nkb = ti.dense ? nkb_d : nkb_r;
+        // swap-AB tiles: the MMA's N is the tile's token count rounded up to 16, so a group's
+        // last, partial tile costs only the tokens it holds
+        uint32_t idesc = kIdesc;
+        if constexpr (kSwap) {
+          const int n = ti.valid >= kBN ? kBN : ((ti.valid + 15) & ~15);
+          idesc = idesc_bf16_f32_n(n);
+        }
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * S::ACC_COLS;
@@ -262,9 +269,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
                        idesc_bf16_f32<128, kBN - 256>(), accum);
               continue;
             }
-            mma_bf16(d0, sw128_kmajor_desc(sa + k16 * 32), bdesc, kIdesc, accum);
+            mma_bf16(d0, sw128_kmajor_desc(sa + k16 * 32), bdesc, idesc, accum);
             if (kSwap && S::kSwiGLU)
-              mma_bf16(d0 + kBN, sw128_kmajor_desc(sa + kBoxBytes + k16 * 32), bdesc, kIdesc,
+              mma_bf16(d0 + kBN, sw128_kmajor_desc(sa + kBoxBytes + k16 * 32), bdesc, idesc,
                        accum);
           }
           mma_commit(&empty[stage]);
@@ -410,7 +417,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
         // swap: TMEM lane = output feature, columns = tokens of this tile
         const int64_t feat = (int64_t)ti.ft * 128 + r;
 #pragma unroll 1
-        for (int c = 0; c < kBN; c += 16) {
+        for (int c = 0; c < kBN && c < ti.valid; c += 16) {
           uint32_t g[16], u[16];
           tmem_ld16(tb + c, g);
           if (S::kSwiGLU) tmem_ld16(tb + kBN + c, u);
@@ -530,7 +537,7 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
   const bool f32_router = !swap && g.epi == EPI_STORE && g.out_dtype == MOE_F32 && g.F % 256;
   if (g.n128 && g.epi == EPI_STORE && (g.F % 128 || (g.F_d && g.F_d % 128)))
     return cudaErrorInvalidValue;
-  const int act_box = swap ? 32 : 128;
+  const int act_box = swap == 2 ? 256 : swap ? 32 : 128;
   const int kw = g.k_wrap > 0 ? g.k_wrap : g.K;
   if (g.n_routed > 0) {
     if (!make_map_bf16(&p.map_act, g.act, g.act_rows, kw, act_box)) return cudaErrorInvalidValue;
@@ -583,6 +590,11 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
       return launch_variant<false, 128, EPI_STORE>(p, grid, st, g.label);
     if (g.epi == EPI_STORE) return launch_variant<false, 256, EPI_STORE>(p, grid, st, g.label);
     return launch_variant<false, 256, EPI_STORE_ADD>(p, grid, st, g.label);
+  }
+  if (swap == 2) {  // 256-token tiles (the MMA's N follows each tile's token count)
+    if (g.epi == EPI_SWIGLU) return launch_variant<true, 256, EPI_SWIGLU>(p, grid, st, g.label);
+    if (g.epi == EPI_STORE) return launch_variant<true, 256, EPI_STORE>(p, grid, st, g.label);
+    return cudaErrorInvalidValue;
   }
   if (g.epi == EPI_SWIGLU) return launch_variant<true, 32, EPI_SWIGLU>(p, grid, st, g.label);
   if (g.epi == EPI_STORE) return launch_variant<true, 32, EPI_STORE>(p, grid, st, g.label);

@@ -72,6 +72,8 @@ struct GroupedGemm {
 // Tensor-core grouped GEMM (tcgen05 + TMA), bf16 operands, fp32 accumulation in TMEM.
 // swap = 0: token rows are the MMA M side (128-row tiles), weights the N side.
 // swap = 1: weight rows are the M side, tokens the N side (32-token tiles), for few rows per group.
+// swap = 2: as 1 with 256-token tiles; the MMA's N is each tile's token count rounded up to 16
+//           (SwiGLU and plain store only).
 // Requires K % 64 == 0, F % 128 == 0 (F % 256 == 0 for swap = 0 stores).  Returns a CUDA error or
 // cudaErrorInvalidValue when the shapes are not supported (nothing launched).
 cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStream_t st);

@@ -85,7 +85,8 @@ struct Plan {
   int de;             // expert width: d or d_latent
   bool router_tc;     // tensor-core router (3 x bf16 split weights)
   int router_splits;  // split-K slices of the CUDA-core router
-  int swap;           // 1: weight-rows-as-M tensor-core tiles
+  int swap;           // expert GEMM tiles: 0 token rows as M; 1 weight rows as M with 32-token
+                      // tiles; 2 the same with 256-token tiles
   bool tc;            // tensor-core expert GEMMs
   bool fp8;           // e4m3 experts with block scales
 };
@@ -151,9 +152,16 @@ static Plan make_plan(const moe_config_t* c) {
     while (s > 1 && (c->d % (16 * s) != 0)) --s;
     p.router_splits = s < 1 ? 1 : s;
   }
-  // expert GEMM tile orientation
+  // expert GEMM tile orientation.  Few tokens: 32-token swap-AB tiles (each expert's weights
+  // stream once).  Otherwise 128-token rows tiles.  The 256-token swap-AB tiles (MMA N shrinks to
+  // a group's last tokens) waste far less padding in the K3 regime of ~171 rows per expert, but
+  // measured slower there: the SwiGLU accumulators take all of TMEM, so the epilogue no longer
+  // overlaps the next tile, and MMAs with N < 256 read more shared memory per FLOP.  They stay
+  // available through MOE_FLAG_GEMM_SWAP_WIDE.
   if (c->flags & MOE_FLAG_GEMM_SWAP_AB)
     p.swap = 1;
+  else if (c->flags & MOE_FLAG_GEMM_SWAP_WIDE)
+    p.swap = 2;
   else if (c->flags & MOE_FLAG_GEMM_ROWS_MAJOR)
     p.swap = 0;
   else
@@ -324,9 +332,9 @@ static moe_status_t run_permute(Ctx& x, const int32_t* idx, int32_t* counts, int
 // The routed expert GEMMs: tensor cores (token-rows or swap-AB tiles) for bf16, CUDA cores for
 // fp32.  The profiler name carries the variant ("<label>_rows" / "_swap" / "_simt").
 static cudaError_t gemm(Ctx& x, GroupedGemm g, const char* rows_label, const char* swap_label,
-                        const char* simt_label) {
+                        const char* wide_label, const char* simt_label) {
   if (x.pl.tc) {
-    g.label = x.pl.swap ? swap_label : rows_label;
+    g.label = x.pl.swap == 2 ? wide_label : x.pl.swap ? swap_label : rows_label;
     return launch_gemm_tc(g, x.pl.swap, x.sms, x.st);
   }
   g.label = simt_label;
@@ -488,7 +496,8 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.out_dtype = c->act_dtype;
     g.err = x.err;
     g.test_stall = (c->flags & MOE_FLAG_TEST_STALL_EXPERTS) != 0;
-    e = gemm(x, g, "gemm13_swiglu_rows", "gemm13_swiglu_swap", "gemm13_swiglu_simt");
+    e = gemm(x, g, "gemm13_swiglu_rows", "gemm13_swiglu_swap", "gemm13_swiglu_swap256",
+             "gemm13_swiglu_simt");
     if (e != cudaSuccess) return from_cuda(e);
   }
   // W2 -> y_perm [P][de] (+ shared rows [T][d])
@@ -526,7 +535,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.out_dtype = MOE_F32;
     g.err = x.err;
     g.n128 = (c->flags & MOE_FLAG_GEMM_N128) != 0;
-    e = gemm(x, g, "gemm2_rows", "gemm2_swap", "gemm2_simt");
+    e = gemm(x, g, "gemm2_rows", "gemm2_swap", "gemm2_swap256", "gemm2_simt");
     if (e != cudaSuccess) return from_cuda(e);
   }
   return MOE_OK;

@@ -18,6 +18,7 @@ pytestmark = pytest.mark.gpu
 
 ROWS = B.MOE_FLAG_GEMM_ROWS_MAJOR
 SWAP = B.MOE_FLAG_GEMM_SWAP_AB
+WIDE = B.MOE_FLAG_GEMM_SWAP_WIDE  # 256-token swap-AB tiles with a run-time MMA N
 
 
 def _lib():
@@ -71,12 +72,12 @@ def test_zero_tokens_is_a_no_op(cuda_device):
 SMALL_BF16 = replace(S.WORKLOADS["tiny_fp32"], name="small_bf16", act="bf16", T=300)
 
 
-@pytest.mark.parametrize("flags", [ROWS, SWAP], ids=["rows", "swap"])
+@pytest.mark.parametrize("flags", [ROWS, SWAP, WIDE], ids=["rows", "swap", "wide"])
 def test_bf16_small_all_tokens(cuda_device, flags):
     _full_check(_layer(SMALL_BF16, seed=1), flags)
 
 
-@pytest.mark.parametrize("flags", [ROWS, SWAP], ids=["rows", "swap"])
+@pytest.mark.parametrize("flags", [ROWS, SWAP, WIDE], ids=["rows", "swap", "wide"])
 def test_bf16_one_expert_takes_every_token(cuda_device, flags):
     """k = 1 and a bias that forces expert 5: one group of T rows, every other group empty.
 
@@ -95,7 +96,7 @@ def test_bf16_one_expert_takes_every_token(cuda_device, flags):
     _full_check(layer, flags, output_rounding=True, expert_rows=64)
 
 
-@pytest.mark.parametrize("flags", [ROWS, SWAP], ids=["rows", "swap"])
+@pytest.mark.parametrize("flags", [ROWS, SWAP, WIDE], ids=["rows", "swap", "wide"])
 def test_bf16_every_expert_selected(cuda_device, flags):
     """k == E: every token visits every expert."""
     w = replace(SMALL_BF16, E=4, k=4, T=130)
@@ -124,16 +125,33 @@ def test_bf16_router_paths_agree(cuda_device):
     L.check_routing(layer, b)
 
 
+# The K3 path rounds x_lat, h, u_hat and the output to bf16 (each a GEMM operand or the result).
+# An ideal pipeline with exactly those roundings already reaches max|err| = 2.01e-2 rms(ref) (rms
+# error 3.4e-3) on a 700-token instance of these widths, computed in numpy: the tail of the error
+# distribution sits at the bf16 bound.  The largest single term is the output's own rounding, so
+# the latent checks subtract it (2^-8 |ref|, the largest half-ulp of a bf16 result) before the max
+# bound, as the k = 1 case does; the rms bound is unchanged.
+LATENT_OUTPUT_ROUNDING = True
+
+
 def test_latent_small_all_tokens(cuda_device):
     w = replace(SMALL_BF16, name="latent_small", d=512, d_latent=256, latent_norm=1, T=300,
                 w_init="fan_in")
-    _full_check(_layer(w, seed=6), ROWS)
+    _full_check(_layer(w, seed=6), ROWS, output_rounding=LATENT_OUTPUT_ROUNDING)
+
+
+def test_latent_small_wide_swap_tiles(cuda_device):
+    """The latent path in 256-token swap-AB tiles (MOE_FLAG_GEMM_SWAP_WIDE): routed groups at
+    width L and the full-width shared expert (its own K) in the same launches."""
+    w = replace(SMALL_BF16, name="latent_small", d=512, d_latent=256, latent_norm=1, T=700,
+                w_init="fan_in")
+    _full_check(_layer(w, seed=9), WIDE, output_rounding=LATENT_OUTPUT_ROUNDING)
 
 
 def test_latent_small_without_norm(cuda_device):
     w = replace(SMALL_BF16, name="latent_small", d=512, d_latent=256, latent_norm=0, T=70,
                 w_init="fan_in")
-    _full_check(_layer(w, seed=7), SWAP)
+    _full_check(_layer(w, seed=7), SWAP, output_rounding=LATENT_OUTPUT_ROUNDING)
 
 
 # ---------------------------------------------------------------------------------------------
@@ -169,7 +187,7 @@ def test_fp8_zero_activation_group_gets_unit_scale(cuda_device):
 # K2 widths (d = 7168, I = 2048) with fewer experts: every token checked
 # ---------------------------------------------------------------------------------------------
 
-@pytest.mark.parametrize("flags", [ROWS, SWAP], ids=["rows", "swap"])
+@pytest.mark.parametrize("flags", [ROWS, SWAP, WIDE], ids=["rows", "swap", "wide"])
 def test_k2_widths_32_experts(cuda_device, flags):
     w = replace(S.WORKLOADS["k2_decode_bf16"], name="k2_e32", E=32, T=72)
     _full_check(_layer(w, seed=8), flags)
@@ -186,7 +204,8 @@ def _sample(T, n=6, seed=1):
 def _full_workload(name):
     w = S.WORKLOADS[name]
     layer = _layer(w)
-    res = _full_check(layer, 0, rows=_sample(w.T))
+    res = _full_check(layer, 0, rows=_sample(w.T),
+                      output_rounding=LATENT_OUTPUT_ROUNDING and w.d_latent > 0)
     del layer
     torch.cuda.empty_cache()
     return res
