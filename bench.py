@@ -66,6 +66,8 @@ def parse_args():
     ap.add_argument("--experts", type=int, default=0,
                     help="override the routed expert count (small profiling cases)")
     ap.add_argument("--tokens", type=int, default=0, help="override the token count")
+    ap.add_argument("--block", action="store_true",
+                    help="time the block's FFN half (moe_forward_block: RMSNorm, layer, residual)")
     ap.add_argument("--flags", type=lambda v: int(v, 0), default=0,
                     help="moe_config_t.flags tuning overrides (MOE_FLAG_*)")
     return ap.parse_args()
@@ -272,8 +274,13 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
     B.moe_router(cfg, layer.x, layer.W_r, layer.b, None, idx, wgt, ws)
     idx_np = idx.cpu().numpy()
 
-    def step():
-        B.moe_forward(cfg, layer.x, *weights, out, ws, stream=stream)
+    norm_w = S.make_block_norm(w, seed=0, device=dev) if args.block else None
+
+    def step(x=layer.x):
+        if args.block:
+            B.moe_forward_block(cfg, x, norm_w, *weights, out, ws, stream=stream)
+        else:
+            B.moe_forward(cfg, x, *weights, out, ws, stream=stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -325,20 +332,33 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
     if not args.no_e2e:
         x_host = layer.x.cpu().pin_memory()
         out_host = torch.empty(w.T, w.d, dtype=layer.x.dtype).pin_memory()
+        x_dev = torch.empty_like(layer.x)
+
+        def e2e_step():
+            if args.block:  # host x'_n -> device, the block, device x_{n+1} -> host
+                x_dev.copy_(x_host, non_blocking=True)
+                step(x=x_dev)
+                out_host.copy_(out, non_blocking=True)
+                torch.cuda.synchronize(dev)
+            else:
+                B.moe_forward_host_io(cfg, x_host, *weights, out_host, ws, stream=stream)
+
         for _ in range(3):
-            B.moe_forward_host_io(cfg, x_host, *weights, out_host, ws, stream=stream)
+            e2e_step()
         if world > 1:
             dist.barrier()
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
-            B.moe_forward_host_io(cfg, x_host, *weights, out_host, ws, stream=stream)
+            e2e_step()
         e2e_s = time.perf_counter() - t0
         e2e_t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
         if world > 1:
             dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
         e2e = {"value": world * w.T * args.e2e_steps / float(e2e_t.item()), "unit": "tokens/s",
                "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
-               "path": "moe_forward_host_io (pinned host x / out, synchronised per step)"}
+               "path": ("pinned host x'_n -> moe_forward_block -> pinned host x_{n+1}, "
+                        "synchronised per step") if args.block else
+                       "moe_forward_host_io (pinned host x / out, synchronised per step)"}
 
     if rank != 0:
         return
@@ -402,7 +422,8 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if w.act == "f32" else ("e4m3" if w.fp8 else "bf16"),
         "data": "synthetic",
-        "config": {"workload": w.name, "tokens": w.T, "d": w.d, "experts": w.E, "top_k": w.k,
+        "config": {"workload": w.name + ("_block" if args.block else ""), "tokens": w.T, "d": w.d,
+                   "experts": w.E, "top_k": w.k, "block_ffn_half": bool(args.block),
                    "expert_intermediate": w.I, "shared_intermediate": w.I_shared,
                    "d_latent": w.d_latent, "router": "fp32 logits",
                    "parallelism": "replicas" if world > 1 else "single GPU",

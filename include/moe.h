@@ -194,6 +194,24 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const float* W_
                          const float* Ws13_scale, const float* Ws2_scale, const void* W_down,
                          const void* W_up, void* out, void* ws, size_t ws_bytes, void* stream);
 
+/* The FFN half of a transformer block with the layer inside it, [K2-MoE] "x_ffn = RMSNorm(x'_n)",
+ * the "Mixture of experts" steps, and "x_{n+1} = x'_n + D_ffn" ([NN-PRINT]: the post-attention
+ * norm is DeepseekV3RMSNorm((7168,), eps=1e-06); [K2-PARAM]: "MoE RMSNorm" has 7168 weights).
+ *   x_resid   [T][d] act_dtype: x'_n, the residual stream entering the FFN half
+ *   norm_w    [d] act_dtype: the RMSNorm weight
+ *   out       [T][d] act_dtype: x'_n + D_ffn(norm_w * x'_n / sqrt(mean(x'_n^2) + rms_eps))
+ *   other arguments as moe_forward
+ * The normalised input is computed in fp32 and rounded once to act_dtype (the router and expert
+ * GEMMs' operand); the residual is added inside the combine (on the K3 path, to the fp32
+ * shared-expert rows that the up-projection adds), before the output's single rounding.  The K3
+ * path needs its shared expert (n_shared = 1), else MOE_ERR_UNSUPPORTED. */
+moe_status_t moe_forward_block(const moe_config_t* cfg, const void* x_resid, const void* norm_w,
+                               const float* W_r, const float* b, const void* W13, const void* W2,
+                               const float* W13_scale, const float* W2_scale, const void* Ws13,
+                               const void* Ws2, const float* Ws13_scale, const float* Ws2_scale,
+                               const void* W_down, const void* W_up, void* out, void* ws,
+                               size_t ws_bytes, void* stream);
+
 /* The whole layer from HOST buffers: copies x (pinned or pageable host memory, [T][d] act_dtype)
  * to the workspace, runs moe_forward on resident device weights, and copies the output back to
  * out_host ([T][d] act_dtype).  Synchronises `stream` before returning.  Weights stay device

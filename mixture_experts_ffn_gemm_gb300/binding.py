@@ -30,7 +30,8 @@ EXPORTED = ("moe_workspace_size", "moe_router", "moe_permute", "moe_experts", "m
             "moe_forward", "moe_forward_host_io", "moe_reset_device_status", "moe_device_status",
             "moe_status_string", "moe_launch_count", "moe_reset_launch_count",
             "moe_profile_enable", "moe_profile_read", "moe_permute_noalloc",
-            "moe_last_error_string", "moe_dense_mlp_workspace_size", "moe_dense_mlp")
+            "moe_last_error_string", "moe_dense_mlp_workspace_size", "moe_dense_mlp",
+            "moe_forward_block")
 
 
 class MoEError(RuntimeError):
@@ -81,6 +82,9 @@ def load_library():
             lib.moe_forward.restype = S
             lib.moe_forward.argtypes = [C, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
                                         ctypes.c_size_t, P]
+            lib.moe_forward_block.restype = S
+            lib.moe_forward_block.argtypes = [C, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
+                                              ctypes.c_size_t, P]
             lib.moe_forward_host_io.restype = S
             lib.moe_forward_host_io.argtypes = lib.moe_forward.argtypes
             lib.moe_reset_device_status.restype = S
@@ -230,6 +234,16 @@ def moe_forward(cfg, x, W_r, b, W13, W2, W13_scale, W2_scale, Ws13, Ws2, Ws13_sc
                                       _dev(Ws2), _dev(Ws13_scale), _dev(Ws2_scale), _dev(W_down),
                                       _dev(W_up), _dev(out), _dev(ws), ws.numel(),
                                       _stream(stream)), "moe_forward")
+
+
+def moe_forward_block(cfg, x_resid, norm_w, W_r, b, W13, W2, W13_scale, W2_scale, Ws13, Ws2,
+                      Ws13_scale, Ws2_scale, W_down, W_up, out, ws, stream=None):
+    """The FFN half of a block: out = x_resid + layer(RMSNorm(x_resid) * norm_w)."""
+    _check(load_library().moe_forward_block(
+        ctypes.byref(cfg), _dev(x_resid), _dev(norm_w), _dev(W_r), _dev(b), _dev(W13), _dev(W2),
+        _dev(W13_scale), _dev(W2_scale), _dev(Ws13), _dev(Ws2), _dev(Ws13_scale), _dev(Ws2_scale),
+        _dev(W_down), _dev(W_up), _dev(out), _dev(ws), ws.numel(), _stream(stream)),
+        "moe_forward_block")
 
 
 def moe_forward_host_io(cfg, x_host, W_r, b, W13, W2, W13_scale, W2_scale, Ws13, Ws2,

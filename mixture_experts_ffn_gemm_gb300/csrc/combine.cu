@@ -14,34 +14,15 @@
 
 namespace moe {
 
-// 8 consecutive fp32 values (two 16-byte loads) and their store as 8 x bf16 or 8 x fp32.
-__device__ __forceinline__ void load8(const float* p, float (&v)[8]) {
-  const float4 a = __ldg(reinterpret_cast<const float4*>(p));
-  const float4 b = __ldg(reinterpret_cast<const float4*>(p) + 1);
-  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
-  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
-}
-__device__ __forceinline__ void store8(__nv_bfloat16* p, const float (&v)[8]) {
-  uint4 raw;
-  raw.x = pack_bf16x2(v[0], v[1]);
-  raw.y = pack_bf16x2(v[2], v[3]);
-  raw.z = pack_bf16x2(v[4], v[5]);
-  raw.w = pack_bf16x2(v[6], v[7]);
-  *reinterpret_cast<uint4*>(p) = raw;
-}
-__device__ __forceinline__ void store8(float* p, const float (&v)[8]) {
-  reinterpret_cast<float4*>(p)[0] = make_float4(v[0], v[1], v[2], v[3]);
-  reinterpret_cast<float4*>(p)[1] = make_float4(v[4], v[5], v[6], v[7]);
-}
-
 constexpr int kMaxK = 32;
 
-// y_perm and y_shared hold fp32 expert outputs; out is bf16 or fp32 (rounded once).
+// y_perm and y_shared hold fp32 expert outputs; resid (optional, the block's residual stream) is
+// in the output type; out is bf16 or fp32, rounded once from the fp32 sum.
 template <typename TO>
 __global__ void __launch_bounds__(256)
     combine_kernel(const float* __restrict__ y_perm, const float* __restrict__ y_shared,
                    const int32_t* __restrict__ perm_dst, const float* __restrict__ weight,
-                   int64_t T, int k, int d, TO* __restrict__ out) {
+                   int64_t T, int k, int d, const TO* __restrict__ resid, TO* __restrict__ out) {
   __shared__ int64_t rows[kMaxK];
   __shared__ float gw[kMaxK];
   const int64_t P = T * k;
@@ -71,6 +52,12 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] += v[i];
       }
+      if (resid) {
+        float v[8];
+        load8(resid + t * d + c, v);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] += v[i];
+      }
       store8(out + t * d + c, acc);
     }
   }
@@ -78,7 +65,7 @@ __global__ void __launch_bounds__(256)
 
 cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* y_shared,
                            const int32_t* perm_dst, const float* weight, int64_t T, int k, int d,
-                           void* out, int num_sms, cudaStream_t st) {
+                           const void* resid, void* out, int num_sms, cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   if (k > kMaxK || d % 8) return cudaErrorInvalidValue;
   const int64_t blocks = T < (int64_t)num_sms * 8 ? T : (int64_t)num_sms * 8;
@@ -86,10 +73,11 @@ cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* y_shar
   if (act_dtype == MOE_BF16)
     combine_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(
         (const float*)y_perm, (const float*)y_shared, perm_dst, weight, T, k, d,
-        (__nv_bfloat16*)out);
+        (const __nv_bfloat16*)resid, (__nv_bfloat16*)out);
   else
     combine_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(
-        (const float*)y_perm, (const float*)y_shared, perm_dst, weight, T, k, d, (float*)out);
+        (const float*)y_perm, (const float*)y_shared, perm_dst, weight, T, k, d,
+        (const float*)resid, (float*)out);
   return cudaGetLastError();
 }
 

@@ -146,11 +146,17 @@ cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int E, int n_sh
 cudaError_t launch_gather_rows(const void* src, const int32_t* perm_src, int64_t P, int k,
                                int width, int elem_bytes, void* dst, int num_sms, cudaStream_t st);
 
-// Combine: out[t] = sum_j w[t,j] * y[perm_dst[t*k+j]] + y_shared[t]; y fp32, fp32 sum, one
-// rounding to act_dtype.
+// Combine: out[t] = sum_j w[t,j] * y[perm_dst[t*k+j]] + y_shared[t] (+ resid[t]); y fp32, fp32
+// sum, one rounding to act_dtype.  resid (act_dtype) and y_shared may be null.
 cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* y_shared,
                            const int32_t* perm_dst, const float* weight, int64_t T, int k, int d,
-                           void* out, int num_sms, cudaStream_t st);
+                           const void* resid, void* out, int num_sms, cudaStream_t st);
+// Block steps: y = w * x / sqrt(mean(x^2) + eps) per row (fp32, one rounding to act_dtype); and
+// y_f32 += r (r in act_dtype, n elements, n % 8 == 0).
+cudaError_t launch_rmsnorm_rows(int act_dtype, const void* x, const void* w, float eps, int64_t T,
+                                int d, void* y, int num_sms, cudaStream_t st);
+cudaError_t launch_add_residual(float* y, int act_dtype, const void* r, int64_t n, int num_sms,
+                                cudaStream_t st);
 // K3: u_hat[t] = RMSNorm?( sum_j w[t,j] * y[perm_dst[t*k+j]] ) in bf16, width L, y fp32.
 cudaError_t launch_latent_combine(const void* y_perm, const int32_t* perm_dst,
                                   const float* weight, int64_t T, int k, int L, int norm,

@@ -542,7 +542,8 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
 }
 
 static moe_status_t run_combine(Ctx& x, const void* y_perm, const int32_t* perm_dst,
-                                const float* weight, const void* W_up, void* out) {
+                                const float* weight, const void* W_up, void* out,
+                                const void* resid = nullptr) {
   const moe_config_t* c = x.c;
   if (c->T == 0) return MOE_OK;
   const int64_t T = c->T, P = T * c->k;
@@ -550,8 +551,14 @@ static moe_status_t run_combine(Ctx& x, const void* y_perm, const int32_t* perm_
   const void* y_sh =
       c->n_shared ? static_cast<const uint8_t*>(y_perm) + (size_t)P * de * 4 : nullptr;
   if (!x.pl.latent)
-    return from_cuda(
-        launch_combine(c->act_dtype, y_perm, y_sh, perm_dst, weight, T, c->k, d, out, x.sms, x.st));
+    return from_cuda(launch_combine(c->act_dtype, y_perm, y_sh, perm_dst, weight, T, c->k, d,
+                                    resid, out, x.sms, x.st));
+  if (resid) {  // the residual joins the fp32 shared-expert rows the up-projection adds
+    if (!y_sh) return MOE_ERR_UNSUPPORTED;
+    cudaError_t e = launch_add_residual(static_cast<float*>(const_cast<void*>(y_sh)),
+                                        c->act_dtype, resid, T * d, x.sms, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
   void* u_hat = at<void>(x.ws, x.L.u_hat);
   cudaError_t e = launch_latent_combine(y_perm, perm_dst, weight, T, c->k, de, c->latent_norm,
                                         c->rms_eps, u_hat, x.sms, x.st);
@@ -690,6 +697,49 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const float* W_
                        Ws13_scale, Ws2_scale, W_down, y_perm)) != MOE_OK)
     return s;
   return run_combine(c, y_perm, perm_dst, wgt, W_up, out);
+}
+
+moe_status_t moe_forward_block(const moe_config_t* cfg, const void* x_resid, const void* norm_w,
+                               const float* W_r, const float* b, const void* W13, const void* W2,
+                               const float* W13_scale, const float* W2_scale, const void* Ws13,
+                               const void* Ws2, const float* Ws13_scale, const float* Ws2_scale,
+                               const void* W_down, const void* W_up, void* out, void* ws,
+                               size_t ws_bytes, void* stream) {
+  Ctx c;
+  moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
+  if (s != MOE_OK) return s;
+  if (cfg->d_latent > 0 && !cfg->n_shared) return MOE_ERR_UNSUPPORTED;
+  MOE_RETURN_IF_EMPTY(cfg);
+  if (!x_resid || !norm_w || !W_r || !b || !W13 || !W2 || !out) return MOE_ERR_INVALID_ARG;
+  if (cfg->n_shared && (!Ws13 || !Ws2)) return MOE_ERR_INVALID_ARG;
+  if (cfg->w_dtype == MOE_FP8_E4M3 &&
+      (!W13_scale || !W2_scale || (cfg->n_shared && (!Ws13_scale || !Ws2_scale))))
+    return MOE_ERR_INVALID_ARG;
+  if (cfg->d_latent > 0 && (!W_down || !W_up)) return MOE_ERR_INVALID_ARG;
+  const void* ptrs[] = {x_resid, norm_w, W_r, W13, W2, Ws13, Ws2, W_down, W_up, out};
+  for (const void* p : ptrs)
+    if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  ready(c);
+  if (cudaMemsetAsync(c.err, 0, 256, c.st) != cudaSuccess) return MOE_ERR_CUDA;
+  const Layout& L = c.L;
+  // x_ffn = RMSNorm(x'_n) in the host-I/O staging region, which this entry point does not use
+  void* x_ffn = at<void>(ws, L.x_io);
+  cudaError_t e = launch_rmsnorm_rows(cfg->act_dtype, x_resid, norm_w, cfg->rms_eps, cfg->T, cfg->d,
+                                      x_ffn, c.sms, c.st);
+  if (e != cudaSuccess) return from_cuda(e);
+  int32_t* idx = at<int32_t>(ws, L.idx);
+  float* wgt = at<float>(ws, L.weight);
+  int32_t* offsets = at<int32_t>(ws, L.offsets);
+  int32_t* perm_src = at<int32_t>(ws, L.perm_src);
+  int32_t* perm_dst = at<int32_t>(ws, L.perm_dst);
+  void* y_perm = at<void>(ws, L.y_perm);
+  if ((s = run_router(c, x_ffn, W_r, b, nullptr, idx, wgt)) != MOE_OK) return s;
+  if ((s = run_permute(c, idx, at<int32_t>(ws, L.counts), offsets, perm_src, perm_dst)) != MOE_OK)
+    return s;
+  if ((s = run_experts(c, x_ffn, offsets, perm_src, W13, W2, W13_scale, W2_scale, Ws13, Ws2,
+                       Ws13_scale, Ws2_scale, W_down, y_perm)) != MOE_OK)
+    return s;
+  return run_combine(c, y_perm, perm_dst, wgt, W_up, out, x_resid);
 }
 
 moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, const float* W_r,

@@ -238,6 +238,18 @@ def make_layer(w: Workload, seed: int = 0, device="cuda") -> Layer:
                  Ws13_scale, Ws2_scale)
 
 
+def make_block_norm(w, seed: int = 0, device="cuda") -> torch.Tensor:
+    """The post-attention RMSNorm weight of a block around the layer: [d] in the activation
+    type, drawn U(0.8, 1.2) from its own generator (seed + 7919) so that the layer's draws are
+    unchanged.  The layer's x then plays the residual stream x'_n."""
+    device = torch.device(device)
+    g = torch.Generator(device=device)
+    g.manual_seed(seed + 7919)
+    adt = torch.float32 if w.act == "f32" else torch.bfloat16
+    u = torch.rand(w.d, generator=g, device=device, dtype=torch.float32)
+    return (0.8 + 0.4 * u).to(adt).contiguous()
+
+
 def make_dense(w: DenseWorkload, seed: int = 0, device="cuda") -> DenseLayer:
     """Draw the dense MLP's input and weights on ``device`` from ``seed`` (order: x, W13, W2)."""
     device = torch.device(device)

@@ -87,3 +87,43 @@ def dense_mlp(layer, rows: Optional[torch.Tensor] = None, nthreads: int = 1) -> 
     x = layer.x if rows is None else layer.x[rows.to(layer.x.device)]
     return _dense_mlp(mat(x.cpu()), mat(layer.W13.cpu()), mat(layer.W2.cpu()),
                             nthreads=nthreads)
+
+
+def round_bf16(v: np.ndarray) -> np.ndarray:
+    """Round fp64 values to the nearest bf16 value (8 significant bits, ties to even), in fp64.
+    Normal-range values only (the block's normalised activations are O(1))."""
+    m, e = np.frexp(np.asarray(v, dtype=np.float64))  # v = m * 2^e, 0.5 <= |m| < 1
+    return np.ldexp(np.round(m * 256.0) / 256.0, e)
+
+
+def block_forward(layer, norm_w: torch.Tensor, rows: Optional[torch.Tensor] = None,
+                  nthreads: int = 1) -> dict:
+    """The FFN half of a transformer block around the layer ("Kimi K2 · Transformer blocks > MoE
+    transformer block": x_ffn = RMSNorm(x'_n), the mixture of experts, x_{n+1} = x'_n + D_ffn),
+    in fp64 on ``rows`` of the layer's x, which plays x'_n.  The RMSNorm is the oracle's unit
+    RMSNorm times the weight; x_ffn is then rounded once to the activation type, as the layer's
+    GEMM operand.  Returns the layer forward's dict with "delta" (D_ffn), "x_ffn" and
+    "out" = x'_n + D_ffn."""
+    from . import forward as orc_forward, route as orc_route, rmsnorm_unit
+    xr = layer.x if rows is None else layer.x[rows.to(layer.x.device)]
+    x64 = _np_bits(xr.float()).astype(np.float64)
+    g64 = _np_bits(norm_w.float()).astype(np.float64)
+    eps = float(layer.w.rms_eps)
+    xn = np.stack([rmsnorm_unit(r, eps) for r in x64]) * g64[None, :] if len(x64) else x64
+    # x_ffn is the router's and the experts' GEMM operand: rounded once to the activation type
+    if layer.w.act == "bf16":
+        xn = round_bf16(xn)
+    elif layer.w.act == "f32":
+        xn = xn.astype(np.float32).astype(np.float64)
+    x = Mat(np.ascontiguousarray(xn), "f64")
+    W_r, b = _np_bits(layer.W_r.float()), _np_bits(layer.b.float())
+    cfg = config(layer, xn.shape[0])
+    experts = np.unique(orc_route(cfg, x, W_r, b)["idx"])
+    W13, W2 = expert_mats(layer, experts)
+    res = orc_forward(cfg, x, W_r, b, W13, W2, mat(layer.Ws13, layer.Ws13_scale),
+                      mat(layer.Ws2, layer.Ws2_scale), mat(layer.W_down), mat(layer.W_up),
+                      nthreads=nthreads)
+    res["delta"] = res["out"]
+    res["x_ffn"] = xn
+    res["out"] = x64 + res["out"]
+    return res

@@ -133,6 +133,29 @@ def test_dense_mlp_host_validation(moelib):
     assert call(T=0, x=None, W13=None, W2=None, out=None, nbytes=need0) == B.MOE_OK
 
 
+def test_block_host_validation(moelib):
+    cfg = _cfg()
+    need = B.moe_workspace_size(cfg)
+    p = 0x10000
+
+    def blk(c, ws=p, nbytes=need, **override):
+        names = ["x", "norm_w", "W_r", "b", "W13", "W2", "W13_s", "W2_s", "Ws13", "Ws2",
+                 "Ws13_s", "Ws2_s", "W_down", "W_up", "out"]
+        ptrs = [override.get(n, p) for n in names]
+        return moelib.moe_forward_block(c, *ptrs, ws, nbytes, None)
+
+    c = ctypes.byref(cfg)
+    assert blk(c, nbytes=need - 1) == B.MOE_ERR_WORKSPACE
+    assert blk(c, norm_w=None) == B.MOE_ERR_INVALID_ARG
+    assert blk(c, x=None) == B.MOE_ERR_INVALID_ARG
+    assert blk(c, norm_w=p + 4) == B.MOE_ERR_INVALID_ARG
+    lat = _cfg(d_latent=3584, latent_norm=1, n_shared=0)
+    assert blk(ctypes.byref(lat), nbytes=B.moe_workspace_size(lat)) == B.MOE_ERR_UNSUPPORTED
+    empty = _cfg(T=0)
+    assert blk(ctypes.byref(empty), nbytes=B.moe_workspace_size(empty), x=None, norm_w=None,
+               out=None) == B.MOE_OK
+
+
 def test_status_strings(moelib):
     for code in range(7):
         assert B.status_string(code).startswith("MOE_")

@@ -227,6 +227,52 @@ def test_swiglu_hand_computed(orc):
     assert np.allclose(y, rows["E"], rtol=0, atol=1e-15)
 
 
+# --------------------------------------------------------------------------------------------
+# The block around the layer: x_ffn = RMSNorm(x'_n), layer, x_{n+1} = x'_n + D_ffn
+# --------------------------------------------------------------------------------------------
+
+def test_bf16_rounding_matches_the_format(orc):
+    """round_bf16 (8 significant bits, ties to even) against torch's fp32 -> bf16 conversion on
+    values exact in fp32, including exact ties, and its own idempotence."""
+    from oracle import torch_bridge as TB
+    g = torch.Generator().manual_seed(3)
+    v = torch.randn(20000, generator=g) * torch.exp2(torch.randint(-20, 20, (20000,), generator=g).float())
+    ties = (torch.randint(128, 256, (2000,), generator=g).double() * 2 + 1) / 512.0  # m + half ulp
+    vals = torch.cat([v.double(), ties, -ties])
+    ours = TB.round_bf16(vals.numpy())
+    ref = vals.float().bfloat16().double().numpy()
+    assert np.array_equal(ours, ref)
+    assert np.array_equal(TB.round_bf16(ours), ours)
+
+
+def test_block_with_zero_norm_weight_passes_the_residual(orc):
+    """A zero RMSNorm weight makes x_ffn = 0: every expert and the shared expert see a zero input,
+    SiLU(0) * 0 = 0, so D_ffn = 0 and the block returns x'_n unchanged, bit for bit."""
+    from oracle import torch_bridge as TB
+    layer = _tiny_layer(T=20)
+    res = TB.block_forward(layer, torch.zeros(layer.w.d), nthreads=2)
+    assert np.all(res["delta"] == 0.0)
+    assert np.array_equal(res["out"], layer.x.double().numpy())
+
+
+def test_block_norm_closed_form_and_scale_invariance(orc):
+    """With unit weight every normalised row has mean square m / (m + eps) (m the row's mean
+    square, up to the rounding of x_ffn to the activation type), and the FFN half is invariant to scaling x'_n (up to eps): block(4x) - 4x equals
+    block(x) - x."""
+    from oracle import torch_bridge as TB
+    layer = _tiny_layer(T=16)
+    x = layer.x.double().numpy()
+    res = TB.block_forward(layer, torch.ones(layer.w.d), nthreads=2)
+    m = np.mean(x * x, axis=1)
+    # x_ffn is rounded once to the fp32 activation type: 2^-24 per element, 2^-23 per square
+    assert np.allclose(np.mean(res["x_ffn"] ** 2, axis=1), m / (m + layer.w.rms_eps), rtol=3e-7)
+    g = torch.rand(layer.w.d, generator=torch.Generator().manual_seed(5)) + 0.5
+    r1 = TB.block_forward(layer, g, nthreads=2)
+    layer.x = layer.x * 4.0
+    r4 = TB.block_forward(layer, g, nthreads=2)
+    assert np.allclose(r4["out"] - 4.0 * x, r1["out"] - x, rtol=1e-5, atol=1e-6)
+
+
 def test_dense_mlp_hand_computed(orc):
     """The dense block MLP on the hand-computed SwiGLU case, with a zero token beside it:
     SiLU(0) * 0 = 0, so the second row must be exactly zero."""
