@@ -146,8 +146,9 @@ def touched_bytes(w, idx: np.ndarray) -> dict:
     expert outputs in fp32)."""
     touched = np.unique(idx)
     ab = 4 if w.act == "f32" else 2
-    wb = 1 if w.fp8 else ab                       # bytes per expert weight
-    sb = 4.0 / (128 * 128) if w.fp8 else 0.0      # block-scale bytes per weight
+    int4 = getattr(w, "int4", False)
+    wb = 1 if w.fp8 else (0.5 if int4 else ab)   # bytes per expert weight
+    sb = 4.0 / (128 * 128) if w.fp8 else (2.0 / 32 if int4 else 0.0)  # scale bytes per weight
     hb = 1 + 4.0 / 128 if w.fp8 else ab           # bytes per activation entering a GEMM
     de = w.d_expert
     T, P = idx.shape[0], idx.size
@@ -420,7 +421,9 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "f32" if w.act == "f32" else ("e4m3" if w.fp8 else "bf16"),
+        "dtype": "f32" if w.act == "f32" else ("e4m3" if w.fp8 else
+                                               "int4 weights, bf16" if getattr(w, "int4", False)
+                                               else "bf16"),
         "data": "synthetic",
         "config": {"workload": w.name + ("_block" if args.block else ""), "tokens": w.T, "d": w.d,
                    "experts": w.E, "top_k": w.k, "block_ffn_half": bool(args.block),

@@ -61,7 +61,20 @@ typedef enum {
   MOE_ERR_TIMEOUT = 6       /* a kernel gave up a bounded wait (pipeline stalled) and returned   */
 } moe_status_t;
 
-typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2 } moe_dtype_t;
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2, MOE_INT4 = 3 } moe_dtype_t;
+
+/* MOE_INT4 expert weights ("4-bit integer groups", the storage of K2-Thinking and K2.5 per the
+ * nnterp "kimi_k2" page; bf16 activations):
+ *   - a weight matrix [rows][K] is stored packed, [rows][K/2] bytes, eight codes per 32-bit
+ *     little-endian word: code i of the word (input channel 8w + i) is the 4-bit nibble number
+ *     (i / 2) + 4 * (i % 2), counted from bit 0;
+ *   - a nibble u encodes the integer u - 8 (excess-8, -8..7);
+ *   - one bf16 scale per 32 consecutive input channels of each row, stored transposed,
+ *     [K/32][rows];
+ *   - the weight is RN_bf16((u - 8) * scale): the product rounded once to bf16, the MMA operand.
+ * W13 is then [E][2I][d/2] packed with W13_scale [E][d/32][2I]; W2 [E][d][I/2] with W2_scale
+ * [E][I/32][d]; the shared expert likewise ([2 I_s][d/2], [d/32][2 I_s]; [d][I_s/2], [I_s/32][d]).
+ * The *_scale arguments then point to bf16 data.  quant_block must be 32. */
 
 /* moe_config_t.flags */
 #define MOE_FLAG_GEMM_ROWS_MAJOR 0x1u /* force the token-rows-as-M tensor-core GEMM tiles       */
@@ -88,8 +101,8 @@ typedef struct {
   int32_t d_latent;    /* 0: K2 path; L > 0: K3 latent width (3584) [K3-UP]                      */
   int32_t latent_norm; /* 1: RMSNorm with unit weight on the latent gate-weighted sum [K3-UP]    */
   int32_t act_dtype;   /* MOE_F32 or MOE_BF16: x, out, W_down, W_up, intermediates               */
-  int32_t w_dtype;     /* expert weights: equal to act_dtype, or MOE_FP8_E4M3 (with block scales) */
-  int32_t quant_block; /* fp8 block edge (128): weight scales per 128x128, activations per 1x128  */
+  int32_t w_dtype;     /* expert weights: act_dtype, MOE_FP8_E4M3 (block scales) or MOE_INT4      */
+  int32_t quant_block; /* fp8: block edge 128 (weights 128x128, activations 1x128); int4: group 32 */
   uint32_t flags;      /* MOE_FLAG_* tuning overrides; 0 = automatic choice                      */
   float gate_scale;    /* routed_scaling_factor (2.827) [NN-CFG]                                 */
   float rms_eps;       /* rms_norm_eps (1e-6) [NN-CFG]                                           */

@@ -19,7 +19,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libmoe_gb300.so")
 
 MOE_OK, MOE_ERR_INVALID_ARG, MOE_ERR_UNSUPPORTED, MOE_ERR_WORKSPACE = 0, 1, 2, 3
 MOE_ERR_CUDA, MOE_ERR_DEVICE_CHECK, MOE_ERR_TIMEOUT = 4, 5, 6
-MOE_F32, MOE_BF16, MOE_FP8_E4M3 = 0, 1, 2
+MOE_F32, MOE_BF16, MOE_FP8_E4M3, MOE_INT4 = 0, 1, 2, 3
 MOE_FLAG_GEMM_ROWS_MAJOR, MOE_FLAG_GEMM_SWAP_AB = 0x1, 0x2
 MOE_FLAG_ROUTER_SIMT, MOE_FLAG_ROUTER_TC = 0x4, 0x8
 MOE_FLAG_TEST_STALL_EXPERTS = 0x100
@@ -126,6 +126,8 @@ def _dt(dtype: torch.dtype) -> int:
         return MOE_BF16
     if dtype == torch.float8_e4m3fn:
         return MOE_FP8_E4M3
+    if dtype == torch.uint8:  # packed 4-bit integer groups
+        return MOE_INT4
     raise TypeError(f"unsupported dtype {dtype}")
 
 
@@ -146,7 +148,8 @@ def config_for(w, T: Optional[int] = None, flags: int = 0) -> moe_config_t:
     return make_config(T=w.T if T is None else T, d=w.d, E=w.E, k=w.k, I=w.I,
                        I_shared=w.I_shared, n_shared=w.n_shared, d_latent=w.d_latent,
                        latent_norm=w.latent_norm, act_dtype=act,
-                       w_dtype=torch.float8_e4m3fn if w.fp8 else act,
+                       w_dtype=(torch.float8_e4m3fn if w.fp8 else
+                                torch.uint8 if getattr(w, "int4", False) else act),
                        quant_block=w.quant_block, flags=flags, gate_scale=w.gate_scale,
                        rms_eps=w.rms_eps)
 

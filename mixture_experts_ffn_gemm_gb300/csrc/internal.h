@@ -118,6 +118,39 @@ struct Fp8Gemm {
 };
 cudaError_t launch_gemm_fp8(const Fp8Gemm& g, int num_sms, cudaStream_t st);
 
+// Grouped GEMM with 4-bit integer group-quantised weights (packed [w_rows][K/2]; bf16 scales per
+// weight group, [n_routed][K/32][w_group_rows] for the routed experts and [K/32][w_d_rows] for the
+// dense group) and bf16 activations, swap-AB tiles: M = 128 weight rows, N = up to 32 tokens.
+// swiglu: out = bf16 h [rows][ldo] (W3 rows at +u_off); else fp32 out [rows][ldo].
+struct W4Gemm {
+  const void* act = nullptr;
+  int64_t act_rows = 0;
+  const void* wq = nullptr;
+  const void* ws = nullptr;
+  int64_t w_rows = 0;
+  const int32_t* offsets = nullptr;
+  int n_routed = 0;
+  int w_group_rows = 0;
+  int u_off = 0;
+  const void* act_d = nullptr;
+  int64_t act_d_rows = 0;
+  int dense_act_row0 = 0;
+  const void* wq_d = nullptr;
+  const void* ws_d = nullptr;
+  int64_t w_d_rows = 0;
+  int dense_rows = 0;
+  int dense_out_row0 = 0;
+  int u_off_d = 0;
+  int K = 0;
+  int F = 0;
+  bool swiglu = false;
+  void* out = nullptr;
+  int64_t ldo = 0;
+  uint32_t* err = nullptr;
+  const char* label = "gemm_w4";
+};
+cudaError_t launch_gemm_w4(const W4Gemm& g, int num_sms, cudaStream_t st);
+
 // x bf16 [rows][d] -> e4m3 codes [rows][d] and scales sT [d/128][rows] (amax / 448 per 128).
 cudaError_t launch_quantize_rows(const void* x, int64_t rows, int d, uint8_t* q, float* sT,
                                  cudaStream_t st);

@@ -89,6 +89,7 @@ struct Plan {
                       // tiles; 2 the same with 256-token tiles
   bool tc;            // tensor-core expert GEMMs
   bool fp8;           // e4m3 experts with block scales
+  bool w4;            // 4-bit integer group-quantised experts
 };
 
 struct Layout {
@@ -107,7 +108,8 @@ static moe_status_t validate(const moe_config_t* c) {
   if (c->n_shared != 0 && c->n_shared != 1) return MOE_ERR_INVALID_ARG;
   if (c->d_latent < 0 || c->reserved_ != 0) return MOE_ERR_INVALID_ARG;
   if (c->act_dtype != MOE_F32 && c->act_dtype != MOE_BF16) return MOE_ERR_INVALID_ARG;
-  if (c->w_dtype != MOE_F32 && c->w_dtype != MOE_BF16 && c->w_dtype != MOE_FP8_E4M3)
+  if (c->w_dtype != MOE_F32 && c->w_dtype != MOE_BF16 && c->w_dtype != MOE_FP8_E4M3 &&
+      c->w_dtype != MOE_INT4)
     return MOE_ERR_INVALID_ARG;
   if (c->k > 32 || c->E > 1023) return MOE_ERR_UNSUPPORTED;
   if (c->n_shared && c->I_shared != c->I) return MOE_ERR_UNSUPPORTED;
@@ -115,6 +117,13 @@ static moe_status_t validate(const moe_config_t* c) {
   if (c->w_dtype == MOE_FP8_E4M3) {
     // e4m3 experts: bf16 activations, 128 x 128 weight blocks, K2 path only
     if (c->act_dtype != MOE_BF16 || c->quant_block != 128 || c->d_latent > 0)
+      return MOE_ERR_UNSUPPORTED;
+    if (c->d % 256 || c->I % 128) return MOE_ERR_UNSUPPORTED;
+    return MOE_OK;
+  }
+  if (c->w_dtype == MOE_INT4) {
+    // 4-bit groups of 32 input channels: bf16 activations, K2 path only
+    if (c->act_dtype != MOE_BF16 || c->quant_block != 32 || c->d_latent > 0)
       return MOE_ERR_UNSUPPORTED;
     if (c->d % 256 || c->I % 128) return MOE_ERR_UNSUPPORTED;
     return MOE_OK;
@@ -136,6 +145,7 @@ static Plan make_plan(const moe_config_t* c) {
   p.de = p.latent ? c->d_latent : c->d;
   p.tc = c->act_dtype == MOE_BF16;
   p.fp8 = c->w_dtype == MOE_FP8_E4M3;
+  p.w4 = c->w_dtype == MOE_INT4;
   // router
   const bool tc_ok = c->act_dtype == MOE_BF16 && c->E % 128 == 0 && c->d % 64 == 0;
   if (c->flags & MOE_FLAG_ROUTER_SIMT)
@@ -435,6 +445,68 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     return from_cuda(launch_gemm_fp8(g2, x.sms, x.st));
   }
 
+  if (x.pl.w4) {  // 4-bit experts: gather bf16 x, two grouped GEMMs that expand the weights
+    e = launch_gather_rows(xin, perm_src, P, c->k, d, (int)ab, x_perm, x.sms, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+    const bool sh = c->n_shared != 0;
+    W4Gemm g;
+    g.act = x_perm;
+    g.act_rows = P;
+    g.wq = W13;
+    g.ws = W13_scale;
+    g.w_rows = (int64_t)E * 2 * I;
+    g.offsets = offsets;
+    g.n_routed = E;
+    g.w_group_rows = 2 * I;
+    g.u_off = I;
+    if (sh) {
+      g.act_d = xin;
+      g.act_d_rows = T;
+      g.wq_d = Ws13;
+      g.ws_d = Ws13_scale;
+      g.w_d_rows = 2 * I;
+      g.dense_rows = (int)T;
+      g.dense_out_row0 = (int)P;
+      g.u_off_d = I;
+    }
+    g.K = d;
+    g.F = I;
+    g.swiglu = true;
+    g.out = h;
+    g.ldo = I;
+    g.err = x.err;
+    g.label = "gemm13_swiglu_w4";
+    e = launch_gemm_w4(g, x.sms, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+    W4Gemm g2;
+    g2.act = h;
+    g2.act_rows = P + (sh ? T : 0);
+    g2.wq = W2;
+    g2.ws = W2_scale;
+    g2.w_rows = (int64_t)E * d;
+    g2.offsets = offsets;
+    g2.n_routed = E;
+    g2.w_group_rows = d;
+    if (sh) {
+      g2.act_d = h;
+      g2.act_d_rows = P + T;
+      g2.dense_act_row0 = (int)P;
+      g2.wq_d = Ws2;
+      g2.ws_d = Ws2_scale;
+      g2.w_d_rows = d;
+      g2.dense_rows = (int)T;
+      g2.dense_out_row0 = (int)P;
+    }
+    g2.K = I;
+    g2.F = d;
+    g2.swiglu = false;
+    g2.out = y_perm;
+    g2.ldo = d;
+    g2.err = x.err;
+    g2.label = "gemm2_w4";
+    return from_cuda(launch_gemm_w4(g2, x.sms, x.st));
+  }
+
   const void* route_src = xin;
   if (x.pl.latent) {  // x_lat = x W_down^T on every token (the router saw the full width)
     void* x_lat = at<void>(x.ws, x.L.x_lat);
@@ -636,7 +708,7 @@ moe_status_t moe_experts(const moe_config_t* cfg, const void* x, const int32_t* 
   MOE_RETURN_IF_EMPTY(cfg);
   if (!x || !offsets || !perm_src || !W13 || !W2 || !y_perm) return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared && (!Ws13 || !Ws2)) return MOE_ERR_INVALID_ARG;
-  if (cfg->w_dtype == MOE_FP8_E4M3 &&
+  if ((cfg->w_dtype == MOE_FP8_E4M3 || cfg->w_dtype == MOE_INT4) &&
       (!W13_scale || !W2_scale || (cfg->n_shared && (!Ws13_scale || !Ws2_scale))))
     return MOE_ERR_INVALID_ARG;
   if (cfg->d_latent > 0 && !W_down) return MOE_ERR_INVALID_ARG;
@@ -674,7 +746,7 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const float* W_
   MOE_RETURN_IF_EMPTY(cfg);
   if (!x || !W_r || !b || !W13 || !W2 || !out) return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared && (!Ws13 || !Ws2)) return MOE_ERR_INVALID_ARG;
-  if (cfg->w_dtype == MOE_FP8_E4M3 &&
+  if ((cfg->w_dtype == MOE_FP8_E4M3 || cfg->w_dtype == MOE_INT4) &&
       (!W13_scale || !W2_scale || (cfg->n_shared && (!Ws13_scale || !Ws2_scale))))
     return MOE_ERR_INVALID_ARG;
   if (cfg->d_latent > 0 && (!W_down || !W_up)) return MOE_ERR_INVALID_ARG;
@@ -712,7 +784,7 @@ moe_status_t moe_forward_block(const moe_config_t* cfg, const void* x_resid, con
   MOE_RETURN_IF_EMPTY(cfg);
   if (!x_resid || !norm_w || !W_r || !b || !W13 || !W2 || !out) return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared && (!Ws13 || !Ws2)) return MOE_ERR_INVALID_ARG;
-  if (cfg->w_dtype == MOE_FP8_E4M3 &&
+  if ((cfg->w_dtype == MOE_FP8_E4M3 || cfg->w_dtype == MOE_INT4) &&
       (!W13_scale || !W2_scale || (cfg->n_shared && (!Ws13_scale || !Ws2_scale))))
     return MOE_ERR_INVALID_ARG;
   if (cfg->d_latent > 0 && (!W_down || !W_up)) return MOE_ERR_INVALID_ARG;

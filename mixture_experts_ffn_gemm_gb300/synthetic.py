@@ -75,6 +75,7 @@ class Workload:
     latent_norm: int = 0
     act: str = "bf16"        # activation / weight storage: "f32" | "bf16"
     fp8: bool = False        # expert weights e4m3 + block scales, activations quantised
+    int4: bool = False       # expert weights 4-bit integer groups of 32 (bf16 scales)
     x_dist: str = "normal"   # "normal" | "clusters16"
     w_init: str = "std0.02"  # "std0.02" | "fan_in"
     bias_range: float = 0.05
@@ -101,6 +102,8 @@ WORKLOADS: Dict[str, Workload] = {
                                I_shared=2048, d_latent=3584, latent_norm=1, w_init="fan_in"),
     "k2_fp8": Workload("k2_fp8", T=8192, d=7168, E=384, k=8, I=2048, I_shared=2048,
                        x_dist="clusters16", fp8=True),
+    "k2_int4_decode": Workload("k2_int4_decode", T=128, d=7168, E=384, k=8, I=2048,
+                               I_shared=2048, int4=True, quant_block=32),
 }
 
 
@@ -176,6 +179,28 @@ def _block_quantize(m: torch.Tensor, qb: int):
     return q.to(torch.float8_e4m3fn), scale.contiguous()
 
 
+# nibble n of a packed 32-bit word holds code _W4_CODE_OF_NIBBLE[n] of its 8 channels
+_W4_CODE_OF_NIBBLE = (0, 2, 4, 6, 1, 3, 5, 7)
+
+
+def _int4_quantize(m: torch.Tensor, group: int = 32):
+    """Store a weight matrix [R][C] as 4-bit integer groups (the MOE_INT4 format): per row and 32
+    input channels a bf16 scale (amax / 7, rounded to bf16; 1 for an all-zero group) and codes
+    round(w / scale) clamped to -8..7, stored as nibbles u = code + 8, packed eight to a
+    little-endian 32-bit word with code i in nibble (i / 2) + 4 (i % 2).  Returns (packed uint8
+    [R][C/2], scales bf16 [C/32][R]).  Input preparation for the int4 workload."""
+    R, C = m.shape
+    assert C % group == 0 and C % 8 == 0
+    g = m.float().reshape(R, C // group, group)
+    scale = (g.abs().amax(dim=2) / 7.0).to(torch.bfloat16)
+    scale = torch.where(scale == 0, torch.ones_like(scale), scale)
+    codes = torch.round(g / scale.float()[:, :, None]).clamp(-8, 7).to(torch.int32) + 8
+    words = codes.reshape(R, C // 8, 8)
+    nib = words[:, :, list(_W4_CODE_OF_NIBBLE)]  # nibble n's code
+    packed = (nib[:, :, 0::2] | (nib[:, :, 1::2] << 4)).to(torch.uint8)  # byte b: nibbles 2b, 2b+1
+    return packed.reshape(R, C // 2).contiguous(), scale.t().contiguous()
+
+
 def make_layer(w: Workload, seed: int = 0, device="cuda") -> Layer:
     """Draw one layer's inputs and weights on ``device`` from ``seed``."""
     device = torch.device(device)
@@ -201,11 +226,17 @@ def make_layer(w: Workload, seed: int = 0, device="cuda") -> Layer:
     b = ((torch.rand(E, generator=g, device=device, dtype=torch.float32) * 2 - 1)
          * w.bias_range).contiguous()
 
-    wdt = torch.float8_e4m3fn if w.fp8 else adt
-    W13 = torch.empty(E, 2 * I, de, device=device, dtype=wdt)
-    W2 = torch.empty(E, de, I, device=device, dtype=wdt)
     qb = w.quant_block
     W13_scale = W2_scale = None
+    if w.int4:  # packed codes [rows][K/2] and bf16 scales [K/32][rows] per expert
+        W13 = torch.empty(E, 2 * I, de // 2, device=device, dtype=torch.uint8)
+        W2 = torch.empty(E, de, I // 2, device=device, dtype=torch.uint8)
+        W13_scale = torch.empty(E, de // 32, 2 * I, device=device, dtype=torch.bfloat16)
+        W2_scale = torch.empty(E, I // 32, de, device=device, dtype=torch.bfloat16)
+    else:
+        wdt = torch.float8_e4m3fn if w.fp8 else adt
+        W13 = torch.empty(E, 2 * I, de, device=device, dtype=wdt)
+        W2 = torch.empty(E, de, I, device=device, dtype=wdt)
     if w.fp8:
         W13_scale = torch.empty(E, 2 * I // qb, de // qb, device=device, dtype=torch.float32)
         W2_scale = torch.empty(E, de // qb, I // qb, device=device, dtype=torch.float32)
@@ -213,14 +244,18 @@ def make_layer(w: Workload, seed: int = 0, device="cuda") -> Layer:
         m = randn(2 * I, de, std=_std(w, de))
         if w.fp8:
             W13[e], W13_scale[e] = _block_quantize(m, qb)
+        elif w.int4:
+            W13[e], W13_scale[e] = _int4_quantize(m)
         else:
-            W13[e] = m.to(wdt)
+            W13[e] = m.to(W13.dtype)
     for e in range(E):
         m = randn(de, I, std=_std(w, I))
         if w.fp8:
             W2[e], W2_scale[e] = _block_quantize(m, qb)
+        elif w.int4:
+            W2[e], W2_scale[e] = _int4_quantize(m)
         else:
-            W2[e] = m.to(wdt)
+            W2[e] = m.to(W2.dtype)
     Ws13 = Ws2 = Ws13_scale = Ws2_scale = None
     if w.n_shared:
         m13 = randn(2 * Is, d, std=_std(w, d))
@@ -228,8 +263,11 @@ def make_layer(w: Workload, seed: int = 0, device="cuda") -> Layer:
         if w.fp8:
             Ws13, Ws13_scale = _block_quantize(m13, qb)
             Ws2, Ws2_scale = _block_quantize(m2, qb)
+        elif w.int4:
+            Ws13, Ws13_scale = _int4_quantize(m13)
+            Ws2, Ws2_scale = _int4_quantize(m2)
         else:
-            Ws13, Ws2 = m13.to(wdt).contiguous(), m2.to(wdt).contiguous()
+            Ws13, Ws2 = m13.to(adt).contiguous(), m2.to(adt).contiguous()
     W_down = W_up = None
     if L > 0:
         W_down = randn(L, d, std=_std(w, d)).to(adt).contiguous()

@@ -32,9 +32,9 @@ _HDR = os.path.join(_HERE, "moe_oracle.h")
 _BUILD = os.path.join(_HERE, "_build")
 _SO = os.path.join(_BUILD, "libmoe_oracle.so")
 
-F32, BF16, E4M3, F64 = 0, 1, 2, 3
-_DTYPES = {"f32": F32, "bf16": BF16, "e4m3": E4M3, "f64": F64}
-_NP = {F32: np.float32, BF16: np.uint16, E4M3: np.uint8, F64: np.float64}
+F32, BF16, E4M3, F64, INT4 = 0, 1, 2, 3, 4
+_DTYPES = {"f32": F32, "bf16": BF16, "e4m3": E4M3, "f64": F64, "int4": INT4}
+_NP = {F32: np.float32, BF16: np.uint16, E4M3: np.uint8, F64: np.float64, INT4: np.uint8}
 
 _lock = threading.Lock()
 _lib = None
@@ -65,7 +65,7 @@ class _Cfg(ctypes.Structure):
 
 
 class _Tensor(ctypes.Structure):
-    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("pad_", ctypes.c_int32),
+    _fields_ = [("data", ctypes.c_void_p), ("dtype", ctypes.c_int32), ("rows", ctypes.c_int32),
                 ("scale", ctypes.c_void_p)]
 
 
@@ -99,6 +99,9 @@ def _load():
                                            _Tensor, ctypes.c_int, ctypes.c_int, P]
             lib.orc_rmsnorm_unit.restype = None
             lib.orc_rmsnorm_unit.argtypes = [P, ctypes.c_int, ctypes.c_double, P]
+            lib.orc_dequant_row.restype = ctypes.c_int
+            lib.orc_dequant_row.argtypes = [_Tensor, ctypes.c_int64, ctypes.c_int, ctypes.c_int64,
+                                            P]
             lib.orc_dense_mlp.restype = ctypes.c_int
             lib.orc_dense_mlp.argtypes = [ctypes.c_int64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                           _Tensor, _Tensor, _Tensor, P]
@@ -131,8 +134,9 @@ class Config:
 
 @dataclass
 class Mat:
-    """A row-major matrix: ``data`` holds f32 / f64 values, bf16 bit patterns (uint16) or e4m3
-    codes (uint8, with ``scale`` one fp32 per quant_block x quant_block block)."""
+    """A row-major matrix: ``data`` holds f32 / f64 values, bf16 bit patterns (uint16), e4m3
+    codes (uint8, with ``scale`` one fp32 per quant_block x quant_block block) or int4 packed
+    bytes (uint8 [rows][cols/2], with ``scale`` [cols/32][rows], the format of moe_oracle.h)."""
     data: np.ndarray
     dtype: str
     scale: Optional[np.ndarray] = None
@@ -142,11 +146,12 @@ class Mat:
         self.data = np.ascontiguousarray(self.data, dtype=_NP[code])
         if self.scale is not None:
             self.scale = np.ascontiguousarray(self.scale, dtype=np.float32)
-        if code == E4M3 and self.scale is None:
-            raise ValueError("an e4m3 matrix needs its block scales")
+        if code in (E4M3, INT4) and self.scale is None:
+            raise ValueError("an e4m3 or int4 matrix needs its scales")
 
     def _c(self) -> _Tensor:
-        return _Tensor(self.data.ctypes.data, _DTYPES[self.dtype], 0,
+        rows = self.data.shape[0] if _DTYPES[self.dtype] == INT4 else 0
+        return _Tensor(self.data.ctypes.data, _DTYPES[self.dtype], rows,
                        self.scale.ctypes.data if self.scale is not None else None)
 
 
@@ -268,6 +273,15 @@ def swiglu_row(x: np.ndarray, W13: Mat, W2: Mat, I: int, qb: int = 128,
     if st != 0:
         raise RuntimeError(f"orc_swiglu_row failed with status {st}")
     return y
+
+
+def dequant_row(W: Mat, r: int, cols: int, qb: int = 128) -> np.ndarray:
+    """Row r of W widened to fp64 as the oracle's GEMMs see it."""
+    out = np.zeros((cols,), np.float64)
+    st = _load().orc_dequant_row(W._c(), int(cols), int(qb), int(r), _ptr(out))
+    if st != 0:
+        raise RuntimeError(f"orc_dequant_row failed with status {st}")
+    return out
 
 
 def dense_mlp(x: Mat, W13: Mat, W2: Mat, nthreads: int = 1) -> np.ndarray:

@@ -102,6 +102,27 @@ static void e4m3_table_init(void) {
   for (int c = 0; c < 256; ++c) e4m3_table[c] = orc_e4m3_decode((uint8_t)c);
 }
 
+/* Round to the nearest bf16 value (8 significant bits, ties to even) in fp64: v = m 2^e with
+ * 0.5 <= |m| < 1, and m keeps 8 bits.  Normal-range values (every use here is O(1) or a small
+ * integer times a weight scale). */
+static double round_bf16(double v) {
+  int e;
+  const double m = frexp(v, &e);
+  return ldexp(nearbyint(m * 256.0), e - 8); /* the default rounding mode is to nearest even */
+}
+
+/* int4 element (r, c): the nibble of input channel c in row r's packed words, value u - 8, times
+ * the row's scale for its group of 32 channels, rounded once to bf16. */
+static double int4_elem(const orc_tensor* t, int64_t cols, int64_t r, int64_t c) {
+  const int64_t w = c / 8;
+  const int i = (int)(c % 8);
+  const int nib = i / 2 + 4 * (i % 2);
+  const uint8_t byte = ((const uint8_t*)t->data)[r * (cols / 2) + w * 4 + nib / 2];
+  const int u = (byte >> (4 * (nib % 2))) & 0xF;
+  const double s = (double)t->scale[(c / 32) * (int64_t)t->rows + r];
+  return round_bf16((double)(u - 8) * s);
+}
+
 /* Element (r, c) of a row-major [rows][cols] tensor, widened to fp64.  For e4m3 the value is the
  * code's value times the fp32 scale of its qb x qb block. */
 static double elem(const orc_tensor* t, int64_t cols, int qb, int64_t r, int64_t c) {
@@ -114,6 +135,7 @@ static double elem(const orc_tensor* t, int64_t cols, int qb, int64_t r, int64_t
       const double s = (double)t->scale[(r / qb) * nbc + c / qb];
       return e4m3_table[((const uint8_t*)t->data)[r * cols + c]] * s;
     }
+    case ORC_INT4: return int4_elem(t, cols, r, c);
     default: return NAN;
   }
 }
@@ -135,6 +157,20 @@ static double row_dot(const orc_tensor* W, int64_t cols, int qb, int64_t r, cons
     case ORC_BF16: {
       const uint16_t* w = (const uint16_t*)W->data + r * cols;
       for (int64_t c = 0; c < cols; ++c) acc += bf16_bits_to_double(w[c]) * v[c];
+      return acc;
+    }
+    case ORC_INT4: { /* int4_elem per channel, with the 16 values of each group's scale tabled */
+      for (int64_t c0 = 0; c0 < cols; c0 += 32) {
+        double val[16];
+        const double s = (double)W->scale[(c0 / 32) * (int64_t)W->rows + r];
+        for (int u = 0; u < 16; ++u) val[u] = round_bf16((double)(u - 8) * s);
+        const uint8_t* bytes = (const uint8_t*)W->data + r * (cols / 2) + c0 / 2;
+        for (int i = 0; i < 32 && c0 + i < cols; ++i) {
+          const int nib = (i % 8) / 2 + 4 * (i % 2);
+          const int u = (bytes[(i / 8) * 4 + nib / 2] >> (4 * (nib % 2))) & 0xF;
+          acc += val[u] * v[c0 + i];
+        }
+      }
       return acc;
     }
     default:
@@ -550,4 +586,15 @@ int orc_dense_mlp(int64_t T, int d, int I, int nthreads, orc_tensor x, orc_tenso
   }
   free(started); free(jobs); free(th);
   return status;
+}
+
+/* Row r of a matrix [rows][cols] in any ORC_* type, widened to fp64 (the values every GEMM of the
+ * oracle multiplies with). */
+int orc_dequant_row(orc_tensor t, int64_t cols, int qb, int64_t r, double* out) {
+  if (!t.data || !out || cols < 1 || r < 0) return ORC_EINVAL;
+  if ((t.dtype == ORC_E4M3 || t.dtype == ORC_INT4) && !t.scale) return ORC_EINVAL;
+  if (t.dtype == ORC_INT4 && (cols % 32 || r >= t.rows)) return ORC_EINVAL;
+  pthread_once(&e4m3_table_once, e4m3_table_init);
+  for (int64_t c = 0; c < cols; ++c) out[c] = elem(&t, cols, qb, r, c);
+  return ORC_OK;
 }

@@ -30,7 +30,7 @@
 extern "C" {
 #endif
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_F64 = 3 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_F64 = 3, ORC_INT4 = 4 };
 
 typedef struct {
   int64_t T;            /* tokens                                                     */
@@ -51,11 +51,16 @@ typedef struct {
 } orc_config;
 
 /* A row-major matrix in one of the ORC_* types.  For ORC_E4M3, `scale` holds one fp32 scale per
- * quant_block x quant_block block, row-major over [ceil(rows/qb)][ceil(cols/qb)]. */
+ * quant_block x quant_block block, row-major over [ceil(rows/qb)][ceil(cols/qb)].  For ORC_INT4
+ * ("4-bit integer groups"), `data` holds [rows][cols/2] packed bytes: code i of each 32-bit
+ * little-endian word w (input channel 8w + i) is nibble (i / 2) + 4 (i % 2), and a nibble u
+ * stands for u - 8; `scale` holds one scale per 32 input channels of each row, transposed,
+ * [cols/32][rows] (bf16 values widened to fp32); `rows` is the row count; the element is the
+ * product (u - 8) * scale rounded once to bf16 (the GEMM operand). */
 typedef struct {
   const void* data;
   int32_t dtype;
-  int32_t pad_;
+  int32_t rows;         /* ORC_INT4 only: rows of the matrix (the scale layout's pitch) */
   const float* scale;
 } orc_tensor;
 
@@ -115,6 +120,10 @@ int orc_swiglu_row(const double* x, int din, int I, int dout, orc_tensor W13, or
  *  out [T][d] fp64.  nthreads >= 1 worker threads split the tokens. */
 int orc_dense_mlp(int64_t T, int d, int I, int nthreads, orc_tensor x, orc_tensor W13,
                   orc_tensor W2, double* out);
+
+/* Row r of a matrix [rows][cols] of any ORC_* type widened to fp64, the values the oracle's GEMMs
+ * use (e4m3: code value x block scale; int4: RN_bf16((u - 8) x group scale)). */
+int orc_dequant_row(orc_tensor t, int64_t cols, int qb, int64_t r, double* out);
 
 /* RMSNorm with unit weight: y = v / sqrt(mean(v^2) + eps). */
 void orc_rmsnorm_unit(const double* v, int n, double eps, double* y);

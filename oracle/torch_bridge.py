@@ -31,6 +31,8 @@ def mat(t: Optional[torch.Tensor], scale: Optional[torch.Tensor] = None) -> Opti
         return Mat(_np_bits(t), "bf16")
     if t.dtype == torch.float8_e4m3fn:
         return Mat(_np_bits(t), "e4m3", _np_bits(scale.float()))
+    if t.dtype == torch.uint8:  # 4-bit integer groups: packed codes, bf16 scales [K/32][rows]
+        return Mat(_np_bits(t), "int4", _np_bits(scale.float()))
     if t.dtype == torch.float32:
         return Mat(_np_bits(t), "f32")
     if t.dtype == torch.float64:

@@ -180,8 +180,9 @@ def check_expert_rows(layer, g: GpuRun, nrows: int = 6, seed: int = 0, tol=None)
         p = int(perm_src[r])
         t, e = p // k, int(idx[p])
         xr = layer.x[t].double().cpu().numpy()
-        s13 = layer.W13_scale[e] if w.fp8 else None
-        s2 = layer.W2_scale[e] if w.fp8 else None
+        quantized = w.fp8 or getattr(w, "int4", False)
+        s13 = layer.W13_scale[e] if quantized else None
+        s2 = layer.W2_scale[e] if quantized else None
         ref = oracle.swiglu_row(xr, OB.mat(layer.W13[e], s13), OB.mat(layer.W2[e], s2), I=w.I,
                                 qb=w.quant_block, quant_act=w.fp8)
         got = y[r].float().cpu().numpy()

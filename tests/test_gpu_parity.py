@@ -194,6 +194,29 @@ def test_k2_widths_32_experts(cuda_device, flags):
 
 
 # ---------------------------------------------------------------------------------------------
+# 4-bit integer group experts (bf16 activations): the weights both sides use are the decoded
+# RN_bf16((u - 8) * scale) values, so the bf16 bounds apply
+# ---------------------------------------------------------------------------------------------
+
+SMALL_INT4 = replace(S.WORKLOADS["tiny_fp32"], name="small_int4", act="bf16", int4=True,
+                     quant_block=32, T=300, w_init="std0.02", bias_range=0.05)
+
+
+def test_int4_small_all_tokens(cuda_device):
+    _full_check(_layer(SMALL_INT4, seed=31))
+
+
+@pytest.mark.parametrize("T", [1, 17, 129])
+def test_int4_ragged_tokens(cuda_device, T):
+    _full_check(_layer(SMALL_INT4.with_tokens(T), seed=32 + T))
+
+
+def test_int4_k2_widths_32_experts(cuda_device):
+    w = replace(S.WORKLOADS["k2_int4_decode"], name="k2_int4_e32", E=32, T=72)
+    _full_check(_layer(w, seed=33))
+
+
+# ---------------------------------------------------------------------------------------------
 # Full workloads, in the launch configuration of the benchmark (automatic flags)
 # ---------------------------------------------------------------------------------------------
 
@@ -224,6 +247,11 @@ def test_full_k2_prefill(cuda_device):
 def test_full_k3_latent(cuda_device):
     res = _full_workload("k3_latent_bf16")
     print("k3_latent", res)
+
+
+def test_full_k2_int4_decode(cuda_device):
+    res = _full_workload("k2_int4_decode")
+    print("k2_int4_decode", res)
 
 
 def test_full_k2_fp8(cuda_device):

@@ -228,6 +228,71 @@ def test_swiglu_hand_computed(orc):
 
 
 # --------------------------------------------------------------------------------------------
+# 4-bit integer groups
+# --------------------------------------------------------------------------------------------
+
+def test_int4_hand_decoded(orc):
+    """Two rows decoded by hand from the format definition (tests/golden/int4_hand.txt): the
+    nibble order inside a word, the excess-8 codes, the per-32 scale and the bf16 rounding of the
+    product (values that round up, round down and round away in magnitude)."""
+    rows = {r[0]: r[1:] for r in read_golden("int4_hand.txt")}
+    row_bytes = np.array([int(b, 16) for b in rows["bytes"]], np.uint8)
+    packed = np.stack([row_bytes, row_bytes])                      # [2][16]
+    scales = np.array([[float(v) for v in rows["scales"]]], np.float32)  # [K/32 = 1][rows = 2]
+    W = orc.Mat(packed, "int4", scales)
+    r0 = orc.dequant_row(W, 0, 32)
+    assert np.array_equal(r0, np.array([float(v) for v in rows["row0"]]))
+    r1 = orc.dequant_row(W, 1, 32)
+    for pick in rows["row1_picks"]:
+        ch, val = pick.split(":")
+        assert r1[int(ch)] == float(val), pick
+
+
+def test_int4_decode_against_torch(orc):
+    """The oracle's int4 decode of synthetic weights against an independent decode in torch
+    (nibbles by the format, excess-8, times the scale, torch's bf16 rounding)."""
+    from mixture_experts_ffn_gemm_gb300 import synthetic as S
+    g = torch.Generator().manual_seed(11)
+    m = torch.randn(16, 256, generator=g) * 0.02
+    packed, scale = S._int4_quantize(m)
+    W = orc.Mat(packed.numpy(), "int4", scale.float().numpy())
+    b = packed.to(torch.int32)                                        # [16][128] bytes
+    nib = torch.stack([b & 15, b >> 4], dim=-1).reshape(16, 32, 8)    # per word: nibbles 0..7
+    code = nib[:, :, [0, 4, 1, 5, 2, 6, 3, 7]].reshape(16, 256) - 8   # channel 8w + i
+    ref = (code.double() * scale.t().double().repeat_interleave(32, dim=1)).float().bfloat16()
+    for r in range(16):
+        assert np.array_equal(orc.dequant_row(W, r, 256), ref[r].double().numpy())
+
+
+def test_int4_layer_equals_the_bf16_layer_of_its_values(orc):
+    """A layer with int4 experts gives exactly the output of the same layer with bf16 experts
+    holding the decoded values (routing reads no expert weight; the GEMMs see equal fp64 values)."""
+    from dataclasses import replace
+    from mixture_experts_ffn_gemm_gb300 import synthetic as S
+    from oracle import torch_bridge as TB
+    w = replace(S.WORKLOADS["tiny_fp32"], name="tiny_int4", act="bf16", int4=True,
+                quant_block=32, T=24)
+    L4 = S.make_layer(w, seed=5, device="cpu")
+    r4 = TB.forward(L4, nthreads=2)
+
+    def decode(packed, scale):
+        M = orc.Mat(packed.numpy(), "int4", scale.float().numpy())
+        cols = packed.shape[1] * 2
+        return torch.from_numpy(np.stack([orc.dequant_row(M, r, cols)
+                                          for r in range(packed.shape[0])])).bfloat16()
+
+    Lb = S.make_layer(replace(w, int4=False), seed=5, device="cpu")
+    for e in range(w.E):
+        Lb.W13[e] = decode(L4.W13[e], L4.W13_scale[e])
+        Lb.W2[e] = decode(L4.W2[e], L4.W2_scale[e])
+    Lb.Ws13 = decode(L4.Ws13, L4.Ws13_scale)
+    Lb.Ws2 = decode(L4.Ws2, L4.Ws2_scale)
+    rb = TB.forward(Lb, nthreads=2)
+    assert np.array_equal(r4["idx"], rb["idx"])
+    assert np.array_equal(r4["out"], rb["out"])
+
+
+# --------------------------------------------------------------------------------------------
 # The block around the layer: x_ffn = RMSNorm(x'_n), layer, x_{n+1} = x'_n + D_ffn
 # --------------------------------------------------------------------------------------------
 
