@@ -6,21 +6,39 @@
 // excess-8 nibbles and one bf16 scale per 32 input channels (stored [K/32][rows]); the weight is
 // RN_bf16((u - 8) * scale), rounded once as the MMA operand.
 //
-// Orientation: swap-AB as in the bf16 kernel's decode tiles -- M = 128 weight rows (the features
-// of one tile), N = the tile's tokens (at most 32, rounded up to 16).  Decode streams the weights,
-// so the weight bytes (0.5 B + 1/16 B per weight instead of 2 B) bound the layer.
+// Orientation: swap-AB as in the bf16 kernel's decode tiles -- M = 128 weight rows per MMA, N = the
+// tile's tokens (at most 32, rounded up to 16).  Decode streams the weights, so the weight bytes
+// (0.5 B + 1/16 B per weight instead of 2 B) bound the layer, and everything per input channel
+// has to run four times faster than in the bf16 kernel:
+//   * copies: a TMA engine finishes only a few boxes at a time, so a small box costs about as much
+//     as a large one.  One copy stage covers 256 input channels with three boxes: the packed codes
+//     of two 128-row blocks (128 B a row, 32 KB), their scales (8 groups, 4 KB) and the tokens
+//     (4 chunks of 32 rows x 64 channels, 16 KB, each chunk in the MMA's 128-byte swizzled layout);
+//   * the expanded weights never touch shared memory: a converter thread owns one weight row,
+//     expands 64 codes into 32 bf16 pairs in registers and writes them to TMEM with one tcgen05.st;
+//     the MMA takes A from TMEM (row m on lane m, two bf16 per 32-bit column).
+//   * the MMA floor: an M = 128, K = 16 MMA with N <= 32 costs a fixed ~45 cycles, so 32 MMAs per
+//     copy stage stay just under the stage's HBM time -- but only with two issuing warps: one
+//     thread that waits on an mbarrier (or touches shared memory at all) between groups of MMAs
+//     lets the tensor pipe drain and runs at ~90 cycles per MMA.  The two issuers take alternate
+//     64-channel sub-blocks into their own accumulators (split K); the epilogue adds the halves.
+// Blocks: SwiGLU tiles pair 128 W1 rows with the matching 128 W3 rows (h = SiLU(W1 x) * W3 x for
+// 128 features); store tiles take 256 consecutive rows as two blocks (two accumulators).
 //
-// Kernel shape: persistent, one CTA per SM, 320 threads:
-//   warp 0      TMA producer: per K-block (64 input channels) the packed boxes (128 rows x 32 B)
-//               and scale boxes (2 groups x 128 rows) of the tile's weight rows (W1 and W3 for
-//               SwiGLU) and the token box (32 rows x 128 B), into one stage, on full[s];
-//   warps 2..5  converters: thread = weight row; expand its 64 codes per box to bf16 with one
-//               mask-and-OR per pair of codes ((0x4300 | u) is the bf16 of 128 + u), a bf16x2
-//               subtract of 136 and a bf16x2 multiply by the scale, and store them in the
-//               stage's 128-byte-swizzled A tile; fence the async proxy, arrive on conv[s];
-//   warp 1      MMA issuer: tcgen05.mma (A = the converted tile, B = the tokens) into one of two
-//               TMEM accumulators (W1 and W3 side by side for SwiGLU), frees the stage;
-//   warps 6..9  epilogue (TMEM lane quarters): SwiGLU -> bf16 h, or a plain fp32 store.
+// Kernel shape: persistent, one CTA per SM, 480 threads:
+//   warp 0       TMA producer, copy ring (pfull / pempty);
+//   warps 2..9   converters: warp w writes TMEM lanes 32 (w % 4) .. +31 of block (w - 2) / 4; per
+//                copy stage it reads its row's 128 code bytes and 8 scales, releases the stage,
+//                then fills four TMEM sub-stages (64 channels each; cfull / cempty).  Per pair of
+//                codes: one mask-and-OR ((0x4300 | u) is the bf16 of 128 + u), a bf16x2 subtract
+//                of 136 and a bf16x2 multiply by the scale;
+//   warps 1, 14  MMA issuers i = 0, 1: the tile's sub-blocks of parity i (4 K-steps x 2 blocks
+//                each) into accumulator half i of one of two buffers; their commits free the TMEM
+//                sub-stage and, with the converters, the copy stage;
+//   warps 10..13 epilogue (TMEM lane quarters): adds the two halves, SwiGLU -> bf16 h, or plain
+//                fp32 stores.
+// TMEM columns: [0, 256) accumulators [buffer][issuer][block] x 32 columns, then 4 sub-stages of
+// 2 x 32 (sub-stage c is read by issuer c % 2).
 // Every wait is bounded as in the other kernels.
 #include <cstring>
 #include <mutex>
@@ -31,56 +49,51 @@
 
 namespace moe {
 
-constexpr int kW4Conv = 8;                            // converter warps
-constexpr int kW4Threads = 32 * (2 + kW4Conv + 4);    // producer, MMA, converters, epilogue
-constexpr int kW4BK = 64;                  // input channels per stage
+constexpr int kW4Conv = 8;                          // converter warps
+constexpr int kW4Threads = 32 * (3 + kW4Conv + 4);  // producer, 2 MMA, converters, epilogue
+constexpr int kW4Mma1Warp = 2 + kW4Conv + 4;        // the second MMA issuer (the last warp)
+constexpr int kW4BK = 256;                 // input channels per copy stage
+constexpr int kW4Sub = 64;                 // input channels per TMEM sub-stage
 constexpr int kW4BN = 32;                  // tokens per tile
-constexpr int kW4ABox = 128 * 128;         // converted bf16 A tile: 128 rows x 128 bytes
-constexpr int kW4PackBox = 128 * 32;       // packed codes: 128 rows x 32 bytes
-constexpr int kW4ScaleBox = 2 * 128 * 2;   // 2 groups x 128 rows of bf16 scales
-constexpr int kW4TokBox = kW4BN * 128;     // 32 token rows x 128 bytes
+constexpr int kW4ACols = kW4Sub / 2;       // TMEM columns of one block's sub-stage (bf16 pairs)
+constexpr int kW4TokChunk = kW4BN * 128;   // 32 token rows x 128 bytes
+constexpr int kW4PackBlock = 128 * 128;    // 128 rows x 128 code bytes
+constexpr int kW4ScaleBlock = 8 * 128 * 2; // 8 groups x 128 rows of bf16 scales
 constexpr int kW4MaxGroups = 1025;
 constexpr int kW4SmemLimit = 232448;
+constexpr int kW4TmemCols = 512;
 
-// Two rings: copy stages (tokens, packed codes, scales: what the TMA brings, small, so that several
-// are in flight while the weights stream from HBM) and converted stages (the bf16 A tiles and a
-// copy of the tokens: what the MMA reads; enough of them to cover the converter -> MMA -> release
-// round trip).
-template <bool kSwiGLU>
 struct W4Shape {
-  static constexpr int NW = kSwiGLU ? 2 : 1;  // weight boxes per K-block
-  static constexpr int P_TOK = 0;
-  static constexpr int P_PACK = kW4TokBox;
-  static constexpr int P_SCALE = P_PACK + NW * kW4PackBox;
-  static constexpr int PSTAGE = (P_SCALE + NW * kW4ScaleBox + 1023) & ~1023;
-  static constexpr int TX = kW4TokBox + NW * (kW4PackBox + kW4ScaleBox);  // TMA bytes per stage
-  static constexpr int C_TOK = NW * kW4ABox;
-  static constexpr int CSTAGE = C_TOK + kW4TokBox;
-  static constexpr int CSTAGES = kSwiGLU ? 4 : 6;
-  static constexpr int ACC_COLS = NW * kW4BN;
-  static constexpr int TMEM_COLS = 2 * ACC_COLS <= 64 ? 64 : 128;
+  static constexpr int P_TOK = 0;                           // [4 chunks][32 rows][128 B]
+  static constexpr int P_PACK = 4 * kW4TokChunk;            // [2 blocks][128 rows][128 B]
+  static constexpr int P_SCALE = P_PACK + 2 * kW4PackBlock; // [2 blocks][8 groups][128 rows]
+  static constexpr int PSTAGE = P_SCALE + 2 * kW4ScaleBlock;
+  static constexpr int TX = PSTAGE;                         // TMA bytes per copy stage
+  static constexpr int ACC_COLS = 2 * 2 * kW4BN;  // one buffer: [issuer][block] x 32 columns
+  static constexpr int A_COL0 = 2 * ACC_COLS;
+  static constexpr int CSTAGE_COLS = 2 * kW4ACols;
+  static constexpr int CSTAGES = (kW4TmemCols - A_COL0) / CSTAGE_COLS;
   static constexpr int TABLE_BYTES = 2 * (kW4MaxGroups + 1) * 4 + kW4Threads * 4;
-  static constexpr int BAR_BYTES = 256 + 64;
-  static constexpr int PSTAGES_FIT =
-      (kW4SmemLimit - 1024 - BAR_BYTES - TABLE_BYTES - CSTAGES * CSTAGE) / PSTAGE;
-  static constexpr int PSTAGES_MAX = kSwiGLU ? 5 : 7;
-  static constexpr int PSTAGES = PSTAGES_FIT > PSTAGES_MAX ? PSTAGES_MAX : PSTAGES_FIT;
-  static constexpr int RINGS = CSTAGES * CSTAGE + PSTAGES * PSTAGE;
+  static constexpr int NBARS = 32;
+  static constexpr int BAR_BYTES = NBARS * 8 + 64;
+  static constexpr int PSTAGES = (kW4SmemLimit - 1024 - BAR_BYTES - TABLE_BYTES) / PSTAGE;
+  static constexpr int RINGS = PSTAGES * PSTAGE;
   static constexpr int SMEM = 1024 + RINGS + BAR_BYTES + TABLE_BYTES;
-  static_assert(PSTAGES >= 4, "not enough shared memory for the copy ring");
+  static_assert(PSTAGES >= 3, "not enough shared memory for the copy ring");
+  static_assert(CSTAGES >= 4 && CSTAGES % 2 == 0, "TMEM ring: even, at least 4 sub-stages");
   static_assert(SMEM <= kW4SmemLimit, "shared memory");
-  static_assert(2 * PSTAGES + 2 * CSTAGES + 5 <= 32, "barrier area too small");
-  static_assert(CSTAGE % 1024 == 0 && PSTAGE % 1024 == 0 && P_SCALE % 128 == 0,
+  static_assert(2 * PSTAGES + 2 * CSTAGES + 6 <= NBARS, "barrier area too small");
+  static_assert(PSTAGE % 1024 == 0 && P_PACK % 1024 == 0 && P_SCALE % 128 == 0,
                 "TMA and MMA operands misaligned");
 };
 
 struct W4Params {
-  CUtensorMap map_act, map_act_d;  // tokens, bf16 [rows][K], box {64, 32}, 128-byte swizzle
-  CUtensorMap map_wq, map_wq_d;    // packed codes, uint8 [w_rows][K/2], box {32, 128}
-  CUtensorMap map_ws, map_ws_d;    // scales, bf16: routed [E * K/32][w_group_rows] (each expert's
-                                   // [K/32][rows] in turn), dense [K/32][w_d_rows]; box {128, 2}
+  CUtensorMap map_act, map_act_d;  // tokens, bf16, 3D {64, rows, K/64}, box {64, 32, 4}, swizzled
+  CUtensorMap map_wq, map_wq_d;    // codes, uint8, 3D {K/2, rows - blk, 2}, box {128, 128, 2}
+  CUtensorMap map_ws, map_ws_d;    // scales, bf16, 3D {rows_per_group - blk, groups K/32, 2},
+                                   // box {128, 8, 2}: routed experts' [K/32][rows] in turn
   const int32_t* offsets;
-  int32_t n_routed, w_group_rows, u_off, u_off_d;
+  int32_t n_routed, w_group_rows;
   int32_t dense_rows, dense_act_row0, dense_out_row0;
   int32_t K, F;
   void* out;  // SwiGLU: bf16 h [rows][ldo]; store: fp32 [rows][ldo]
@@ -88,10 +101,19 @@ struct W4Params {
   uint32_t* err;
 };
 
-// Four bf16 pairs (one 16-byte chunk: input channels 8i .. 8i+7) from one packed word.
-__device__ __forceinline__ uint4 w4_expand_word(uint32_t w, __nv_bfloat162 s2) {
+__device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
+// Four bf16 pairs (input channels 8i .. 8i+7, the even channel in each low half) from one packed
+// word, whose code c sits in nibble c/2 + 4 (c % 2).
+__device__ __forceinline__ void w4_expand_word(uint32_t w, __nv_bfloat162 s2, uint32_t* r) {
   const __nv_bfloat162 off = __floats2bfloat162_rn(136.0f, 136.0f);
-  uint32_t r[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const uint32_t bits = ((w >> (4 * j)) & 0x000F000Fu) | 0x43004300u;  // bf16(128 + u) pair
@@ -99,17 +121,15 @@ __device__ __forceinline__ uint4 w4_expand_word(uint32_t w, __nv_bfloat162 s2) {
     v = __hmul2(__hsub2(v, off), s2);  // (u - 8) exact, then one rounding of the product
     r[j] = *reinterpret_cast<const uint32_t*>(&v);
   }
-  return make_uint4(r[0], r[1], r[2], r[3]);
 }
 
 template <bool kSwiGLU>
 __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid_constant__ W4Params p) {
-  using S = W4Shape<kSwiGLU>;
+  using S = W4Shape;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* cring = smem;                             // [CSTAGES][CSTAGE]
-  uint8_t* pring = smem + S::CSTAGES * S::CSTAGE;    // [PSTAGES][PSTAGE]
+  uint8_t* pring = smem;  // [PSTAGES][PSTAGE]
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::RINGS);
   uint64_t* pfull = bars;
   uint64_t* pempty = pfull + S::PSTAGES;
@@ -117,8 +137,8 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
   uint64_t* cempty = cfull + S::CSTAGES;
   uint64_t* tfull = cempty + S::CSTAGES;
   uint64_t* tempty = tfull + 2;
-  uint64_t* drain = tempty + 2;
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 32);
+  uint64_t* drain = tempty + 2;  // one per issuer
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + S::NBARS);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
   int* tile_start = reinterpret_cast<int*>(smem + S::RINGS + S::BAR_BYTES);
   int* row_start = tile_start + (kW4MaxGroups + 1);
@@ -126,21 +146,22 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const int rows_per_tile = kSwiGLU ? 128 : 256;  // features a tile covers
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S::PSTAGES; ++s) {
       mbar_init(&pfull[s], 1);
-      mbar_init(&pempty[s], kW4Conv);  // one arrival per converter warp
+      mbar_init(&pempty[s], kW4Conv + 2);  // every converter warp and both issuers
     }
     for (int s = 0; s < S::CSTAGES; ++s) {
       mbar_init(&cfull[s], kW4Conv);
       mbar_init(&cempty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(&tfull[a], 1);
+      mbar_init(&tfull[a], 2);
       mbar_init(&tempty[a], 128);
+      mbar_init(&drain[a], 1);
     }
-    mbar_init(drain, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -150,18 +171,19 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
     tma_prefetch_map(&p.map_ws);
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, S::TMEM_COLS);
+    tmem_alloc(tmem_holder, kW4TmemCols);
     tmem_relinquish();
   }
   build_tile_table(tile_start, row_start, scratch, p.offsets, p.n_routed, p.dense_rows, kW4BN,
-                   p.F / 128);  // ends with __syncthreads
+                   p.F / rows_per_tile);  // ends with __syncthreads
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int G = p.n_routed + (p.dense_rows > 0 ? 1 : 0);
   const int total = tile_start[G];
-  const int nkb = p.K / kW4BK;
+  const int nsub_all = p.K / kW4Sub;                // TMEM sub-stages per tile (even)
+  const int nkb = (nsub_all + 3) / 4;               // copy stages per tile (the last may be short)
 
   if (warp == 0) {
     if (lane == 0) {  // ------------------------------------------------ TMA producer
@@ -175,10 +197,9 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
         const CUtensorMap* mq = ti.dense ? &p.map_wq_d : &p.map_wq;
         const CUtensorMap* ms = ti.dense ? &p.map_ws_d : &p.map_ws;
         const int act_y = ti.grp_row0 + ti.rt * kW4BN;
-        const int w_local = ti.ft * 128;  // the tile's first row within its group's weights
+        const int w_local = ti.ft * rows_per_tile;  // block 0's first row within its group
         const int w_y = (ti.dense ? 0 : ti.g * p.w_group_rows) + w_local;
         const int s_y = ti.dense ? 0 : ti.g * (p.K / 32);  // the group's first scale row
-        const int u_off = ti.dense ? p.u_off_d : p.u_off;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&pempty[stage], phase ^ 1u, abort_flag, p.err)) {
             ok = false;
@@ -186,14 +207,9 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
           }
           uint8_t* st = pring + stage * S::PSTAGE;
           mbar_arrive_expect_tx(&pfull[stage], S::TX);
-          tma_load_2d(st + S::P_TOK, ma, &pfull[stage], kb * kW4BK, act_y);
-#pragma unroll
-          for (int j = 0; j < S::NW; ++j) {
-            tma_load_2d(st + S::P_PACK + j * kW4PackBox, mq, &pfull[stage], kb * (kW4BK / 2),
-                        w_y + j * u_off);
-            tma_load_2d(st + S::P_SCALE + j * kW4ScaleBox, ms, &pfull[stage], w_local + j * u_off,
-                        s_y + kb * 2);
-          }
+          tma_load_3d(st + S::P_TOK, ma, &pfull[stage], 0, act_y, kb * 4);
+          tma_load_3d(st + S::P_PACK, mq, &pfull[stage], kb * (kW4BK / 2), w_y, 0);
+          tma_load_3d(st + S::P_SCALE, ms, &pfull[stage], w_local, s_y + kb * 8, 0);
           if (armed < S::PSTAGES) ++armed;
           if (++stage == S::PSTAGES) {
             stage = 0;
@@ -214,63 +230,76 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
     }
   } else if (warp >= 2 && warp < 2 + kW4Conv) {
     // ---------------------------------------------------------------- converters
-    const int ct = (warp - 2) * 32 + lane;  // 0 .. 255
+    const int j = (warp - 2) >> 2;  // the block this warp expands
+    const int quarter = warp & 3;   // the TMEM lanes this warp may write
+    const int row = quarter * 32 + lane;
+    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + j * kW4ACols;
     uint32_t ps = 0, pph = 0, cs = 0, cph = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
-      for (int kb = 0; kb < nkb; ++kb) {
+      for (int kb = 0; kb < nkb && ok; ++kb) {
+        const int nsub = min(4, nsub_all - kb * 4);
         int w_ok = 1;
-        if (lane == 0)
-          w_ok = (mbar_wait(&pfull[ps], pph, abort_flag, p.err) &&
-                  mbar_wait(&cempty[cs], cph ^ 1u, abort_flag, p.err)) ? 1 : 0;
+        if (lane == 0) w_ok = mbar_wait(&pfull[ps], pph, abort_flag, p.err) ? 1 : 0;
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
         if (!w_ok) {
           ok = false;
           break;
         }
+        // this row's 128 code bytes (128-byte swizzle: chunk c sits at c ^ (row % 8)) and scales
         const uint8_t* src = pring + ps * S::PSTAGE;
-        uint8_t* dst = cring + cs * S::CSTAGE;
-        // units (box j, scale group g, row): lanes take consecutive rows
+        const uint8_t* qrow = src + S::P_PACK + j * kW4PackBlock + row * 128;
+        const __nv_bfloat16* srow =
+            reinterpret_cast<const __nv_bfloat16*>(src + S::P_SCALE + j * kW4ScaleBlock) + row;
+        uint4 q[8];
+        __nv_bfloat162 sc[8];
 #pragma unroll
-        for (int u = ct; u < S::NW * 256; u += 256) {
-          const int j = u >> 8, g = (u >> 7) & 1, row = u & 127;
-          const uint4 q = *reinterpret_cast<const uint4*>(src + S::P_PACK + j * kW4PackBox +
-                                                          row * 32 + g * 16);
-          const __nv_bfloat16 sc = *reinterpret_cast<const __nv_bfloat16*>(
-              src + S::P_SCALE + j * kW4ScaleBox + (g * 128 + row) * 2);
-          const __nv_bfloat162 s2 = __bfloat162bfloat162(sc);
-          const uint32_t words[4] = {q.x, q.y, q.z, q.w};
-          uint8_t* a_row = dst + j * kW4ABox + row * 128;
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int chunk = g * 4 + i;  // 16-byte chunk of the 128-byte row
-            *reinterpret_cast<uint4*>(a_row + ((chunk ^ (row & 7)) << 4)) =
-                w4_expand_word(words[i], s2);
-          }
+        for (int c = 0; c < 8; ++c) {
+          q[c] = *reinterpret_cast<const uint4*>(qrow + ((c ^ (row & 7)) << 4));
+          sc[c] = __bfloat162bfloat162(srow[c * 128]);
         }
-        // the token box moves as is (both stages are 1024-byte aligned: the swizzle is kept)
-        reinterpret_cast<uint4*>(dst + S::C_TOK)[ct] =
-            reinterpret_cast<const uint4*>(src + S::P_TOK)[ct];
-        // the tensor core reads the converted stage through the async proxy
-        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&cfull[cs]);
-          mbar_arrive(&pempty[ps]);
-        }
+        if (lane == 0) mbar_arrive(&pempty[ps]);  // the stage's codes and scales are in registers
         if (++ps == S::PSTAGES) {
           ps = 0;
           pph ^= 1u;
         }
-        if (++cs == S::CSTAGES) {
-          cs = 0;
-          cph ^= 1u;
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+          if (b < nsub) {
+            if (lane == 0) w_ok = mbar_wait(&cempty[cs], cph ^ 1u, abort_flag, p.err) ? 1 : 0;
+            w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+            if (!w_ok) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            uint32_t a[32];
+            w4_expand_word(q[2 * b].x, sc[2 * b], a + 0);
+            w4_expand_word(q[2 * b].y, sc[2 * b], a + 4);
+            w4_expand_word(q[2 * b].z, sc[2 * b], a + 8);
+            w4_expand_word(q[2 * b].w, sc[2 * b], a + 12);
+            w4_expand_word(q[2 * b + 1].x, sc[2 * b + 1], a + 16);
+            w4_expand_word(q[2 * b + 1].y, sc[2 * b + 1], a + 20);
+            w4_expand_word(q[2 * b + 1].z, sc[2 * b + 1], a + 24);
+            w4_expand_word(q[2 * b + 1].w, sc[2 * b + 1], a + 28);
+            tmem_st32(t_lane + S::A_COL0 + cs * S::CSTAGE_COLS, a);
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&cfull[cs]);
+            if (++cs == S::CSTAGES) {
+              cs = 0;
+              cph ^= 1u;
+            }
+          }
         }
       }
     }
-  } else if (warp == 1) {
-    if (lane == 0) {  // ------------------------------------------------ MMA issuer
-      uint32_t cs = 0, cph = 0, acc = 0, acc_phase = 0;
+  } else if (warp == 1 || warp == kW4Mma1Warp) {
+    if (lane == 0) {  // ------------------------------------------------ MMA issuers
+      const int me = warp == 1 ? 0 : 1;
+      uint32_t ps = 0, pph = 0, m = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
@@ -279,27 +308,38 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
         const uint32_t idesc = idesc_bf16_f32_n(n);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem_base + acc * S::ACC_COLS;
-        for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&cfull[cs], cph, abort_flag, p.err)) {
+        const uint32_t d0 = tmem_base + acc * S::ACC_COLS + me * 2 * kW4BN;
+        uint32_t accum = 0;
+        for (int kb = 0; kb < nkb && ok; ++kb) {
+          const int nsub = min(4, nsub_all - kb * 4);  // 2 or 4: every stage has work for both
+          if (!mbar_wait(&pfull[ps], pph, abort_flag, p.err)) {  // the stage's tokens
             ok = false;
             break;
           }
-          tc_fence_after();
-          const uint32_t st = smem_u32(cring + cs * S::CSTAGE);
+          const uint32_t tok = smem_u32(pring + ps * S::PSTAGE + S::P_TOK);
+          for (int b = me; b < nsub; b += 2, ++m) {
+            const uint32_t cs = me + 2 * (m % (S::CSTAGES / 2));
+            const uint32_t cph = (m / (S::CSTAGES / 2)) & 1u;
+            if (!mbar_wait(&cfull[cs], cph, abort_flag, p.err)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = tmem_base + S::A_COL0 + cs * S::CSTAGE_COLS;
 #pragma unroll
-          for (int k16 = 0; k16 < kW4BK / 16; ++k16) {
-            const uint32_t accum = (kb | k16) != 0;
-            const uint64_t bdesc = sw128_kmajor_desc(st + S::C_TOK + k16 * 32);
-#pragma unroll
-            for (int j = 0; j < S::NW; ++j)
-              mma_bf16(d0 + j * kW4BN, sw128_kmajor_desc(st + j * kW4ABox + k16 * 32), bdesc,
-                       idesc, accum);
+            for (int k16 = 0; k16 < kW4Sub / 16; ++k16) {
+              const uint64_t bdesc = sw128_kmajor_desc(tok + b * kW4TokChunk + k16 * 32);
+              mma_bf16_tmem_a(d0, a0 + k16 * 8, bdesc, idesc, accum);
+              mma_bf16_tmem_a(d0 + kW4BN, a0 + kW4ACols + k16 * 8, bdesc, idesc, accum);
+              accum = 1;
+            }
+            mma_commit(&cempty[cs]);
           }
-          mma_commit(&cempty[cs]);
-          if (++cs == S::CSTAGES) {
-            cs = 0;
-            cph ^= 1u;
+          if (!ok) break;
+          mma_commit(&pempty[ps]);
+          if (++ps == S::PSTAGES) {
+            ps = 0;
+            pph ^= 1u;
           }
         }
         if (!ok) break;
@@ -307,8 +347,8 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
-      mma_commit(drain);
-      mbar_wait(drain, 0, nullptr, nullptr, kDrainLimitNs);
+      mma_commit(&drain[me]);
+      mbar_wait(&drain[me], 0, nullptr, nullptr, kDrainLimitNs);
     }
   } else {
     // ---------------------------------------------------------------- epilogue (4 warps)
@@ -326,22 +366,28 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
       const uint32_t tb = tmem_base + acc * S::ACC_COLS + ((uint32_t)(quarter * 32) << 16);
       const int64_t out_row0 = (ti.dense ? (int64_t)p.dense_out_row0 : (int64_t)ti.grp_row0) +
                                (int64_t)ti.rt * kW4BN;
-      const int64_t feat = (int64_t)ti.ft * 128 + r;
+      const int64_t feat = (int64_t)ti.ft * rows_per_tile + r;
 #pragma unroll 1
       for (int c = 0; c < kW4BN && c < ti.valid; c += 16) {
-        uint32_t gv[16], uv[16];
-        tmem_ld16(tb + c, gv);
-        if (kSwiGLU) tmem_ld16(tb + kW4BN + c, uv);
+        uint32_t v0[16], v1[16], w0[16], w1[16];  // [issuer 0 | 1] x [block 0 | 1]
+        tmem_ld16(tb + c, v0);
+        tmem_ld16(tb + kW4BN + c, v1);
+        tmem_ld16(tb + 2 * kW4BN + c, w0);
+        tmem_ld16(tb + 3 * kW4BN + c, w1);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           if (c + i < ti.valid) {
             const int64_t orow = out_row0 + c + i;
+            const float y0 = __uint_as_float(v0[i]) + __uint_as_float(w0[i]);
+            const float y1 = __uint_as_float(v1[i]) + __uint_as_float(w1[i]);
             if (kSwiGLU) {
-              const float h = silu_fast(__uint_as_float(gv[i])) * __uint_as_float(uv[i]);
-              ((__nv_bfloat16*)p.out)[orow * p.ldo + feat] = __float2bfloat16_rn(h);
+              ((__nv_bfloat16*)p.out)[orow * p.ldo + feat] =
+                  __float2bfloat16_rn(silu_fast(y0) * y1);
             } else {
-              ((float*)p.out)[orow * p.ldo + feat] = __uint_as_float(gv[i]);
+              float* o = (float*)p.out + orow * p.ldo + feat;
+              o[0] = y0;
+              o[128] = y1;
             }
           }
         }
@@ -357,7 +403,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
   __syncthreads();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, S::TMEM_COLS);
+    tmem_dealloc(tmem_base, kW4TmemCols);
   }
 }
 
@@ -383,62 +429,74 @@ static EncodeTiledFnW4 encode_fn_w4() {
   return fn;
 }
 
-// 2D map over [outer][inner] elements with a dense row pitch, box {box_in, box_out}, zero fill.
-static bool make_map_w4(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base,
-                        int64_t outer, int64_t inner, int box_in, int box_out,
+// 3D map: dims {d0, d1, d2} elements, byte strides {s1, s2} of dims 1 and 2, box {b0, b1, b2}.
+static bool make_map_w4(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int64_t d0,
+                        int64_t d1, int64_t d2, int64_t s1, int64_t s2, int b0, int b1, int b2,
                         CUtensorMapSwizzle swz) {
   EncodeTiledFnW4 enc = encode_fn_w4();
-  if (!enc || !base || outer <= 0 || inner <= 0) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)outer};
-  cuuint64_t strides[1] = {(cuuint64_t)(inner * esize)};
-  cuuint32_t box[2] = {(cuuint32_t)box_in, (cuuint32_t)box_out};
-  cuuint32_t estr[2] = {1, 1};
-  return enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+  if (!enc || !base || d0 <= 0 || d1 <= 0 || d2 <= 0) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d0, (cuuint64_t)d1, (cuuint64_t)d2};
+  cuuint64_t strides[2] = {(cuuint64_t)s1, (cuuint64_t)s2};
+  cuuint32_t box[3] = {(cuuint32_t)b0, (cuuint32_t)b1, (cuuint32_t)b2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, dt, 3, const_cast<void*>(base), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// groups: the weight groups the scales come in (n experts each [K/32][rows_per_group]).
+// The three maps of one weight set.  groups: how many [rows_per_group] weight groups (each with
+// its [K/32][rows_per_group] scales); blk: rows from block 0 to block 1.  The row extents stop
+// `blk` rows short of the end, so that block 1 of the last tile is still inside the tensor.
 static bool w4_maps(CUtensorMap* act, CUtensorMap* wq, CUtensorMap* ws, const void* a,
                     int64_t a_rows, const void* q, const void* s, int64_t groups,
-                    int64_t rows_per_group, int K) {
-  return make_map_w4(act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, a, a_rows, K, kW4BK, kW4BN,
-                     CU_TENSOR_MAP_SWIZZLE_128B) &&
-         make_map_w4(wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, q, groups * rows_per_group, K / 2,
-                     kW4BK / 2, 128, CU_TENSOR_MAP_SWIZZLE_NONE) &&
-         make_map_w4(ws, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, s, groups * (K / 32), rows_per_group,
-                     128, 2, CU_TENSOR_MAP_SWIZZLE_NONE);
+                    int64_t rows_per_group, int64_t blk, int K) {
+  const int64_t half_k = K / 2;
+  return make_map_w4(act, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, kW4Sub, a_rows, K / kW4Sub,
+                     (int64_t)K * 2, kW4Sub * 2, kW4Sub, kW4BN, 4, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map_w4(wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, q, half_k, groups * rows_per_group - blk, 2,
+                     half_k, blk * half_k, kW4BK / 2, 128, 2, CU_TENSOR_MAP_SWIZZLE_128B) &&
+         make_map_w4(ws, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, s, rows_per_group - blk,
+                     groups * (K / 32), 2, rows_per_group * 2, blk * 2, 128, kW4BK / 32, 2,
+                     CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 template <bool kSwiGLU>
 static cudaError_t launch_w4_variant(const W4Params& p, int grid, cudaStream_t st,
                                      const char* label) {
-  using S = W4Shape<kSwiGLU>;
   auto kern = moe_gemm_w4_kernel<kSwiGLU>;
   static int attr_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (attr_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, S::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, W4Shape::SMEM);
     if (e != cudaSuccess) return e;
     attr_dev = dev;
   }
   LaunchScope ls(label, st);
-  kern<<<grid, kW4Threads, S::SMEM, st>>>(p);
+  kern<<<grid, kW4Threads, W4Shape::SMEM, st>>>(p);
   return cudaGetLastError();
 }
 
 cudaError_t launch_gemm_w4(const W4Gemm& g, int num_sms, cudaStream_t st) {
-  if (g.K % kW4BK || g.F % 128 || g.n_routed > kW4MaxGroups - 1) return cudaErrorInvalidValue;
+  // SwiGLU tiles: 128 features from W1 rows and the W3 rows u_off further; store tiles: 256 rows
+  const int tile_rows = g.swiglu ? 128 : 256;
+  if (g.K % (2 * kW4Sub) || g.F % tile_rows || g.n_routed > kW4MaxGroups - 1)
+    return cudaErrorInvalidValue;
   if (g.w_group_rows % 128 || g.ldo % 8) return cudaErrorInvalidValue;
+  const int blk = g.swiglu ? g.u_off : 128;
+  const int blk_d = g.swiglu ? g.u_off_d : 128;
+  if (g.swiglu && (blk < g.F || (g.dense_rows > 0 && blk_d < g.F))) return cudaErrorInvalidValue;
   W4Params p;
   memset(&p, 0, sizeof(p));
   if (g.n_routed > 0 && (g.w_rows != (int64_t)g.n_routed * g.w_group_rows ||
+                         g.w_group_rows < blk + g.F - (g.swiglu ? 0 : 128) ||
                          !w4_maps(&p.map_act, &p.map_wq, &p.map_ws, g.act, g.act_rows, g.wq, g.ws,
-                                  g.n_routed, g.w_group_rows, g.K)))
+                                  g.n_routed, g.w_group_rows, blk, g.K)))
     return cudaErrorInvalidValue;
-  if (g.dense_rows > 0 && !w4_maps(&p.map_act_d, &p.map_wq_d, &p.map_ws_d, g.act_d, g.act_d_rows,
-                                   g.wq_d, g.ws_d, 1, g.w_d_rows, g.K))
+  if (g.dense_rows > 0 && (g.w_d_rows < blk_d + g.F - (g.swiglu ? 0 : 128) ||
+                           !w4_maps(&p.map_act_d, &p.map_wq_d, &p.map_ws_d, g.act_d, g.act_d_rows,
+                                    g.wq_d, g.ws_d, 1, g.w_d_rows, blk_d, g.K)))
     return cudaErrorInvalidValue;
   if (g.n_routed == 0) {  // keep the unused maps valid objects
     p.map_act = p.map_act_d;
@@ -453,8 +511,6 @@ cudaError_t launch_gemm_w4(const W4Gemm& g, int num_sms, cudaStream_t st) {
   p.offsets = g.offsets;
   p.n_routed = g.n_routed;
   p.w_group_rows = g.w_group_rows;
-  p.u_off = g.u_off;
-  p.u_off_d = g.u_off_d;
   p.dense_rows = g.dense_rows;
   p.dense_act_row0 = g.dense_act_row0;
   p.dense_out_row0 = g.dense_out_row0;
