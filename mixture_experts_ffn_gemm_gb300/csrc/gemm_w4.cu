@@ -25,20 +25,23 @@
 // Blocks: SwiGLU tiles pair 128 W1 rows with the matching 128 W3 rows (h = SiLU(W1 x) * W3 x for
 // 128 features); store tiles take 256 consecutive rows as two blocks (two accumulators).
 //
-// Kernel shape: persistent, one CTA per SM, 480 threads:
+// Kernel shape: persistent, one CTA per SM, 736 threads (23 warps):
 //   warp 0       TMA producer, copy ring (pfull / pempty);
-//   warps 2..9   converters: warp w writes TMEM lanes 32 (w % 4) .. +31 of block (w - 2) / 4; per
-//                copy stage it reads its row's 128 code bytes and 8 scales, releases the stage,
-//                then fills four TMEM sub-stages (64 channels each; cfull / cempty).  Per pair of
-//                codes: one mask-and-OR ((0x4300 | u) is the bf16 of 128 + u), a bf16x2 subtract
-//                of 136 and a bf16x2 multiply by the scale;
-//   warps 1, 14  MMA issuers i = 0, 1: the tile's sub-blocks of parity i (4 K-steps x 2 blocks
-//                each) into accumulator half i of one of two buffers; their commits free the TMEM
-//                sub-stage and, with the converters, the copy stage;
-//   warps 10..13 epilogue (TMEM lane quarters): adds the two halves, SwiGLU -> bf16 h, or plain
-//                fp32 stores.
-// TMEM columns: [0, 256) accumulators [buffer][issuer][block] x 32 columns, then 4 sub-stages of
-// 2 x 32 (sub-stage c is read by issuer c % 2).
+//   warps 2..17  converters in two groups: group g = (w - 2) / 8 expands the sub-blocks of parity
+//                g (those MMA issuer g takes), block ((w - 2) / 4) % 2, and writes TMEM lanes
+//                32 (w % 4) .. +31 (thread = weight row).  Per copy stage a warp reads its row's
+//                codes and scales of its two sub-blocks before any tcgen05 operation (a shared-
+//                memory read behind outstanding tcgen05 work stalls), releases the stage, then
+//                fills one TMEM sub-stage per sub-block (cfull / cempty).  Per pair of codes: one
+//                mask-and-OR ((0x4300 | u) is the bf16 of 128 + u), a bf16x2 subtract of 136 and a
+//                bf16x2 multiply by the scale;
+//   warps 1, 22  MMA issuers i = 0, 1: the tile's sub-blocks of parity i (4 K-steps x 2 blocks
+//                each) into accumulator half i; their commits free the TMEM sub-stage and, with
+//                the converters, the copy stage;
+//   warps 18..21 epilogue (TMEM lane quarters): reads and adds the two halves, frees the
+//                accumulator at once, then SwiGLU -> bf16 h, or plain fp32 stores.
+// TMEM columns: [0, 128) the accumulator [issuer][block] x 32 columns (one buffer: the epilogue
+// holds it only for its reads), then 6 sub-stages of 2 x 32 (sub-stage c is read by issuer c % 2).
 // Every wait is bounded as in the other kernels.
 #include <cstring>
 #include <mutex>
@@ -49,7 +52,7 @@
 
 namespace moe {
 
-constexpr int kW4Conv = 8;                          // converter warps
+constexpr int kW4Conv = 16;                         // converter warps: 2 groups x 2 blocks x 4
 constexpr int kW4Threads = 32 * (3 + kW4Conv + 4);  // producer, 2 MMA, converters, epilogue
 constexpr int kW4Mma1Warp = 2 + kW4Conv + 4;        // the second MMA issuer (the last warp)
 constexpr int kW4BK = 256;                 // input channels per copy stage
@@ -69,8 +72,8 @@ struct W4Shape {
   static constexpr int P_SCALE = P_PACK + 2 * kW4PackBlock; // [2 blocks][8 groups][128 rows]
   static constexpr int PSTAGE = P_SCALE + 2 * kW4ScaleBlock;
   static constexpr int TX = PSTAGE;                         // TMA bytes per copy stage
-  static constexpr int ACC_COLS = 2 * 2 * kW4BN;  // one buffer: [issuer][block] x 32 columns
-  static constexpr int A_COL0 = 2 * ACC_COLS;
+  static constexpr int ACC_COLS = 2 * 2 * kW4BN;  // [issuer][block] x 32 columns
+  static constexpr int A_COL0 = ACC_COLS;
   static constexpr int CSTAGE_COLS = 2 * kW4ACols;
   static constexpr int CSTAGES = (kW4TmemCols - A_COL0) / CSTAGE_COLS;
   static constexpr int TABLE_BYTES = 2 * (kW4MaxGroups + 1) * 4 + kW4Threads * 4;
@@ -123,6 +126,22 @@ __device__ __forceinline__ void w4_expand_word(uint32_t w, __nv_bfloat162 s2, ui
   }
 }
 
+// One sub-block (64 input channels) of one weight row: its 32 code bytes (q0: channels 0..31,
+// q1: 32..63) and the scales of its two groups.
+__device__ __forceinline__ void w4_expand_sub(uint4 q0, uint4 q1, __nv_bfloat16 sc0,
+                                              __nv_bfloat16 sc1, uint32_t (&a)[32]) {
+  const __nv_bfloat162 s0 = __bfloat162bfloat162(sc0);
+  const __nv_bfloat162 s1 = __bfloat162bfloat162(sc1);
+  w4_expand_word(q0.x, s0, a + 0);
+  w4_expand_word(q0.y, s0, a + 4);
+  w4_expand_word(q0.z, s0, a + 8);
+  w4_expand_word(q0.w, s0, a + 12);
+  w4_expand_word(q1.x, s1, a + 16);
+  w4_expand_word(q1.y, s1, a + 20);
+  w4_expand_word(q1.z, s1, a + 24);
+  w4_expand_word(q1.w, s1, a + 28);
+}
+
 template <bool kSwiGLU>
 __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid_constant__ W4Params p) {
   using S = W4Shape;
@@ -154,7 +173,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
       mbar_init(&pempty[s], kW4Conv + 2);  // every converter warp and both issuers
     }
     for (int s = 0; s < S::CSTAGES; ++s) {
-      mbar_init(&cfull[s], kW4Conv);
+      mbar_init(&cfull[s], kW4Conv / 2);  // the converter group of the sub-stage's parity
       mbar_init(&cempty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
@@ -230,15 +249,16 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
     }
   } else if (warp >= 2 && warp < 2 + kW4Conv) {
     // ---------------------------------------------------------------- converters
-    const int j = (warp - 2) >> 2;  // the block this warp expands
-    const int quarter = warp & 3;   // the TMEM lanes this warp may write
+    const int grp = (warp - 2) >> 3;      // the sub-blocks of this parity (MMA issuer grp's)
+    const int j = ((warp - 2) >> 2) & 1;  // the block this warp expands
+    const int quarter = warp & 3;         // the TMEM lanes this warp may write
     const int row = quarter * 32 + lane;
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + j * kW4ACols;
-    uint32_t ps = 0, pph = 0, cs = 0, cph = 0;
+    uint32_t ps = 0, pph = 0, m = 0;
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       for (int kb = 0; kb < nkb && ok; ++kb) {
-        const int nsub = min(4, nsub_all - kb * 4);
+        const int nsub = min(4, nsub_all - kb * 4);  // 2 or 4
         int w_ok = 1;
         if (lane == 0) w_ok = mbar_wait(&pfull[ps], pph, abort_flag, p.err) ? 1 : 0;
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
@@ -246,69 +266,66 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
           ok = false;
           break;
         }
-        // this row's 128 code bytes (128-byte swizzle: chunk c sits at c ^ (row % 8)) and scales
+        // this warp's sub-blocks b = grp, grp + 2 of the stage: codes (128-byte swizzled row, 16-byte
+        // chunk c at c ^ (row % 8)) and scales, read before any tcgen05 operation of the stage
         const uint8_t* src = pring + ps * S::PSTAGE;
         const uint8_t* qrow = src + S::P_PACK + j * kW4PackBlock + row * 128;
         const __nv_bfloat16* srow =
             reinterpret_cast<const __nv_bfloat16*>(src + S::P_SCALE + j * kW4ScaleBlock) + row;
-        uint4 q[8];
-        __nv_bfloat162 sc[8];
+        uint4 q[4];
+        __nv_bfloat16 sc[4];
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          q[c] = *reinterpret_cast<const uint4*>(qrow + ((c ^ (row & 7)) << 4));
-          sc[c] = __bfloat162bfloat162(srow[c * 128]);
+        for (int h = 0; h < 2; ++h) {
+          const int b = grp + 2 * h;
+          if (b < nsub) {
+            q[2 * h] = *reinterpret_cast<const uint4*>(qrow + (((2 * b) ^ (row & 7)) << 4));
+            q[2 * h + 1] = *reinterpret_cast<const uint4*>(qrow + (((2 * b + 1) ^ (row & 7)) << 4));
+            sc[2 * h] = srow[(2 * b) * 128];
+            sc[2 * h + 1] = srow[(2 * b + 1) * 128];
+          }
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&pempty[ps]);  // the stage's codes and scales are in registers
+        if (lane == 0) mbar_arrive(&pempty[ps]);
+#pragma unroll
+        for (int h = 0; h < 2; ++h, ++m) {
+          const int b = grp + 2 * h;
+          if (b >= nsub) break;
+          const uint32_t cs = grp + 2 * (m % (S::CSTAGES / 2));
+          const uint32_t cph = (m / (S::CSTAGES / 2)) & 1u;
+          if (lane == 0) w_ok = mbar_wait(&cempty[cs], cph ^ 1u, abort_flag, p.err) ? 1 : 0;
+          w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
+          if (!w_ok) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          uint32_t a[32];
+          w4_expand_sub(q[2 * h], q[2 * h + 1], sc[2 * h], sc[2 * h + 1], a);
+          tmem_st32(t_lane + S::A_COL0 + cs * S::CSTAGE_COLS, a);
+          tmem_st_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&cfull[cs]);
+        }
         if (++ps == S::PSTAGES) {
           ps = 0;
           pph ^= 1u;
-        }
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-          if (b < nsub) {
-            if (lane == 0) w_ok = mbar_wait(&cempty[cs], cph ^ 1u, abort_flag, p.err) ? 1 : 0;
-            w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
-            if (!w_ok) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
-            uint32_t a[32];
-            w4_expand_word(q[2 * b].x, sc[2 * b], a + 0);
-            w4_expand_word(q[2 * b].y, sc[2 * b], a + 4);
-            w4_expand_word(q[2 * b].z, sc[2 * b], a + 8);
-            w4_expand_word(q[2 * b].w, sc[2 * b], a + 12);
-            w4_expand_word(q[2 * b + 1].x, sc[2 * b + 1], a + 16);
-            w4_expand_word(q[2 * b + 1].y, sc[2 * b + 1], a + 20);
-            w4_expand_word(q[2 * b + 1].z, sc[2 * b + 1], a + 24);
-            w4_expand_word(q[2 * b + 1].w, sc[2 * b + 1], a + 28);
-            tmem_st32(t_lane + S::A_COL0 + cs * S::CSTAGE_COLS, a);
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&cfull[cs]);
-            if (++cs == S::CSTAGES) {
-              cs = 0;
-              cph ^= 1u;
-            }
-          }
         }
       }
     }
   } else if (warp == 1 || warp == kW4Mma1Warp) {
     if (lane == 0) {  // ------------------------------------------------ MMA issuers
       const int me = warp == 1 ? 0 : 1;
-      uint32_t ps = 0, pph = 0, m = 0, acc = 0, acc_phase = 0;
+      uint32_t ps = 0, pph = 0, m = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
                                         p.dense_rows, p.dense_act_row0, kW4BN);
         const int n = ti.valid >= kW4BN ? kW4BN : ((ti.valid + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32_n(n);
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err)) break;
+        if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
-        const uint32_t d0 = tmem_base + acc * S::ACC_COLS + me * 2 * kW4BN;
+        const uint32_t d0 = tmem_base + me * 2 * kW4BN;
         uint32_t accum = 0;
         for (int kb = 0; kb < nkb && ok; ++kb) {
           const int nsub = min(4, nsub_all - kb * 4);  // 2 or 4: every stage has work for both
@@ -343,9 +360,8 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
           }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);
-        acc ^= 1u;
-        if (acc == 0) acc_phase ^= 1u;
+        mma_commit(tfull);
+        acc_phase ^= 1u;
       }
       mma_commit(&drain[me]);
       mbar_wait(&drain[me], 0, nullptr, nullptr, kDrainLimitNs);
@@ -354,48 +370,67 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
     // ---------------------------------------------------------------- epilogue (4 warps)
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
-    uint32_t acc = 0, acc_phase = 0;
+    uint32_t acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
                                       p.dense_rows, p.dense_act_row0, kW4BN);
       int w_ok = 1;
-      if (lane == 0) w_ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err) ? 1 : 0;
+      if (lane == 0) w_ok = mbar_wait(tfull, acc_phase, abort_flag, p.err) ? 1 : 0;
       w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
       if (!w_ok) break;
       tc_fence_after();
-      const uint32_t tb = tmem_base + acc * S::ACC_COLS + ((uint32_t)(quarter * 32) << 16);
+      const uint32_t tb = tmem_base + ((uint32_t)(quarter * 32) << 16);
+      // y_b = issuer 0's half + issuer 1's half of block b, tokens 0..31 of the tile.  SwiGLU keeps
+      // h = SiLU(y_0) * y_1 as bf16 pairs and stores after freeing the accumulator; the plain store
+      // writes each 8-token chunk as soon as it is read.
       const int64_t out_row0 = (ti.dense ? (int64_t)p.dense_out_row0 : (int64_t)ti.grp_row0) +
                                (int64_t)ti.rt * kW4BN;
       const int64_t feat = (int64_t)ti.ft * rows_per_tile + r;
-#pragma unroll 1
-      for (int c = 0; c < kW4BN && c < ti.valid; c += 16) {
-        uint32_t v0[16], v1[16], w0[16], w1[16];  // [issuer 0 | 1] x [block 0 | 1]
-        tmem_ld16(tb + c, v0);
-        tmem_ld16(tb + kW4BN + c, v1);
-        tmem_ld16(tb + 2 * kW4BN + c, w0);
-        tmem_ld16(tb + 3 * kW4BN + c, w1);
-        tmem_ld_wait();
+      uint32_t hpair[kSwiGLU ? kW4BN / 2 : 1];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          if (c + i < ti.valid) {
-            const int64_t orow = out_row0 + c + i;
-            const float y0 = __uint_as_float(v0[i]) + __uint_as_float(w0[i]);
-            const float y1 = __uint_as_float(v1[i]) + __uint_as_float(w1[i]);
+      for (int c = 0; c < kW4BN; c += 8) {
+        if (c < ti.valid) {
+          uint32_t g0[8], g1[8], u0[8], u1[8];
+          tmem_ld8(tb + c, g0);
+          tmem_ld8(tb + 2 * kW4BN + c, g1);
+          tmem_ld8(tb + kW4BN + c, u0);
+          tmem_ld8(tb + 3 * kW4BN + c, u1);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 8; i += 2) {
+            const float ga = __uint_as_float(g0[i]) + __uint_as_float(g1[i]);
+            const float gb = __uint_as_float(g0[i + 1]) + __uint_as_float(g1[i + 1]);
+            const float ua = __uint_as_float(u0[i]) + __uint_as_float(u1[i]);
+            const float ub = __uint_as_float(u0[i + 1]) + __uint_as_float(u1[i + 1]);
             if (kSwiGLU) {
-              ((__nv_bfloat16*)p.out)[orow * p.ldo + feat] =
-                  __float2bfloat16_rn(silu_fast(y0) * y1);
+              hpair[kSwiGLU ? (c + i) / 2 : 0] = pack_bf16x2(silu_fast(ga) * ua, silu_fast(gb) * ub);
             } else {
-              float* o = (float*)p.out + orow * p.ldo + feat;
-              o[0] = y0;
-              o[128] = y1;
+              if (c + i < ti.valid) {
+                float* o = (float*)p.out + (out_row0 + c + i) * p.ldo + feat;
+                o[0] = ga;
+                o[128] = ua;
+              }
+              if (c + i + 1 < ti.valid) {
+                float* o = (float*)p.out + (out_row0 + c + i + 1) * p.ldo + feat;
+                o[0] = gb;
+                o[128] = ub;
+              }
             }
           }
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
-      acc ^= 1u;
-      if (acc == 0) acc_phase ^= 1u;
+      mbar_arrive(tempty);  // the accumulator is free for the next tile
+      acc_phase ^= 1u;
+      if (kSwiGLU) {
+        __nv_bfloat16* o = (__nv_bfloat16*)p.out + out_row0 * p.ldo + feat;
+#pragma unroll
+        for (int i = 0; i < kW4BN; ++i)
+          if (i < ti.valid) {
+            const uint32_t v = hpair[kSwiGLU ? i / 2 : 0] >> (16 * (i & 1));
+            o[(int64_t)i * p.ldo] = __ushort_as_bfloat16((unsigned short)(v & 0xFFFFu));
+          }
+      }
     }
   }
 
