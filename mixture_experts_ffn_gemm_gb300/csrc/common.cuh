@@ -86,6 +86,38 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// The same test, but a thread whose phase is not complete yet is suspended in hardware until the
+// phase completes or about `suspend_ns` pass, instead of returning at once.
+__device__ __forceinline__ bool mbar_test_sleep(uint64_t* bar, uint32_t parity, uint32_t suspend_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(suspend_ns)
+      : "memory");
+  return ok != 0;
+}
+
+// mbar_wait for kernels whose waiting warps share the SM's issue slots with busy arithmetic warps:
+// each poll suspends the thread (up to 0.5 us) rather than spinning on the abort flag and the
+// timer.  Same bounds and error behaviour as mbar_wait.
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                                uint32_t* err, uint64_t limit_ns = kWaitLimitNs) {
+  if (mbar_test(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_test_sleep(bar, parity, 500u)) return true;
+    if (abort && *abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      if (abort) *abort = 1;
+      raise_flag(err, kErrTimeout);
+      return false;
+    }
+  }
+}
+
 // ---------------------------------------------------------------------------------------------
 // TMA (cp.async.bulk.tensor), 2D tiles into shared memory, completion counted on an mbarrier.
 // x is the innermost (contiguous) coordinate in elements, y the row.

@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
         const int w_y = (ti.dense ? 0 : ti.g * p.w_group_rows) + w_local;
         const int s_y = ti.dense ? 0 : ti.g * (p.K / 32);  // the group's first scale row
         for (int kb = 0; kb < nkb; ++kb) {
-          if (!mbar_wait(&pempty[stage], phase ^ 1u, abort_flag, p.err)) {
+          if (!mbar_wait_sleep(&pempty[stage], phase ^ 1u, abort_flag, p.err)) {
             ok = false;
             break;
           }
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
             phase ^= 1u;
           }
           --stage;
-          mbar_wait(&pfull[stage], phase, nullptr, nullptr, kDrainLimitNs);
+          mbar_wait_sleep(&pfull[stage], phase, nullptr, nullptr, kDrainLimitNs);
         }
       }
     }
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
       for (int kb = 0; kb < nkb && ok; ++kb) {
         const int nsub = min(4, nsub_all - kb * 4);  // 2 or 4
         int w_ok = 1;
-        if (lane == 0) w_ok = mbar_wait(&pfull[ps], pph, abort_flag, p.err) ? 1 : 0;
+        if (lane == 0) w_ok = mbar_wait_sleep(&pfull[ps], pph, abort_flag, p.err) ? 1 : 0;
         w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
         if (!w_ok) {
           ok = false;
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
           if (b >= nsub) break;
           const uint32_t cs = grp + 2 * (m % (S::CSTAGES / 2));
           const uint32_t cph = (m / (S::CSTAGES / 2)) & 1u;
-          if (lane == 0) w_ok = mbar_wait(&cempty[cs], cph ^ 1u, abort_flag, p.err) ? 1 : 0;
+          if (lane == 0) w_ok = mbar_wait_sleep(&cempty[cs], cph ^ 1u, abort_flag, p.err) ? 1 : 0;
           w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
           if (!w_ok) {
             ok = false;
@@ -323,13 +323,13 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
                                         p.dense_rows, p.dense_act_row0, kW4BN);
         const int n = ti.valid >= kW4BN ? kW4BN : ((ti.valid + 15) & ~15);
         const uint32_t idesc = idesc_bf16_f32_n(n);
-        if (!mbar_wait(tempty, acc_phase ^ 1u, abort_flag, p.err)) break;
+        if (!mbar_wait_sleep(tempty, acc_phase ^ 1u, abort_flag, p.err)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + me * 2 * kW4BN;
         uint32_t accum = 0;
         for (int kb = 0; kb < nkb && ok; ++kb) {
           const int nsub = min(4, nsub_all - kb * 4);  // 2 or 4: every stage has work for both
-          if (!mbar_wait(&pfull[ps], pph, abort_flag, p.err)) {  // the stage's tokens
+          if (!mbar_wait_sleep(&pfull[ps], pph, abort_flag, p.err)) {  // the stage's tokens
             ok = false;
             break;
           }
@@ -337,7 +337,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
           for (int b = me; b < nsub; b += 2, ++m) {
             const uint32_t cs = me + 2 * (m % (S::CSTAGES / 2));
             const uint32_t cph = (m / (S::CSTAGES / 2)) & 1u;
-            if (!mbar_wait(&cfull[cs], cph, abort_flag, p.err)) {
+            if (!mbar_wait_sleep(&cfull[cs], cph, abort_flag, p.err)) {
               ok = false;
               break;
             }
@@ -364,7 +364,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
         acc_phase ^= 1u;
       }
       mma_commit(&drain[me]);
-      mbar_wait(&drain[me], 0, nullptr, nullptr, kDrainLimitNs);
+      mbar_wait_sleep(&drain[me], 0, nullptr, nullptr, kDrainLimitNs);
     }
   } else {
     // ---------------------------------------------------------------- epilogue (4 warps)
@@ -375,7 +375,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
       const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
                                       p.dense_rows, p.dense_act_row0, kW4BN);
       int w_ok = 1;
-      if (lane == 0) w_ok = mbar_wait(tfull, acc_phase, abort_flag, p.err) ? 1 : 0;
+      if (lane == 0) w_ok = mbar_wait_sleep(tfull, acc_phase, abort_flag, p.err) ? 1 : 0;
       w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
       if (!w_ok) break;
       tc_fence_after();
