@@ -46,6 +46,8 @@ MEASURED_TRAFFIC_RATIO = {
     "gemm13_swiglu_fp8": (1.018, "profiles/gemm_fp8_E64_T4096.md",
                           "a 64-expert, 4096-token fp8 capture"),
     "gemm2_fp8": (0.977, "profiles/gemm_fp8_E64_T4096.md", "a 64-expert, 4096-token fp8 capture"),
+    "gemm13_swiglu_w4": (1.010, "profiles/gemm_w4_decode_E32.md", "a 32-expert INT4 decode capture"),
+    "gemm2_w4": (0.966, "profiles/gemm_w4_decode_E32.md", "a 32-expert INT4 decode capture"),
 }
 DENSE_METRIC = "Dense block-0 MLP tokens/s (d=7168, I=18432) and % of roofline (HBM or TC)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
