@@ -105,6 +105,25 @@ def test_stage_entry_points_validate(moelib):
     assert moelib.moe_reset_device_status(None, 0, None) == B.MOE_ERR_WORKSPACE
 
 
+def test_int4_host_validation(moelib):
+    """4-bit group experts (MOE_INT4): bf16 activations, groups of 32, the K2 path, d % 256 and
+    I % 128; anything else is refused before a launch, and the scales are required."""
+    int4 = dict(w_dtype=B.torch.uint8, quant_block=32)
+    assert B.moe_workspace_size(_cfg(**int4)) > 0
+    for bad in (dict(quant_block=128), dict(act_dtype=B.torch.float32),
+                dict(d_latent=3584, latent_norm=1), dict(d=7040), dict(I=2000)):
+        assert B.moe_workspace_size(_cfg(**{**int4, **bad})) == 0, bad
+    cfg = _cfg(**int4)
+    need = B.moe_workspace_size(cfg)
+    p = 0x10000  # aligned stand-in address: validation fails before anything dereferences it
+    names = ["x", "W_r", "b", "W13", "W2", "W13_s", "W2_s", "Ws13", "Ws2", "Ws13_s", "Ws2_s",
+             "W_down", "W_up", "out"]
+    for missing in ("W13_s", "W2_s", "Ws13_s", "Ws2_s"):
+        ptrs = [None if n == missing or n in ("W_down", "W_up") else p for n in names]
+        assert moelib.moe_forward(ctypes.byref(cfg), *ptrs, p, need, None) == \
+            B.MOE_ERR_INVALID_ARG, missing
+
+
 def test_dense_mlp_host_validation(moelib):
     p = 0x10000  # aligned stand-in address: every call below fails (or returns) before using it
     bf, f32 = B.MOE_BF16, B.MOE_F32

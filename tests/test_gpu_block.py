@@ -65,6 +65,12 @@ def test_block_fp8_small(cuda_device):
     _check(w, seed=4)
 
 
+def test_block_int4_small(cuda_device):
+    w = replace(S.WORKLOADS["tiny_fp32"], name="small_int4", act="bf16", int4=True, quant_block=32,
+                T=200, w_init="std0.02", bias_range=0.05)
+    _check(w, seed=5)
+
+
 def test_block_k2_decode_widths(cuda_device):
     """The K2 decode workload's shapes (128 tokens, d = 7168, 384 experts), every token."""
     _check(S.WORKLOADS["k2_decode_bf16"], seed=0)

@@ -211,6 +211,24 @@ def test_int4_ragged_tokens(cuda_device, T):
     _full_check(_layer(SMALL_INT4.with_tokens(T), seed=32 + T))
 
 
+def test_int4_zero_tokens_is_a_no_op(cuda_device):
+    w = SMALL_INT4.with_tokens(0)
+    layer = _layer(w)
+    cfg = B.config_for(w)
+    ws = B.alloc_workspace(cfg)
+    out = torch.empty(0, w.d, dtype=torch.bfloat16, device="cuda")
+    B.moe_forward(cfg, layer.x, *B.layer_weights(layer), out, ws)
+    torch.cuda.synchronize()
+    assert B.moe_device_status(ws) == B.MOE_OK
+
+
+def test_int4_every_expert_skewed(cuda_device):
+    """Clustered tokens: a few experts get several token tiles (their weights are expanded once
+    per tile), most get one or none."""
+    w = replace(SMALL_INT4, name="int4_clusters", T=600, x_dist="clusters16")
+    _full_check(_layer(w, seed=34))
+
+
 def test_int4_k2_widths_32_experts(cuda_device):
     w = replace(S.WORKLOADS["k2_int4_decode"], name="k2_int4_e32", E=32, T=72)
     _full_check(_layer(w, seed=33))
