@@ -33,7 +33,7 @@ NTHREADS = os.cpu_count() or 4
 
 
 @dataclass
-class GpuRun:
+class GpuResult:
     logits: torch.Tensor
     idx: torch.Tensor
     weight: torch.Tensor
@@ -48,7 +48,7 @@ class GpuRun:
     status_fwd: int
 
 
-def run_gpu(layer, flags: int = 0) -> GpuRun:
+def run_gpu(layer, flags: int = 0) -> GpuResult:
     w = layer.w
     cfg = B.config_for(w, T=layer.x.shape[0], flags=flags)
     T, E, k, d, de = layer.x.shape[0], w.E, w.k, w.d, w.d_expert
@@ -75,11 +75,11 @@ def run_gpu(layer, flags: int = 0) -> GpuRun:
     out_fwd = torch.full((T, d), float("nan"), dtype=act, device=dev)
     B.moe_forward(cfg, layer.x, *B.layer_weights(layer), out_fwd, ws)
     status_fwd = B.moe_device_status(ws)
-    return GpuRun(logits, idx, wgt, counts, offsets, perm_src, perm_dst, y_perm, out, out_fwd,
+    return GpuResult(logits, idx, wgt, counts, offsets, perm_src, perm_dst, y_perm, out, out_fwd,
                   status, status_fwd)
 
 
-def check_routing(layer, g: GpuRun) -> dict:
+def check_routing(layer, g: GpuResult) -> dict:
     """Bit-exact indices (near ties excepted) and gates against the oracle's rule on the GPU's
     logits.  Returns counts for reporting."""
     cfg = OB.config(layer, layer.x.shape[0])
@@ -98,7 +98,7 @@ def check_routing(layer, g: GpuRun) -> dict:
     return {"near_ties": int(near.sum()), "tokens": int(len(near))}
 
 
-def check_permutation(layer, g: GpuRun):
+def check_permutation(layer, g: GpuResult):
     """counts / offsets / permutation bit-exact against a stable sort of the expert ids."""
     T, E, k = layer.x.shape[0], layer.w.E, layer.w.k
     idx = g.idx.cpu().numpy().reshape(-1)
@@ -142,7 +142,7 @@ def compare(got: np.ndarray, ref: np.ndarray, act: str, tol=None,
     return {"err": e_max, "rms_err": e_rms}
 
 
-def check_outputs(layer, g: GpuRun, rows=None, tol=None, output_rounding=False) -> dict:
+def check_outputs(layer, g: GpuResult, rows=None, tol=None, output_rounding=False) -> dict:
     """Layer outputs (and the shared expert rows of y_perm) against the oracle on `rows`
     (all rows by default), near-tie tokens excluded and counted."""
     T = layer.x.shape[0]
@@ -164,7 +164,7 @@ def check_outputs(layer, g: GpuRun, rows=None, tol=None, output_rounding=False) 
     return res
 
 
-def check_expert_rows(layer, g: GpuRun, nrows: int = 6, seed: int = 0, tol=None):
+def check_expert_rows(layer, g: GpuResult, nrows: int = 6, seed: int = 0, tol=None):
     """Sampled permuted rows of y_perm against one oracle SwiGLU of that row's token and expert
     (K2 path): isolates the grouped GEMMs from the combine."""
     w = layer.w
