@@ -293,6 +293,22 @@ __device__ __forceinline__ void named_barrier(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Named barrier that also ANDs one predicate over the `count` threads: every participant gets 1
+// only if all passed a nonzero `pred`.  Lets a group of warps take the same branch after waits
+// whose outcome may differ per warp.
+__device__ __forceinline__ int named_barrier_and(int id, int count, int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.s32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.s32 %0, 1, 0, q;\n\t}\n"
+      : "=r"(r)
+      : "r"(pred), "r"(id), "r"(count)
+      : "memory");
+  return r;
+}
+
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }

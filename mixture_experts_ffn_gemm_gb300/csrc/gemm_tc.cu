@@ -64,12 +64,15 @@ struct TcParams {
 template <bool kSwap, int kBN, int kEpi>
 struct TcShape {
   static constexpr bool kSwiGLU = kEpi == EPI_SWIGLU;
+  // 256-token swap-AB SwiGLU tiles stack 64 W1 rows over the matching 64 W3 rows in one M = 128
+  // operand, so that one 256-column accumulator holds both and two of them fit in TMEM
+  static constexpr bool kStack = kSwap && kSwiGLU && kBN == 256;
   static constexpr int RPT = kSwap ? kBN : 128;                         // token rows per tile
-  static constexpr int FPT = kSwap ? 128 : (kSwiGLU ? kBN / 2 : kBN);  // features per tile
-  static constexpr int OPA = (kSwap && kSwiGLU) ? 2 * kBoxBytes : kBoxBytes;  // A bytes / stage
+  static constexpr int FPT = kSwap ? (kStack ? 64 : 128) : (kSwiGLU ? kBN / 2 : kBN);  // features
+  static constexpr int OPA = (kSwap && kSwiGLU && !kStack) ? 2 * kBoxBytes : kBoxBytes;  // A / stage
   static constexpr int OPB = kBN * 128;                                       // B bytes / stage
   static constexpr int STAGE = OPA + OPB;
-  static constexpr int ACC_COLS = (kSwap && kSwiGLU) ? 2 * kBN : kBN;  // fp32 columns per tile
+  static constexpr int ACC_COLS = (kSwap && kSwiGLU && !kStack) ? 2 * kBN : kBN;  // fp32 columns
   // two accumulators (the epilogue of tile i overlaps the mainloop of tile i+1) when they fit
   static constexpr int NACC = 2 * ACC_COLS <= 512 ? 2 : 1;
   static constexpr int TMEM_NEED = NACC * ACC_COLS;
@@ -84,10 +87,12 @@ struct TcShape {
   // the global stores are whole rows (4 KB per epilogue warp)
   static constexpr bool kStaged = !kSwap && kEpi != EPI_STORE_ADD;
   static constexpr int STAGING = kStaged ? 4 * 4096 : 0;
+  // stacked tiles: g and u of 64 features x 16 tokens meet here (rows padded to 17 words)
+  static constexpr int XCH = kStack ? 2 * 64 * 17 * 4 : 0;
   static constexpr int STAGES_FIT =
-      (kSmemLimit - 1024 - TABLE_BYTES - BAR_BYTES - STAGING) / STAGE;
+      (kSmemLimit - 1024 - TABLE_BYTES - BAR_BYTES - STAGING - XCH) / STAGE;
   static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-  static constexpr int SMEM = 1024 + STAGES * STAGE + BAR_BYTES + TABLE_BYTES + STAGING;
+  static constexpr int SMEM = 1024 + STAGES * STAGE + BAR_BYTES + TABLE_BYTES + STAGING + XCH;
   static_assert(STAGES >= 2, "not enough shared memory for two stages");
   static_assert(TMEM_NEED <= 512, "accumulators exceed TMEM");
   static_assert(STAGE % 1024 == 0, "stages must keep 1024-byte alignment for SWIZZLE_128B");
@@ -207,8 +212,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
                 tma_load_2d(sb + j * kBoxBytes, mw, &full[stage], kx, w_y + j * 128);
             }
           } else {
+            // stacked tiles: the weight map's box is 64 rows, W3 lands in operand rows 64..127
             tma_load_2d(sa, mw, &full[stage], kx, w_y);
-            if (S::kSwiGLU) tma_load_2d(sa + kBoxBytes, mw, &full[stage], kx, w_y + u_off);
+            if (S::kSwiGLU)
+              tma_load_2d(sa + (S::kStack ? kBoxBytes / 2 : kBoxBytes), mw, &full[stage], kx,
+                          w_y + u_off);
             tma_load_2d(sb, ma, &full[stage], ax, act_y);
           }
           if (armed < S::STAGES) ++armed;
@@ -270,7 +278,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
               continue;
             }
             mma_bf16(d0, sw128_kmajor_desc(sa + k16 * 32), bdesc, idesc, accum);
-            if (kSwap && S::kSwiGLU)
+            if (kSwap && S::kSwiGLU && !S::kStack)
               mma_bf16(d0 + kBN, sw128_kmajor_desc(sa + kBoxBytes + k16 * 32), bdesc, idesc,
                        accum);
           }
@@ -300,6 +308,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err, p.wait_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
+      // stacked tiles meet at a named barrier below: all four warps leave together or none does
+      if (S::kStack) ok = named_barrier_and(1, 128, ok);
       if (!ok) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + acc * S::ACC_COLS + ((uint32_t)(quarter * 32) << 16);
@@ -412,6 +422,33 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
             d4[0] = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             d4[1] = make_uint4(pk[4], pk[5], pk[6], pk[7]);
           }
+        }
+      } else if constexpr (S::kStack) {
+        // stacked SwiGLU: lanes 0..63 hold g = x W1 and lanes 64..127 u = x W3 of features
+        // ft * 64 + (lane % 64); the pair meets in shared memory, 16 tokens at a time
+        float* xch = reinterpret_cast<float*>(staging);
+        const int t = threadIdx.x - 64;          // epilogue thread 0..127
+        const int cf = t & 63, th = t >> 6;      // the feature and token half it computes
+        float* mine = xch + r * 17;               // row r: (r >> 6 ? u : g) of feature r % 64
+        const int64_t feat = (int64_t)ti.ft * 64 + cf;
+#pragma unroll 1
+        for (int c = 0; c < kBN && c < ti.valid; c += 16) {
+          uint32_t v[16];
+          tmem_ld16(tb + c, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) mine[i] = __uint_as_float(v[i]);
+          named_barrier(1, 128);
+          const float* gr = xch + cf * 17 + th * 8;
+          const float* ur = xch + (64 + cf) * 17 + th * 8;
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int tok = c + th * 8 + i;
+            if (tok < ti.valid)
+              ((__nv_bfloat16*)out)[(out_row0 + tok) * ldo + feat] =
+                  __float2bfloat16_rn(silu_fast(gr[i]) * ur[i]);
+          }
+          named_barrier(1, 128);  // the buffer is read before the next chunk overwrites it
         }
       } else {
         // swap: TMEM lane = output feature, columns = tokens of this tile
@@ -538,17 +575,18 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
   if (g.n128 && g.epi == EPI_STORE && (g.F % 128 || (g.F_d && g.F_d % 128)))
     return cudaErrorInvalidValue;
   const int act_box = swap == 2 ? 256 : swap ? 32 : 128;
+  const int w_box = swap == 2 && g.epi == EPI_SWIGLU ? 64 : 128;  // stacked W1 / W3 halves
   const int kw = g.k_wrap > 0 ? g.k_wrap : g.K;
   if (g.n_routed > 0) {
     if (!make_map_bf16(&p.map_act, g.act, g.act_rows, kw, act_box)) return cudaErrorInvalidValue;
-    if (!make_map_bf16(&p.map_w, g.w, g.w_rows, g.K, 128)) return cudaErrorInvalidValue;
+    if (!make_map_bf16(&p.map_w, g.w, g.w_rows, g.K, w_box)) return cudaErrorInvalidValue;
   }
   const int K_d = g.K_d > 0 ? g.K_d : g.K;
   const int kw_d = g.k_wrap_d > 0 ? g.k_wrap_d : (g.K_d > 0 ? g.K_d : kw);
   if (g.dense_rows > 0) {
     if (!make_map_bf16(&p.map_act_d, g.act_d, g.act_d_rows, kw_d, act_box))
       return cudaErrorInvalidValue;
-    if (!make_map_bf16(&p.map_w_d, g.w_d, g.w_d_rows, K_d, 128)) return cudaErrorInvalidValue;
+    if (!make_map_bf16(&p.map_w_d, g.w_d, g.w_d_rows, K_d, w_box)) return cudaErrorInvalidValue;
   }
   if (g.n_routed == 0) {  // keep the unused maps valid objects
     p.map_act = p.map_act_d;
