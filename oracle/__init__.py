@@ -83,7 +83,7 @@ def _load():
             lib.orc_route.restype = ctypes.c_int
             lib.orc_route.argtypes = [ctypes.POINTER(_Cfg), _Tensor, P, P, P, P, P, P]
             lib.orc_route_from_logits.restype = ctypes.c_int
-            lib.orc_route_from_logits.argtypes = [ctypes.POINTER(_Cfg), P, P, P, P, P]
+            lib.orc_route_from_logits.argtypes = [ctypes.POINTER(_Cfg), P, P, P, P, P, P]
             lib.orc_param_count.restype = ctypes.c_int64
             lib.orc_param_count.argtypes = [ctypes.POINTER(_Cfg)]
             lib.orc_param_breakdown.restype = None
@@ -213,9 +213,10 @@ def route(cfg: Config, x: Mat, W_r: np.ndarray, b: np.ndarray) -> dict:
     return res
 
 
-def route_from_logits(cfg: Config, z: np.ndarray, b: np.ndarray):
+def route_from_logits(cfg: Config, z: np.ndarray, b: np.ndarray, with_keys: bool = False):
     """Selection and gates from given fp32 logits [T, E]; the key is fp32(fp32(sigmoid(z)) + b).
-    Returns (idx [T,k] int32, gates [T,k] f64, margin [T] f64)."""
+    Returns (idx [T,k] int32, gates [T,k] f64, margin [T] f64), and with ``with_keys`` also the
+    selected experts' fp32 keys [T,k] in slot order."""
     lib = _load()
     z = np.ascontiguousarray(z, dtype=np.float32)
     b = np.ascontiguousarray(b, dtype=np.float32)
@@ -224,11 +225,12 @@ def route_from_logits(cfg: Config, z: np.ndarray, b: np.ndarray):
     idx = np.zeros((T, cfg.k), np.int32)
     gates = np.zeros((T, cfg.k), np.float64)
     margin = np.zeros((T,), np.float64)
+    keys = np.zeros((T, cfg.k), np.float32)
     st = lib.orc_route_from_logits(ctypes.byref(c), _ptr(z), _ptr(b), _ptr(idx), _ptr(gates),
-                                   _ptr(margin))
+                                   _ptr(margin), _ptr(keys))
     if st != 0:
         raise RuntimeError(f"orc_route_from_logits failed with status {st}")
-    return idx, gates, margin
+    return (idx, gates, margin, keys) if with_keys else (idx, gates, margin)
 
 
 def param_count(cfg: Config) -> int:

@@ -249,7 +249,7 @@ static void gates_from_scores(const double* s, const int32_t* idx, int k, double
 }
 
 int orc_route_from_logits(const orc_config* c, const float* z, const float* b, int32_t* idx,
-                          double* gates, double* margin) {
+                          double* gates, double* margin, float* sel_keys) {
   if (!c || !z || !b || !idx || c->k < 1 || c->k > c->E) return ORC_EINVAL;
   double* s = (double*)malloc(sizeof(double) * c->E);
   float* key = (float*)malloc(sizeof(float) * c->E);
@@ -270,6 +270,8 @@ int orc_route_from_logits(const orc_config* c, const float* z, const float* b, i
     gates_from_scores(s, idx + t * c->k, c->k, c->gate_scale, g);
     if (gates)
       for (int j = 0; j < c->k; ++j) gates[t * c->k + j] = g[j];
+    if (sel_keys)
+      for (int j = 0; j < c->k; ++j) sel_keys[t * c->k + j] = key[idx[t * c->k + j]];
   }
   free(s);
   free(key);

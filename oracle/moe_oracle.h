@@ -89,9 +89,10 @@ int orc_route(const orc_config* cfg, orc_tensor x, const float* W_r, const float
 
 /* Routing from given fp32 logits z [T][E] (the selection rule fed another implementation's logits).
  * Key = fp32( fp32(sigma(z)) + b ), sigma evaluated in fp64 and rounded to fp32.  Gates in fp64 from
- * the unbiased sigma(z).  idx [T][k], gates [T][k], margin [T] (in the fp32 key). */
+ * the unbiased sigma(z).  idx [T][k], gates [T][k], margin [T] (in the fp32 key); sel_keys [T][k]
+ * (may be NULL) receives the keys of the selected experts in slot order. */
 int orc_route_from_logits(const orc_config* cfg, const float* z, const float* b, int32_t* idx,
-                          double* gates, double* margin);
+                          double* gates, double* margin, float* sel_keys);
 
 /* Number of learned parameters of one MoE layer, from the shapes the forward indexes. */
 int64_t orc_param_count(const orc_config* cfg);

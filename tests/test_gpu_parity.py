@@ -262,6 +262,18 @@ def test_full_k2_prefill(cuda_device):
     print("k2_prefill", res)
 
 
+def test_k2_prefill_65536_tokens_offsets_past_2_31(cuda_device):
+    """65536 tokens at the K2 widths: the permuted activations (524288 rows x 7168) and the fp32
+    expert outputs hold more than 2^31 elements, so every row * width product must be 64-bit.
+    About 62 GB on the device; 8 sampled tokens against the oracle."""
+    w = S.WORKLOADS["k2_prefill_bf16"].with_tokens(65536)
+    layer = _layer(w, seed=11)
+    res = _full_check(layer, 0, rows=_sample(w.T, n=8, seed=5), expert_rows=4)
+    del layer
+    torch.cuda.empty_cache()
+    print("k2_prefill_65536", res)
+
+
 def test_full_k3_latent(cuda_device):
     res = _full_workload("k3_latent_bf16")
     print("k3_latent", res)

@@ -162,6 +162,13 @@ def test_topk_matches_brute_force_enumeration(orc, ties):
         # slots in order: each slot ordered before the next
         for a, c in zip(idx[t][:-1], idx[t][1:]):
             assert _before(key[t, a], a, key[t, c], c)
+    # the selected keys it reports are those experts' keys, in slot order, and the margin is the
+    # last selected key minus the best key left out
+    _, _, margin2, sel = orc.route_from_logits(cfg, z, b, with_keys=True)
+    np.testing.assert_array_equal(sel, np.take_along_axis(key, idx.astype(np.int64), 1))
+    for t in range(T):
+        rest = np.delete(key[t], idx[t])
+        assert margin2[t] == np.float64(sel[t, -1]) - np.float64(rest.max())
 
 
 def test_all_equal_scores_pick_lowest_indices(orc):
