@@ -74,24 +74,35 @@ __global__ void __launch_bounds__(kSimtThreads) moe_gemm_simt_kernel(const SimtP
 #pragma unroll
       for (int j = 0; j < 4; ++j) accg[i][j] = accu[i][j] = 0.0f;
 
-    for (int k0 = k_begin; k0 < k_begin + klen; k0 += kSimtK) {
-      // each thread stages 4 consecutive k of one row of A and of W (and W3)
-      const int lr = threadIdx.x / 4;
-      const int lk = (threadIdx.x % 4) * 4;
+    // each thread stages 4 consecutive k of one row of A and of W (and W3); the next K-step's
+    // values are loaded into registers while the current one is multiplied out of shared memory
+    const int lr = threadIdx.x / 4;
+    const int lk = (threadIdx.x % 4) * 4;
+    const bool a_ok = lr < ti.valid, w_ok = f0 + lr < p.F;
+    const bool wrap = p.k_wrap != p.K;
+    const TA* a_row = A + (a_row0 + lr) * p.k_wrap;
+    const TW* wg_row = W + (w_row0 + lr) * p.K;
+    const TW* wu_row = W + (w_row0 + uoff + lr) * p.K;
+    float ra[4], rg[4], ru[4];
+    auto fetch = [&](int k0) {
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         const int kk = k0 + lk + j;
-        float a = 0.0f, wg = 0.0f, wu = 0.0f;
-        if (lr < ti.valid) a = ld_f32(A + (a_row0 + lr) * p.k_wrap + (kk % p.k_wrap));
-        if (f0 + lr < p.F) {
-          wg = ld_f32(W + (w_row0 + lr) * p.K + kk);
-          if (kSwiGLU) wu = ld_f32(W + (w_row0 + uoff + lr) * p.K + kk);
-        }
-        As[lk + j][lr] = a;
-        Bg[lk + j][lr] = wg;
-        if (kSwiGLU) Bu[lk + j][lr] = wu;
+        ra[j] = a_ok ? ld_f32(a_row + (wrap ? kk % p.k_wrap : kk)) : 0.0f;
+        rg[j] = w_ok ? ld_f32(wg_row + kk) : 0.0f;
+        ru[j] = (kSwiGLU && w_ok) ? ld_f32(wu_row + kk) : 0.0f;
+      }
+    };
+    fetch(k_begin);
+    for (int k0 = k_begin; k0 < k_begin + klen; k0 += kSimtK) {
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        As[lk + j][lr] = ra[j];
+        Bg[lk + j][lr] = rg[j];
+        if (kSwiGLU) Bu[lk + j][lr] = ru[j];
       }
       __syncthreads();
+      if (k0 + kSimtK < k_begin + klen) fetch(k0 + kSimtK);
 #pragma unroll
       for (int kk = 0; kk < kSimtK; ++kk) {
         float a[4], bg[4], bu[4];
