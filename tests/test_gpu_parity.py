@@ -306,6 +306,29 @@ def test_host_io_entry_point_matches_device_path(cuda_device):
     assert torch.equal(out_host, out_dev.cpu())
 
 
+def test_forward_replays_from_a_cuda_graph(cuda_device):
+    """moe_forward allocates nothing and never synchronises, so it can be captured into a CUDA
+    graph; every replay must give the eager result bit for bit (decode shapes, 32 experts)."""
+    w = replace(S.WORKLOADS["k2_decode_bf16"], name="k2_e32", E=32)
+    layer = _layer(w, seed=21)
+    out, ws, cfg = B.forward_layer(layer)
+    torch.cuda.synchronize()
+    ref = out.clone()
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        B.forward_layer(layer, out=out, ws=ws, stream=st)  # warm-up on the capture stream
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=st):
+        B.forward_layer(layer, out=out, ws=ws, stream=st)
+    for _ in range(3):
+        out.fill_(float("nan"))
+        g.replay()
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref)
+    assert B.moe_device_status(ws) == B.MOE_OK
+
+
 def test_out_of_range_expert_index_is_flagged(cuda_device):
     """An index outside [0, E) handed to moe_permute is skipped and reported, not followed."""
     w = SMALL_BF16
