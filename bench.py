@@ -53,6 +53,24 @@ DENSE_METRIC = "Dense block-0 MLP tokens/s (d=7168, I=18432) and % of roofline (
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    """The largest of the ranks' values, returned on every rank (collective; the value itself
+    for one rank).  Replicas finish when the slowest one does."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_throughput(units_per_rank: float, world: int, max_seconds: float) -> float:
+    """Whole-job throughput of `world` replicas: the units every rank processed over the time of
+    the slowest rank (weak scaling: the work per rank is fixed)."""
+    return world * units_per_rank / max_seconds
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -264,7 +282,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
     B.load_library()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    layer = S.make_layer(w, seed=0, device=dev)
+    layer = S.make_layer(w, seed=rank, device=dev)  # each replica its own batch
     cfg = B.config_for(w, flags=args.flags)
     ws = B.alloc_workspace(cfg, dev)
     out = torch.empty(w.T, w.d, dtype=layer.x.dtype, device=dev)
@@ -322,12 +340,9 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
     if status != B.MOE_OK:
         raise RuntimeError(f"device status after the timed steps: {B.status_string(status)}")
 
-    t_ms = torch.tensor([ms_total], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_ms, op=dist.ReduceOp.MAX)
-    ms_total = float(t_ms.item())
+    ms_total = max_over_ranks(ms_total, world, dev)
     ms_step = ms_total / args.steps
-    value = world * w.T / (ms_step / 1000.0)
+    value = replica_throughput(w.T, world, ms_step / 1000.0)
 
     # ------------------------------------------------------------- end to end (host buffers)
     io_bytes = w.T * w.d * layer.x.element_size()
@@ -353,11 +368,8 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
             e2e_step()
-        e2e_s = time.perf_counter() - t0
-        e2e_t = torch.tensor([e2e_s], dtype=torch.float64, device=dev)
-        if world > 1:
-            dist.all_reduce(e2e_t, op=dist.ReduceOp.MAX)
-        e2e = {"value": world * w.T * args.e2e_steps / float(e2e_t.item()), "unit": "tokens/s",
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": replica_throughput(w.T * args.e2e_steps, world, e2e_s), "unit": "tokens/s",
                "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
                "path": ("pinned host x'_n -> moe_forward_block -> pinned host x_{n+1}, "
                         "synchronised per step") if args.block else
@@ -505,7 +517,7 @@ def run_dense(args, w, rank: int, world: int, local_rank: int):
     B.load_library()
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    layer = S.make_dense(w, seed=0, device=dev)
+    layer = S.make_dense(w, seed=rank, device=dev)  # each replica its own batch
     ws = torch.zeros(B.moe_dense_mlp_workspace_size(w.T, w.d, w.I, layer.x.dtype),
                      dtype=torch.uint8, device=dev)
     out = torch.empty(w.T, w.d, dtype=layer.x.dtype, device=dev)
@@ -546,11 +558,8 @@ def run_dense(args, w, rank: int, world: int, local_rank: int):
     clocks = sampler.stop()
     if B.moe_device_status(ws) != B.MOE_OK:
         raise RuntimeError("device status after the timed steps")
-    t_ms = torch.tensor([ev0.elapsed_time(ev1)], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(t_ms, op=dist.ReduceOp.MAX)
-    ms_step = float(t_ms.item()) / args.steps
-    value = world * w.T / (ms_step / 1000.0)
+    ms_step = max_over_ranks(ev0.elapsed_time(ev1), world, dev) / args.steps
+    value = replica_throughput(w.T, world, ms_step / 1000.0)
 
     e2e = None
     if not args.no_e2e:  # host x -> device, the MLP, device y -> host, every step
@@ -567,11 +576,13 @@ def run_dense(args, w, rank: int, world: int, local_rank: int):
 
         for _ in range(3):
             e2e_step()
+        if world > 1:
+            dist.barrier()
         t0 = time.perf_counter()
         for _ in range(args.e2e_steps):
             e2e_step()
-        e2e_s = time.perf_counter() - t0
-        e2e = {"value": world * w.T * args.e2e_steps / e2e_s, "unit": "tokens/s",
+        e2e_s = max_over_ranks(time.perf_counter() - t0, world, dev)
+        e2e = {"value": replica_throughput(w.T * args.e2e_steps, world, e2e_s), "unit": "tokens/s",
                "h2d_bytes_per_step": io_bytes, "d2h_bytes_per_step": io_bytes,
                "path": "pinned host x -> moe_dense_mlp -> pinned host y, synchronised per step"}
     if rank != 0:
