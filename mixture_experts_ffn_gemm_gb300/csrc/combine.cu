@@ -18,6 +18,33 @@ constexpr int kMaxK = 32;
 
 // y_perm and y_shared hold fp32 expert outputs; resid (optional, the block's residual stream) is
 // in the output type; out is bf16 or fp32, rounded once from the fp32 sum.
+// acc[0..7] += sum over the token's k slots of gw[j] * y[rows[j]][c .. c+7], in slot order.
+// Four rows are loaded before any is used (a skipped slot, rows[j] < 0, reads nothing and adds
+// zero), so each thread has four row loads in flight instead of one.
+__device__ __forceinline__ void gather_rows8(const float* __restrict__ y, const int64_t* rows,
+                                             const float* gw, int k, int64_t width, int c,
+                                             float (&acc)[8]) {
+  for (int j0 = 0; j0 < k; j0 += 4) {
+    float v[4][8];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int j = j0 + u;
+      if (j < k && rows[j] >= 0) {
+        load8(y + rows[j] * width + c, v[u]);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[u][i] = 0.0f;
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const float g = j0 + u < k ? gw[j0 + u] : 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = fmaf(g, v[u][i], acc[i]);
+    }
+  }
+}
+
 template <typename TO>
 __global__ void __launch_bounds__(256)
     combine_kernel(const float* __restrict__ y_perm, const float* __restrict__ y_shared,
@@ -38,14 +65,7 @@ __global__ void __launch_bounds__(256)
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        if (rows[j] < 0) continue;
-        float v[8];
-        load8(y_perm + rows[j] * d + c, v);
-        const float w = gw[j];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(w, v[i], acc[i]);
-      }
+      gather_rows8(y_perm, rows, gw, k, d, c, acc);
       if (y_shared) {
         float v[8];
         load8(y_shared + t * d + c, v);
@@ -108,13 +128,7 @@ __global__ void __launch_bounds__(256)
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-      for (int j = 0; j < k; ++j) {
-        if (rows[j] < 0) continue;
-        float v[8];
-        load8(y_perm + rows[j] * L + c, v);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) acc[i] = fmaf(gw[j], v[i], acc[i]);
-      }
+      gather_rows8(y_perm, rows, gw, k, L, c, acc);
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         ysum[c + i] = acc[i];
