@@ -44,6 +44,7 @@ struct TcParams {
   CUtensorMap map_w;      // routed weights [E * w_group_rows][K]
   CUtensorMap map_act_d;  // dense-group activations
   CUtensorMap map_w_d;    // dense-group weights
+  CUtensorMap map_out;    // fp32 output [rows][ldo], box {32, 32}, 128-byte swizzle (tma_out)
   const int32_t* offsets;
   int32_t n_routed, w_group_rows, u_off, u_off_d;
   int32_t dense_rows, dense_act_row0, dense_out_row0;
@@ -54,6 +55,7 @@ struct TcParams {
   void* out_d;                   // the dense group's output and row pitch
   int64_t ldo_d;
   int32_t out_f32;
+  int32_t tma_out;      // token-rows fp32 stores: whole 32-row chunks leave by TMA from staging
   const float* addend;  // EPI_STORE_ADD: fp32 [rows][ld_add]
   int64_t ld_add;
   uint32_t* err;
@@ -124,7 +126,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + S::STAGES * S::STAGE);
+  // stages, then the staging / exchange buffers (1024-byte aligned: TMA reads them swizzled),
+  // then barriers and the tile table
+  uint8_t* staging = smem + S::STAGES * S::STAGE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(staging + S::STAGING + S::XCH);
   uint64_t* full = bars;
   uint64_t* empty = bars + S::STAGES;
   uint64_t* tfull = bars + 2 * S::STAGES;
@@ -132,10 +137,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
   uint64_t* drain = tempty + 2;
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  int* tile_start = reinterpret_cast<int*>(smem + S::STAGES * S::STAGE + S::BAR_BYTES);
+  int* tile_start = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(bars) + S::BAR_BYTES);
   int* row_start = tile_start + (kTcMaxGroups + 1);
   int* scratch = row_start + (kTcMaxGroups + 1);
-  uint8_t* staging = smem + S::STAGES * S::STAGE + S::BAR_BYTES + S::TABLE_BYTES;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -363,8 +367,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
               v[q] = make_uint4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
               v[4 + q] = make_uint4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
             }
-            uint8_t* dst = (uint8_t*)out + (row0 * ldo + (int64_t)ti.ft * S::FPT + c) * 4;
-            store_rows_128B(buf, lane, v, dst, ldo * 4, vrows);
+            if (p.tma_out && vrows == 32) {
+              // the chunk in the 128-byte swizzled layout; the TMA unswizzles it on the way out
+              if (lane == 0) tma_store_wait_read();  // the previous chunk has left the buffer
+              __syncwarp();
+#pragma unroll
+              for (int j = 0; j < 8; ++j)
+                *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = v[j];
+              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+              __syncwarp();
+              if (lane == 0) tma_store_2d_stream(&p.map_out, buf, ti.ft * S::FPT + c, (int)row0);
+            } else {
+              if (p.tma_out && lane == 0) tma_store_wait_read();
+              __syncwarp();
+              uint8_t* dst = (uint8_t*)out + (row0 * ldo + (int64_t)ti.ft * S::FPT + c) * 4;
+              store_rows_128B(buf, lane, v, dst, ldo * 4, vrows);
+            }
           }
         } else {  // bf16: chunks of 64 columns
 #pragma unroll 1
@@ -482,6 +500,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
     }
   }
 
+  if (S::kStaged && p.tma_out && warp >= 2 && lane == 0) tma_store_wait_all();
   tc_fence_before();
   __syncthreads();
   if (warp == 1) {
@@ -526,6 +545,19 @@ static bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_
              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
+}
+
+// fp32 output [rows][cols] for bulk stores of 32 x 32 chunks (128-byte swizzle in shared memory).
+static bool make_map_f32_out(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !base || rows <= 0 || cols <= 0) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <bool kSwap, int kBN, int kEpi>
@@ -615,6 +647,16 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
   p.out_d = g.out_d ? g.out_d : g.out;
   p.ldo_d = g.out_d ? g.ldo_d : g.ldo;
   p.out_f32 = g.out_dtype == MOE_F32;
+  // token-rows fp32 stores by TMA when every group writes the same tensor: its rows end at the
+  // routed rows or at the dense group's last row, whichever is later
+  if (!swap && g.epi == EPI_STORE && p.out_f32 && p.out_d == p.out && p.ldo_d == p.ldo &&
+      g.ldo % 4 == 0 &&
+      (reinterpret_cast<uintptr_t>(g.out) & 15) == 0) {
+    const int64_t routed_end = g.n_routed > 0 ? g.act_rows : 0;
+    const int64_t dense_end = g.dense_rows > 0 ? (int64_t)g.dense_out_row0 + g.dense_rows : 0;
+    const int64_t out_rows = routed_end > dense_end ? routed_end : dense_end;
+    if (out_rows > 0 && make_map_f32_out(&p.map_out, g.out, out_rows, g.ldo)) p.tma_out = 1;
+  }
   p.addend = (const float*)g.addend;
   p.ld_add = g.ld_add;
   p.err = g.err;
