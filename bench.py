@@ -39,9 +39,9 @@ METRIC = "MoE-layer tokens/s (d=7168, 384 experts top-8) and % of roofline (HBM 
 MEASURED_TRAFFIC_RATIO = {
     "gemm13_swiglu_swap": (1.004, "profiles/gemm_tc_swap_decode_E32.md", "a 32-expert decode capture"),
     "gemm2_swap": (0.994, "profiles/gemm_tc_swap_decode_E32.md", "a 32-expert decode capture"),
-    "gemm13_swiglu_rows": (1.099, "profiles/gemm_tc_rows_prefill_E64_T4096.md",
+    "gemm13_swiglu_rows": (1.093, "profiles/gemm_tc_rows_prefill_E64_T4096.md",
                            "a 64-expert, 4096-token prefill capture"),
-    "gemm2_rows": (0.984, "profiles/gemm_tc_rows_prefill_E64_T4096.md",
+    "gemm2_rows": (0.982, "profiles/gemm_tc_rows_prefill_E64_T4096.md",
                    "a 64-expert, 4096-token prefill capture"),
     "gemm13_swiglu_fp8": (1.018, "profiles/gemm_fp8_E64_T4096.md",
                           "a 64-expert, 4096-token fp8 capture"),
