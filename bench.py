@@ -49,6 +49,13 @@ MEASURED_TRAFFIC_RATIO = {
     "gemm13_swiglu_w4": (1.010, "profiles/gemm_w4_decode_E32.md", "a 32-expert INT4 decode capture"),
     "gemm2_w4": (0.966, "profiles/gemm_w4_decode_E32.md", "a 32-expert INT4 decode capture"),
 }
+# the K3 latent launches carry the same labels as the K2 ones but other shapes
+MEASURED_TRAFFIC_RATIO_LATENT = {
+    "gemm13_swiglu_rows": (1.04, "profiles/gemm_tc_k3_latent_E64_T4096.md",
+                           "a 64-expert, 4096-token K3 latent capture"),
+    "gemm2_rows": (0.97, "profiles/gemm_tc_k3_latent_E64_T4096.md",
+                   "a 64-expert, 4096-token K3 latent capture"),
+}
 DENSE_METRIC = "Dense block-0 MLP tokens/s (d=7168, I=18432) and % of roofline (HBM or TC)"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -409,7 +416,8 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
             roof = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peak,
                     "unit": "GB/s", "frac": achieved / peak, "peak_source": f"{peak_src} hbm_gbs",
                     "work_per_launch": by[unit_key]}
-        ratio = MEASURED_TRAFFIC_RATIO.get(dom)
+        ratio = ((MEASURED_TRAFFIC_RATIO_LATENT.get(dom) if w.d_latent else None) or
+                 MEASURED_TRAFFIC_RATIO.get(dom))
         roof["traffic"] = ratio[0] * by[unit_key] if ratio else None
         if ratio:
             roof["traffic_source"] = (f"{ratio[1]}: ncu DRAM bytes / algorithmic bytes = "
