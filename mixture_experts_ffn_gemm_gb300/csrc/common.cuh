@@ -132,17 +132,9 @@ __device__ __forceinline__ void tma_load_2d(void* smem_dst, const CUtensorMap* m
 }
 
 // Bulk tensor store of a 2D box from shared memory (the map's swizzle applies), tracked in the
-// thread's bulk async group.  x is the innermost coordinate in elements, y the row.
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void* smem_src,
-                                             int32_t x, int32_t y) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];\n\t"
-      "cp.async.bulk.commit_group;" ::"l"(reinterpret_cast<uint64_t>(map)),
-      "r"(smem_u32(smem_src)), "r"(x), "r"(y)
-      : "memory");
-}
-// The same store marked to leave L2 first (streamed output that no later step of the kernel
-// reads), so that it does not push out operands that are still being re-read.
+// thread's bulk async group; x is the innermost coordinate in elements, y the row.  Marked to
+// leave L2 first (streamed output that no later step of the kernel reads), so that it does not
+// push out operands that are still being re-read.
 __device__ __forceinline__ void tma_store_2d_stream(const CUtensorMap* map, const void* smem_src,
                                                     int32_t x, int32_t y) {
   asm volatile(
@@ -286,19 +278,6 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
         "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
         "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-}
-// Whole warp: each lane reads 32 consecutive 32-bit columns of its TMEM lane.
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-      "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
-        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
-        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
-        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(taddr));
 }
 
