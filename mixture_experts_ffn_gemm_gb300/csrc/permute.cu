@@ -86,13 +86,24 @@ __global__ void __launch_bounds__(32)
   const int64_t p0 = (int64_t)blockIdx.x * kChunk;
   const int64_t p1 = min(P, p0 + kChunk);
   const uint32_t lt = (1u << lane) - 1u;
-  for (int64_t q = p0; q < p1; q += 32) {
-    const int64_t p = q + lane;
+  // the chunk's expert ids, all loaded before the in-order walk (no load latency per step)
+  int ids[kChunk / 32];
+#pragma unroll
+  for (int i = 0; i < kChunk / 32; ++i) {
+    const int64_t p = p0 + i * 32 + lane;
     int e = -2;  // -2: lane past the chunk end
     if (p < p1) {
       e = idx[p];
       if (e < 0 || e >= E) e = -1;  // out of range: skipped (the count kernel raised the flag)
     }
+    ids[i] = e;
+  }
+#pragma unroll
+  for (int i = 0; i < kChunk / 32; ++i) {
+    const int64_t q = p0 + i * 32;
+    if (q >= p1) break;  // warp-uniform
+    const int64_t p = q + lane;
+    const int e = ids[i];
     const uint32_t peers = __match_any_sync(0xffffffffu, e);
     const int rank = __popc(peers & lt);
     const int leader = __ffs(peers) - 1;

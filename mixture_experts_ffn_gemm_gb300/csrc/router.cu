@@ -32,14 +32,23 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
 
   float key[EPL];
   float sig[EPL];
+  // the split-K slices in order; each slice's EPL loads of a lane are issued together
+  float zs[EPL];
+#pragma unroll
+  for (int j = 0; j < EPL; ++j) zs[j] = 0.0f;
+  for (int s = 0; s < S; ++s) {
+    const float* ps = partial + s * split_stride + t * E;
+#pragma unroll
+    for (int j = 0; j < EPL; ++j)
+      if (lane + 32 * j < E) zs[j] += ps[lane + 32 * j];
+  }
 #pragma unroll
   for (int j = 0; j < EPL; ++j) {
     const int e = lane + 32 * j;
     key[j] = -INFINITY;
     sig[j] = 0.0f;
     if (e < E) {
-      float z = 0.0f;
-      for (int s = 0; s < S; ++s) z += partial[s * split_stride + t * E + e];
+      const float z = zs[j];
       if (logits_out) logits_out[t * E + e] = z;
       const float sg = 1.0f / (1.0f + expf(-z));
       const float kv = sg + b[e];
