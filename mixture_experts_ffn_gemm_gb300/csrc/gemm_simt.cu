@@ -38,6 +38,24 @@ __device__ __forceinline__ float ld_f32(const T* p) {
   return to_f32<T>(p[0]);
 }
 
+// Four consecutive values as fp32 with one vector load (p 16-byte aligned for fp32, 8 for bf16).
+__device__ __forceinline__ void ld4_f32(const float* p, float (&v)[4]) {
+  const float4 q = *reinterpret_cast<const float4*>(p);
+  v[0] = q.x;
+  v[1] = q.y;
+  v[2] = q.z;
+  v[3] = q.w;
+}
+__device__ __forceinline__ void ld4_f32(const __nv_bfloat16* p, float (&v)[4]) {
+  const uint2 q = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&q.y));
+  v[0] = a.x;
+  v[1] = a.y;
+  v[2] = b.x;
+  v[3] = b.y;
+}
+
 template <typename TA, typename TW, bool kSwiGLU>
 __global__ void __launch_bounds__(kSimtThreads) moe_gemm_simt_kernel(const SimtParams p) {
   __shared__ int tile_start[kSimtMaxGroups + 1];
@@ -84,13 +102,16 @@ __global__ void __launch_bounds__(kSimtThreads) moe_gemm_simt_kernel(const SimtP
     const TW* wg_row = W + (w_row0 + lr) * p.K;
     const TW* wu_row = W + (w_row0 + uoff + lr) * p.K;
     float ra[4], rg[4], ru[4];
+    // 4 consecutive k per row: one vector load each (k0 + lk is a multiple of 4, and a wrapped
+    // activation row repeats with a period that is a multiple of 16)
     auto fetch = [&](int k0) {
+      const int kk = k0 + lk;
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int kk = k0 + lk + j;
-        ra[j] = a_ok ? ld_f32(a_row + (wrap ? kk % p.k_wrap : kk)) : 0.0f;
-        rg[j] = w_ok ? ld_f32(wg_row + kk) : 0.0f;
-        ru[j] = (kSwiGLU && w_ok) ? ld_f32(wu_row + kk) : 0.0f;
+      for (int j = 0; j < 4; ++j) ra[j] = rg[j] = ru[j] = 0.0f;
+      if (a_ok) ld4_f32(a_row + (wrap ? kk % p.k_wrap : kk), ra);
+      if (w_ok) {
+        ld4_f32(wg_row + kk, rg);
+        if (kSwiGLU) ld4_f32(wu_row + kk, ru);
       }
     };
     fetch(k_begin);
@@ -148,6 +169,11 @@ __global__ void __launch_bounds__(kSimtThreads) moe_gemm_simt_kernel(const SimtP
 cudaError_t launch_gemm_simt(const GroupedGemm& g, int num_sms, cudaStream_t st) {
   if (g.n_routed > kSimtMaxGroups - 1) return cudaErrorInvalidValue;
   if (g.K % (kSimtK * g.k_splits) || (g.K / g.k_splits) % kSimtK) return cudaErrorInvalidValue;
+  // operands are read 4 consecutive values at a time with vector loads
+  auto aligned16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15) == 0; };
+  if (!aligned16(g.act) || !aligned16(g.w) || !aligned16(g.act_d) || !aligned16(g.w_d))
+    return cudaErrorInvalidValue;
+  if (g.k_wrap > 0 && g.k_wrap % kSimtK) return cudaErrorInvalidValue;
   if (g.epi == EPI_STORE_ADD) return cudaErrorInvalidValue;
   SimtParams p;
   p.act = g.act;
