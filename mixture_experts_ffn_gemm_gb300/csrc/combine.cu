@@ -49,7 +49,8 @@ template <typename TO>
 __global__ void __launch_bounds__(256)
     combine_kernel(const float* __restrict__ y_perm, const float* __restrict__ y_shared,
                    const int32_t* __restrict__ perm_dst, const float* __restrict__ weight,
-                   int64_t T, int k, int d, const TO* __restrict__ resid, TO* __restrict__ out) {
+                   int64_t T, int k, int d, const TO* __restrict__ resid, TO* __restrict__ out,
+                   int cols_per_block) {
   __shared__ int64_t rows[kMaxK];
   __shared__ float gw[kMaxK];
   const int64_t P = T * k;
@@ -61,7 +62,11 @@ __global__ void __launch_bounds__(256)
       gw[threadIdx.x] = weight[t * k + threadIdx.x];
     }
     __syncthreads();
-    for (int c = threadIdx.x * 8; c < d; c += blockDim.x * 8) {
+    // columns [c_begin, c_end) of the row: the whole row, or one slice of it when few tokens
+    // spread over blockIdx.y
+    const int c_begin = blockIdx.y * cols_per_block;
+    const int c_end = min(d, c_begin + cols_per_block);
+    for (int c = c_begin + threadIdx.x * 8; c < c_end; c += blockDim.x * 8) {
       float acc[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
@@ -89,15 +94,20 @@ cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* y_shar
   if (T <= 0) return cudaSuccess;
   if (k > kMaxK || d % 8) return cudaErrorInvalidValue;
   const int64_t blocks = T < (int64_t)num_sms * 8 ? T : (int64_t)num_sms * 8;
+  // few tokens: each row in slices of 2048 columns (one 8-column chunk per thread) over
+  // blockIdx.y, so that every slice's loads are in flight at once
+  const int slices = T < (int64_t)num_sms * 4 ? (d + 2047) / 2048 : 1;
+  const int cols = slices > 1 ? 2048 : d;
+  const dim3 grid((unsigned)blocks, (unsigned)slices);
   LaunchScope ls("combine", st);
   if (act_dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(
+    combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
         (const float*)y_perm, (const float*)y_shared, perm_dst, weight, T, k, d,
-        (const __nv_bfloat16*)resid, (__nv_bfloat16*)out);
+        (const __nv_bfloat16*)resid, (__nv_bfloat16*)out, cols);
   else
-    combine_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(
+    combine_kernel<float><<<grid, 256, 0, st>>>(
         (const float*)y_perm, (const float*)y_shared, perm_dst, weight, T, k, d,
-        (const float*)resid, (float*)out);
+        (const float*)resid, (float*)out, cols);
   return cudaGetLastError();
 }
 
