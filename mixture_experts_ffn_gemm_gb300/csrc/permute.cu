@@ -121,12 +121,88 @@ __global__ void __launch_bounds__(32)
   }
 }
 
+// All P <= kChunk pairs in one CTA of 1024 threads: the count, the scan and the ordered walk of
+// the three kernels above, without their launch gaps (decode batches).  Same result.
+__global__ void __launch_bounds__(1024)
+    permute_small_kernel(const int32_t* __restrict__ idx, int P, int E, int64_t shared_rows,
+                         int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                         int32_t* __restrict__ perm_src, int32_t* __restrict__ perm_dst,
+                         uint32_t* err) {
+  __shared__ int hist[kMaxExperts];
+  __shared__ int sc[1024];
+  const int tid = threadIdx.x;
+  for (int e = tid; e < kMaxExperts; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  int my_e = -2;  // this thread's pair: -2 none, -1 out of range
+  if (tid < P) {
+    my_e = idx[tid];
+    if (my_e >= 0 && my_e < E)
+      atomicAdd(&hist[my_e], 1);
+    else
+      my_e = -1;
+  }
+  if (my_e == -1) raise_flag(err, kErrIndex);
+  __syncthreads();
+  const int run = tid < E ? hist[tid] : 0;
+  sc[tid] = run;
+  __syncthreads();
+  for (int off = 1; off < 1024; off <<= 1) {  // inclusive scan over experts
+    const int v = tid >= off ? sc[tid - off] : 0;
+    __syncthreads();
+    sc[tid] += v;
+    __syncthreads();
+  }
+  if (tid < E) {
+    counts[tid] = run;
+    offsets[tid] = sc[tid] - run;
+    hist[tid] = sc[tid] - run;  // from here: the next free row of expert tid
+  }
+  if (tid == 0) {
+    counts[E] = (int32_t)shared_rows;
+    offsets[E] = P;
+    offsets[E + 1] = (int32_t)(P + shared_rows);
+  }
+  __syncthreads();
+  if (tid >= 32) return;
+  // warp 0 walks the pairs in order; lanes with the same expert take consecutive rows
+  const int lane = tid;
+  const uint32_t lt = (1u << lane) - 1u;
+  for (int q = 0; q < P; q += 32) {
+    const int p = q + lane;
+    int e = -2;
+    if (p < P) {
+      e = idx[p];
+      if (e < 0 || e >= E) e = -1;
+    }
+    const uint32_t peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & lt);
+    const int leader = __ffs(peers) - 1;
+    int pos = 0;
+    if (e >= 0) pos = hist[e] + rank;
+    __syncwarp();
+    if (e >= 0 && lane == leader) hist[e] += __popc(peers);
+    __syncwarp();
+    if (e >= 0) {
+      perm_src[pos] = p;
+      perm_dst[p] = pos;
+    } else if (e == -1) {
+      perm_dst[p] = -1;
+    }
+  }
+}
+
 cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int E, int n_shared,
                            int32_t* chunk_counts, int32_t* counts, int32_t* offsets,
                            int32_t* perm_src, int32_t* perm_dst, uint32_t* err, cudaStream_t st) {
   if (E > kMaxExperts - 1) return cudaErrorInvalidValue;
   const int64_t P = T * k;
   const int nchunks = permute_chunks(P);
+  if (P > 0 && P <= kChunk) {
+    LaunchScope ls("permute_small", st);
+    permute_small_kernel<<<1, 1024, 0, st>>>(idx, (int)P, E, T * n_shared, counts, offsets,
+                                             perm_src, perm_dst, err);
+    return cudaGetLastError();
+  }
   if (nchunks > 0) {
     LaunchScope ls("permute_count", st);
     permute_count_kernel<<<nchunks, 256, 0, st>>>(idx, P, E, chunk_counts, err);

@@ -368,5 +368,6 @@ def test_launch_counter_counts_kernels(cuda_device):
     B.forward_layer(layer)
     torch.cuda.synchronize()
     n = B.moe_launch_count()
-    # router GEMM + top-k, count + scan + scatter, gather, two grouped GEMMs, combine
-    assert n >= 8
+    # router GEMM + top-k, the permute (one kernel up to 1024 pairs, else count + scan + scatter),
+    # gather, two grouped GEMMs, combine
+    assert n >= 7
