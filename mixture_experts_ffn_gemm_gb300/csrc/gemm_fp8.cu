@@ -9,19 +9,24 @@
 //
 // Kernel shape: persistent, one CTA per SM, 320 threads:
 //   warp 0      TMA producer: one K-block (128 e4m3 = one 128-byte swizzle row) per stage;
-//   warp 1      MMA issuer: per K-block two products, one per 128-row weight box, each 4 x
-//               tcgen05.mma kind::f8f6f4 (M = 128, N = 128, K = 32) into the next slot of a ring
-//               of four 128-column TMEM partial buffers, commit -> partial_full[slot];
-//   warps 2..9  epilogue/promotion: two warps per TMEM lane quarter; warp half h owns columns
-//               [64h, 64h + 64) of every slot.  Per slot they read the partial, multiply by the
-//               row's activation scale times the box's weight scale and add into fp32 registers,
-//               then free the slot.  With four slots the MMA runs up to two K-blocks ahead of the
-//               promotion, so the two overlap.
+//   warp 1      MMA issuer: per K-block one product, 4 x tcgen05.mma kind::f8f6f4 (M = 128,
+//               N = 256, K = 32), into the next slot of a ring of two 256-column TMEM partial
+//               buffers, commit -> partial_full[slot] (kF8SPK = 2 splits it into one N = 128
+//               product per weight box over four 128-column slots);
+//   warps 2..9  epilogue/promotion: kF8Parts = 2 warps per TMEM lane quarter; warp part p owns
+//               columns [64p, 64p + 64) of each 128-column weight box of every slot.  Per slot
+//               they read the partial, multiply by the row's activation scale times the box's
+//               weight scale and add into fp32 registers, then free the slot.  The TMEM reads are
+//               the long pole of that hand-off: one warp reads at a fixed rate whatever the load
+//               shape, so a slot's 128 KB is read faster by more warps (1000, 820 and 740 cycles
+//               per K-block with 4, 8 and 16 warps in a microbenchmark, against 512 cycles of
+//               MMA).  Four parts (16 warps) measured slower in the kernel itself: at 576
+//               threads a thread gets 96 registers, and the loop no longer fits.
 // Tiles are token rows (M = 128) x 256 weight rows, as in the bf16 rows orientation:
 //   SwiGLU: the first box holds the W1 rows of 128 features, the second the W3 rows of the same
-//           features; warp half 0 owns features 0..63 (g and u), half 1 features 64..127.  The
-//           epilogue forms h = SiLU(g) * u and quantises it per row per 128 features -- exactly one
-//           tile -- to e4m3 with scale amax/448 (the two halves exchange their amax).
+//           features; warp part p owns features 64p..64p + 63 (g and u).  The epilogue forms
+//           h = SiLU(g) * u and quantises it per row per 128 features -- exactly one tile -- to
+//           e4m3 with scale amax/448 (the parts exchange their amax).
 //   store:  the boxes are weight blocks 2 ft and 2 ft + 1 (output features 0..127 and
 //           128..255 of the tile); fp32 output, written through a per-warp staging buffer.
 // Every wait is bounded as in the bf16 kernel.
@@ -34,7 +39,10 @@
 
 namespace moe {
 
-constexpr int kF8Threads = 320;
+constexpr int kF8Parts = 2;                  // promotion warps per TMEM lane quarter (2 or 4)
+constexpr int kF8PartCols = 128 / kF8Parts;  // columns of each weight box per promotion warp
+constexpr int kF8PromoWarps = 4 * kF8Parts;
+constexpr int kF8Threads = 64 + 32 * kF8PromoWarps;
 constexpr int kF8BK = 128;                // e4m3 per K-block = bytes per row of a stage
 constexpr int kF8BN = 256;
 constexpr int kF8Box = 128 * 128;         // one 128-row x 128-byte box
@@ -42,14 +50,15 @@ constexpr int kF8Stage = kF8Box + 2 * kF8Box;
 constexpr int kF8MaxGroups = 1025;
 constexpr int kF8Table = 2 * (kF8MaxGroups + 1) * 4 + kF8Threads * 4;
 constexpr int kF8Bars = 256 + 64;
-constexpr int kF8Xchg = 2 * 2 * 128 * 4;  // [tile parity][half][row] amax exchange
-constexpr int kF8Stages = 4;
+constexpr int kF8Xchg = 2 * kF8Parts * 128 * 4;  // [tile parity][part][row] amax exchange
+constexpr int kF8Stages = 3;  // measured as fast as four (2.71 vs 2.75 ms at 8192 tokens)
 // Partial products per K-block: 1 = one N = 256 product into a ring of two 256-column TMEM
 // buffers; 2 = one N = 128 product per 128-row weight box into a ring of four 128-column slots.
 constexpr int kF8SPK = 1;
 constexpr int kF8SlotCols = 256 / kF8SPK;
 constexpr int kF8Slots = 512 / kF8SlotCols;
-constexpr int kF8Staging = 8 * 2048;     // 2 KB per epilogue warp for row-contiguous stores
+constexpr int kF8Staging = kF8PromoWarps * 2048;  // 2 KB per epilogue warp for row stores
+constexpr int kF8Acc = 2 * kF8PartCols;            // fp32 accumulators per promotion thread
 constexpr int kF8Smem = 1024 + kF8Stages * kF8Stage + kF8Bars + kF8Xchg + kF8Table + kF8Staging;
 static_assert(kF8Smem <= 232448, "fp8 GEMM shared memory");
 
@@ -98,16 +107,44 @@ __device__ __forceinline__ void store_rows_64B(uint8_t* buf, int lane, const uin
   }
 }
 
+// The same for 32 rows x 32 bytes (1 KB of the buffer): each read-back instruction writes 16
+// whole 32-byte row pieces.
+__device__ __forceinline__ void store_rows_32B(uint8_t* buf, int lane, const uint4 (&v)[2],
+                                               uint8_t* row0, int pitch, int valid_rows) {
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 2; ++j)
+    *reinterpret_cast<uint4*>(buf + lane * 32 + ((j ^ ((lane >> 2) & 1)) << 4)) = v[j];
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const int r = i * 16 + (lane >> 1);
+    const int j = lane & 1;
+    const uint4 w = *reinterpret_cast<const uint4*>(buf + r * 32 + ((j ^ ((r >> 2) & 1)) << 4));
+    if (r < valid_rows) *reinterpret_cast<uint4*>(row0 + (r * pitch + j * 16)) = w;
+  }
+}
+
+// A warp's piece of h rows: 64 or 32 bytes of e4m3 per row, by the width of its part.
+__device__ __forceinline__ void store_h_rows(uint8_t* buf, int lane, const uint4 (&v)[4],
+                                             uint8_t* row0, int pitch, int valid_rows) {
+  store_rows_64B(buf, lane, v, row0, pitch, valid_rows);
+}
+__device__ __forceinline__ void store_h_rows(uint8_t* buf, int lane, const uint4 (&v)[2],
+                                             uint8_t* row0, int pitch, int valid_rows) {
+  store_rows_32B(buf, lane, v, row0, pitch, valid_rows);
+}
+
 // SiLU for the fp8 epilogue: the quotient with the fast division (h is quantised to e4m3 next)
 __device__ __forceinline__ float silu_fp8(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 // One promotion step of a warp: wait for partial product ks (slot ks % kF8Slots), which holds
 // weight boxes BOX0 .. BOX0 + kF8SlotCols / 128 - 1; add s_box * partial[box column c] into
-// acc[box * 64 + c] for this thread's 64 columns of each box (tq addresses its lane and first
-// column; box 0 is scaled by s0, box 1 by s1), then release the slot.  False when the wait gave
-// up.
+// acc[box * kF8PartCols + c] for this thread's kF8PartCols columns of each box (tq addresses its
+// lane and first column; box 0 is scaled by s0, box 1 by s1), then release the slot.  False when
+// the wait gave up.
 template <int BOX0>
-__device__ __forceinline__ bool promote_slot(float (&acc)[128], float s0, float s1, uint32_t tq,
+__device__ __forceinline__ bool promote_slot(float (&acc)[kF8Acc], float s0, float s1, uint32_t tq,
                                              uint32_t ks,
                                              uint64_t* pfull, uint64_t* pempty, int lane,
                                              volatile int* abort_flag, uint32_t* err) {
@@ -120,20 +157,16 @@ __device__ __forceinline__ bool promote_slot(float (&acc)[128], float s0, float 
   const uint32_t tb = tq + slot * kF8SlotCols;
 #pragma unroll
   for (int j = 0; j < kF8SlotCols / 128; ++j) {  // the weight boxes this slot holds
-    constexpr int kBase = BOX0 * 64;
+    constexpr int kBase = BOX0 * kF8PartCols;
     const float sc = (BOX0 + j) ? s1 : s0;
 #pragma unroll
-    for (int c = 0; c < 64; c += 32) {
-      uint32_t v0[16], v1[16];
-      tmem_ld16(tb + j * 128 + c, v0);
-      tmem_ld16(tb + j * 128 + c + 16, v1);
+    for (int c = 0; c < kF8PartCols; c += 16) {  // 16 columns per TMEM load and wait
+      uint32_t v[16];
+      tmem_ld16(tb + j * 128 + c, v);
       tmem_ld_wait();
+      float* a = acc + kBase + j * kF8PartCols + c;
 #pragma unroll
-      for (int i = 0; i < 16; i += 2) {
-        fma2(acc[kBase + j * 64 + c + i], acc[kBase + j * 64 + c + i + 1], sc, v0[i], v0[i + 1]);
-        fma2(acc[kBase + j * 64 + c + 16 + i], acc[kBase + j * 64 + c + 16 + i + 1], sc, v1[i],
-             v1[i + 1]);
-      }
+      for (int i = 0; i < 16; i += 2) fma2(a[i], a[i + 1], sc, v[i], v[i + 1]);
     }
   }
   // every lane's loads of this slot have completed (tcgen05.wait::ld); one arrival per warp
@@ -155,10 +188,10 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
   uint64_t* pfull = bars + 2 * kF8Stages;  // [kF8Slots]
   uint64_t* pempty = pfull + kF8Slots;     // [kF8Slots]
   uint64_t* drain = pempty + kF8Slots;
-  uint64_t* xbar = drain + 1;  // [2]: amax exchange between the two epilogue halves
+  uint64_t* xbar = drain + 1;  // [2]: amax exchange between the epilogue parts
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 32);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-  float* xchg = reinterpret_cast<float*>(smem + kF8Stages * kF8Stage + kF8Bars);  // [2][128]
+  float* xchg = reinterpret_cast<float*>(smem + kF8Stages * kF8Stage + kF8Bars);  // [2][parts][128]
   int* tile_start = reinterpret_cast<int*>(smem + kF8Stages * kF8Stage + kF8Bars + kF8Xchg);
   int* row_start = tile_start + (kF8MaxGroups + 1);
   int* scratch = row_start + (kF8MaxGroups + 1);
@@ -175,11 +208,11 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
     }
     for (int b = 0; b < kF8Slots; ++b) {
       mbar_init(&pfull[b], 1);
-      mbar_init(&pempty[b], 8);  // one arrival per promotion warp
+      mbar_init(&pempty[b], kF8PromoWarps);  // one arrival per promotion warp
     }
     mbar_init(drain, 1);
-    mbar_init(&xbar[0], 8);
-    mbar_init(&xbar[1], 8);
+    mbar_init(&xbar[0], kF8PromoWarps);
+    mbar_init(&xbar[1], kF8PromoWarps);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -297,7 +330,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
   } else {
     // ---------------------------------------------------------------- promotion + epilogue
     const int quarter = warp & 3;
-    const int half = (warp - 2) >> 2;
+    const int part = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
     uint8_t* wbuf = staging + (warp - 2) * 2048;
     uint32_t ks = 0;  // partial products consumed so far (all tiles), as counted by the MMA issuer
@@ -326,9 +359,9 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
         ws0 = base + (int64_t)(ti.ft * 2) * nkb;
         ws1 = ws0 + nkb;
       }
-      float acc[128];
+      float acc[kF8Acc];
 #pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+      for (int i = 0; i < kF8Acc; ++i) acc[i] = 0.0f;
       // the scales of K-block kb + 1 are loaded while block kb is promoted (their global-memory
       // latency then hides behind the MMA instead of stalling every block)
       const float* sx_ptr = sx_col + act_row;
@@ -341,9 +374,9 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
           w0_n = __ldg(ws0 + kb + 1);
           w1_n = __ldg(ws1 + kb + 1);
         }
-        // this thread owns columns [half * 64, half * 64 + 64) of both slots of the K-block:
-        // acc[0..63] from the first weight box, acc[64..127] from the second
-        const uint32_t tq = tmem_base + half * 64 + ((uint32_t)(quarter * 32) << 16);
+        // this thread owns columns [part * P, part * P + P) of both weight boxes of the
+        // K-block, P = kF8PartCols: acc[0..P-1] from the first box, acc[P..2P-1] from the second
+        const uint32_t tq = tmem_base + part * kF8PartCols + ((uint32_t)(quarter * 32) << 16);
         const float s0 = sx * w0, s1 = sx * w1;
         if constexpr (kF8SPK == 1) {
           ok = promote_slot<0>(acc, s0, s1, tq, ks, pfull, pempty, lane, abort_flag, p.err);
@@ -357,18 +390,18 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
       const int64_t orow =
           (ti.dense ? (int64_t)p.dense_out_row0 : (int64_t)ti.grp_row0) + ti.rt * 128 + r;
       if (kSwiGLU) {
-        // h = SiLU(g) * u for this thread's 64 features, then e4m3 per 128-feature group
+        // h = SiLU(g) * u for this thread's features, then e4m3 per 128-feature group
         float amax = 0.0f;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          acc[j] = silu_fp8(acc[j]) * acc[64 + j];
+        for (int j = 0; j < kF8PartCols; ++j) {
+          acc[j] = silu_fp8(acc[j]) * acc[kF8PartCols + j];
           amax = fmaxf(amax, fabsf(acc[j]));
         }
-        // exchange with the other half through a double-buffered slot and a bounded mbarrier wait:
-        // slot it&1 is rewritten two tiles later, after the partner has passed the barrier of the
-        // tile in between, i.e. after it read this one
-        float* slot = xchg + (it & 1u) * 256;
-        slot[half * 128 + r] = amax;
+        // exchange with the other parts through a double-buffered slot and a bounded mbarrier
+        // wait: slot it&1 is rewritten two tiles later, after every part has passed the barrier of
+        // the tile in between, i.e. after each has read this one
+        float* slot = xchg + (it & 1u) * (kF8Parts * 128);
+        slot[part * 128 + r] = amax;
         __syncwarp();
         if (lane == 0) mbar_arrive(&xbar[it & 1u]);
         int x_ok = 1;
@@ -376,12 +409,13 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
         x_ok = __shfl_sync(0xffffffffu, x_ok, 0);
         __syncwarp();
         if (!x_ok) break;
-        amax = fmaxf(amax, slot[(half ^ 1) * 128 + r]);
+#pragma unroll
+        for (int q = 0; q < kF8Parts; ++q) amax = fmaxf(amax, slot[q * 128 + r]);
         const float scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
         const float rscale = __frcp_rn(scale);
-        uint4 v[4];
+        uint4 v[kF8PartCols / 16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kF8PartCols / 16; ++c) {
           uint32_t w[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q) {
@@ -393,21 +427,22 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
           }
           v[c] = make_uint4(w[0], w[1], w[2], w[3]);
         }
-        uint8_t* dst0 = (uint8_t*)p.out + (orow - lane) * p.ldo + (int64_t)ti.ft * 128 + half * 64;
-        store_rows_64B(wbuf, lane, v, dst0, (int)p.ldo, vrows);
-        if (valid && half == 0) p.out_sT[(int64_t)ti.ft * p.out_s_ld + orow] = scale;
+        uint8_t* dst0 =
+            (uint8_t*)p.out + (orow - lane) * p.ldo + (int64_t)ti.ft * 128 + part * kF8PartCols;
+        store_h_rows(wbuf, lane, v, dst0, (int)p.ldo, vrows);
+        if (valid && part == 0) p.out_sT[(int64_t)ti.ft * p.out_s_ld + orow] = scale;
       } else {
-        // acc[0..63] are output columns ft*256 + half*64 + j, acc[64..127] the same + 128
+        // acc[j], j < P, is output column ft*256 + part*P + j; acc[P + j] the same + 128
         uint8_t* dst0 = (uint8_t*)p.out +
-                        ((orow - lane) * p.ldo + (int64_t)ti.ft * kF8BN + half * 64) * 4;
+                        ((orow - lane) * p.ldo + (int64_t)ti.ft * kF8BN + part * kF8PartCols) * 4;
 #pragma unroll
-        for (int c = 0; c < 128; c += 16) {
+        for (int c = 0; c < kF8Acc; c += 16) {
           uint4 v[4];
 #pragma unroll
           for (int q = 0; q < 4; ++q)
             v[q] = make_uint4(__float_as_uint(acc[c + 4 * q]), __float_as_uint(acc[c + 4 * q + 1]),
                               __float_as_uint(acc[c + 4 * q + 2]), __float_as_uint(acc[c + 4 * q + 3]));
-          const int col = (c < 64 ? c : 128 + (c - 64));
+          const int col = (c < kF8PartCols ? c : 128 + (c - kF8PartCols));
           store_rows_64B(wbuf, lane, v, dst0 + col * 4, (int)p.ldo * 4, vrows);
         }
       }
