@@ -243,9 +243,12 @@ def _sample(T, n=6, seed=1):
 
 
 def _full_workload(name):
+    """One benchmark workload in the bench's launch configuration: routing and permutation on
+    every token, sampled expert rows, and the outputs of every token for decode-sized batches
+    (128 tokens), else of a seeded sample."""
     w = S.WORKLOADS[name]
     layer = _layer(w)
-    res = _full_check(layer, 0, rows=_sample(w.T),
+    res = _full_check(layer, 0, rows=None if w.T <= 128 else _sample(w.T),
                       output_rounding=LATENT_OUTPUT_ROUNDING and w.d_latent > 0)
     del layer
     torch.cuda.empty_cache()
