@@ -236,10 +236,28 @@ def time_oracle(prep, nthreads: int) -> float:
     return time.perf_counter() - t0
 
 
+def layer_config(w, block: bool, world: int) -> dict:
+    """The JSON line's `config` for a layer workload, the same on both arms."""
+    return {"workload": w.name + ("_block" if block else ""), "tokens": w.T, "d": w.d,
+            "experts": w.E, "top_k": w.k, "block_ffn_half": bool(block),
+            "expert_intermediate": w.I, "shared_intermediate": w.I_shared,
+            "d_latent": w.d_latent, "router": "fp32 logits",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (expert weights stream from HBM every step; no flush)"}
+
+
+def dense_config(w, world: int) -> dict:
+    """The JSON line's `config` for a dense-MLP workload, the same on both arms."""
+    return {"workload": w.name, "tokens": w.T, "d": w.d, "intermediate": w.I,
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (0.8 GB of weights stream from HBM every step; "
+                  "no flush)"}
+
+
 # ----------------------------------------------------------------------------------------------
 # reference arm: the oracle on the host cores
 # ----------------------------------------------------------------------------------------------
-def run_reference(args, w, rank: int):
+def run_reference(args, w, rank: int, world: int):
     if rank != 0:
         return
     import torch
@@ -261,8 +279,7 @@ def run_reference(args, w, rank: int):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1000.0 * statistics.mean(secs), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name, "tokens": w.T, "d": w.d, "experts": w.E, "top_k": w.k,
-                   "expert_intermediate": w.I, "d_latent": w.d_latent, "parallelism": "replicas"},
+        "config": layer_config(w, False, world),
         "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                          "sample": f"{n} of {w.T} tokens (seed 1) per step, fp64 C oracle, "
                                    f"{cores} threads"},
@@ -447,13 +464,7 @@ def run_ours(args, w, rank: int, world: int, local_rank: int):
                                                "int4 weights, bf16" if getattr(w, "int4", False)
                                                else "bf16"),
         "data": "synthetic",
-        "config": {"workload": w.name + ("_block" if args.block else ""), "tokens": w.T, "d": w.d,
-                   "experts": w.E, "top_k": w.k, "block_ffn_half": bool(args.block),
-                   "expert_intermediate": w.I, "shared_intermediate": w.I_shared,
-                   "d_latent": w.d_latent, "router": "fp32 logits",
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (expert weights stream from HBM every step; "
-                         "no flush)"},
+        "config": layer_config(w, args.block, world),
         "roofline": roof,
         "layer_roofline": layer_roof,
         "cpu_baseline": cpu,
@@ -510,8 +521,7 @@ def run_dense(args, w, rank: int, world: int, local_rank: int):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1000.0 * statistics.mean(secs), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": w.name, "tokens": w.T, "d": w.d, "intermediate": w.I,
-                       "parallelism": "replicas"},
+            "config": dense_config(w, world),
             "cpu_baseline": {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                              "sample": f"{n} of {w.T} tokens (seed 1) per step, fp64 C oracle"},
             "e2e": {"value": tps, "unit": "tokens/s", "h2d_bytes_per_step": 0,
@@ -628,10 +638,7 @@ def run_dense(args, w, rank: int, world: int, local_rank: int):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32" if w.act == "f32" else "bf16", "data": "synthetic",
-        "config": {"workload": w.name, "tokens": w.T, "d": w.d, "intermediate": w.I,
-                   "parallelism": "replicas" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (0.8 GB of weights stream from HBM every step; "
-                         "no flush)"},
+        "config": dense_config(w, world),
         "roofline": roof,
         "layer_roofline": {"t_roof_ms": 1000 * t_roof, "frac": 1000 * t_roof / ms_step,
                            "bound": "tensor" if lf / (tc_peak * 1e12) > lb / (peaks["hbm_gbs"] * 1e9)
@@ -668,7 +675,7 @@ def main():
         w = replace(w, name=f"{w.name}_E{args.experts or w.E}_T{args.tokens or w.T}",
                     E=args.experts or w.E, T=args.tokens or w.T)
     if args.impl == "reference":
-        run_reference(args, w, rank)
+        run_reference(args, w, rank, world)
         return
     if world > 1:
         import torch
