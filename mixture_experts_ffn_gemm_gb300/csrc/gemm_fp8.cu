@@ -57,7 +57,8 @@ constexpr int kF8Stages = 3;  // measured as fast as four (2.71 vs 2.75 ms at 81
 constexpr int kF8SPK = 1;
 constexpr int kF8SlotCols = 256 / kF8SPK;
 constexpr int kF8Slots = 512 / kF8SlotCols;
-constexpr int kF8Staging = kF8PromoWarps * 2048;  // 2 KB per epilogue warp for row stores
+constexpr int kF8WarpStaging = 8192;                 // per epilogue warp, for row stores
+constexpr int kF8Staging = kF8PromoWarps * kF8WarpStaging;
 constexpr int kF8Acc = 2 * kF8PartCols;            // fp32 accumulators per promotion thread
 constexpr int kF8Smem = 1024 + kF8Stages * kF8Stage + kF8Bars + kF8Xchg + kF8Table + kF8Staging;
 static_assert(kF8Smem <= 232448, "fp8 GEMM shared memory");
@@ -133,6 +134,28 @@ __device__ __forceinline__ void store_h_rows(uint8_t* buf, int lane, const uint4
 __device__ __forceinline__ void store_h_rows(uint8_t* buf, int lane, const uint4 (&v)[2],
                                              uint8_t* row0, int pitch, int valid_rows) {
   store_rows_32B(buf, lane, v, row0, pitch, valid_rows);
+}
+
+// Warp-cooperative store of 32 rows x 256 bytes (lane l holds row l: 64 fp32 from acc[a0..])
+// through an 8 KB XOR-swizzled buffer.  All 64 values go to shared memory before any is read
+// back, so their registers are free for the read-back; each store instruction then writes two
+// whole 256-byte row pieces.  Rows >= valid_rows are not written.
+__device__ __forceinline__ void store_rows_256B(uint8_t* buf, int lane, const float (&acc)[kF8Acc],
+                                                int a0, uint8_t* row0, int pitch, int valid_rows) {
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 16; ++j)
+    *reinterpret_cast<uint4*>(buf + lane * 256 + ((j ^ (lane & 15)) << 4)) =
+        make_uint4(__float_as_uint(acc[a0 + 4 * j]), __float_as_uint(acc[a0 + 4 * j + 1]),
+                   __float_as_uint(acc[a0 + 4 * j + 2]), __float_as_uint(acc[a0 + 4 * j + 3]));
+  __syncwarp();
+#pragma unroll 4
+  for (int i = 0; i < 16; ++i) {
+    const int r = i * 2 + (lane >> 4);
+    const int j = lane & 15;
+    const uint4 w = *reinterpret_cast<const uint4*>(buf + r * 256 + ((j ^ (r & 15)) << 4));
+    if (r < valid_rows) *reinterpret_cast<uint4*>(row0 + (r * pitch + j * 16)) = w;
+  }
 }
 
 // SiLU for the fp8 epilogue: the quotient with the fast division (h is quantised to e4m3 next)
@@ -332,7 +355,7 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
     const int quarter = warp & 3;
     const int part = (warp - 2) >> 2;
     const int r = quarter * 32 + lane;
-    uint8_t* wbuf = staging + (warp - 2) * 2048;
+    uint8_t* wbuf = staging + (warp - 2) * kF8WarpStaging;
     uint32_t ks = 0;  // partial products consumed so far (all tiles), as counted by the MMA issuer
     uint32_t it = 0;  // tiles finished by this thread: exchange slot it & 1
     bool ok = true;
@@ -435,15 +458,20 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
         // acc[j], j < P, is output column ft*256 + part*P + j; acc[P + j] the same + 128
         uint8_t* dst0 = (uint8_t*)p.out +
                         ((orow - lane) * p.ldo + (int64_t)ti.ft * kF8BN + part * kF8PartCols) * 4;
+        if constexpr (kF8PartCols == 64) {
+          store_rows_256B(wbuf, lane, acc, 0, dst0, (int)p.ldo * 4, vrows);
+          store_rows_256B(wbuf, lane, acc, 64, dst0 + 128 * 4, (int)p.ldo * 4, vrows);
+        } else {
 #pragma unroll
-        for (int c = 0; c < kF8Acc; c += 16) {
-          uint4 v[4];
+          for (int c = 0; c < kF8Acc; c += 16) {
+            uint4 v[4];
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            v[q] = make_uint4(__float_as_uint(acc[c + 4 * q]), __float_as_uint(acc[c + 4 * q + 1]),
-                              __float_as_uint(acc[c + 4 * q + 2]), __float_as_uint(acc[c + 4 * q + 3]));
-          const int col = (c < kF8PartCols ? c : 128 + (c - kF8PartCols));
-          store_rows_64B(wbuf, lane, v, dst0 + col * 4, (int)p.ldo * 4, vrows);
+            for (int q = 0; q < 4; ++q)
+              v[q] = make_uint4(__float_as_uint(acc[c + 4 * q]), __float_as_uint(acc[c + 4 * q + 1]),
+                                __float_as_uint(acc[c + 4 * q + 2]), __float_as_uint(acc[c + 4 * q + 3]));
+            const int col = (c < kF8PartCols ? c : 128 + (c - kF8PartCols));
+            store_rows_64B(wbuf, lane, v, dst0 + col * 4, (int)p.ldo * 4, vrows);
+          }
         }
       }
     }
