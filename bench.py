@@ -43,9 +43,9 @@ MEASURED_TRAFFIC_RATIO = {
                            "a 64-expert, 4096-token prefill capture"),
     "gemm2_rows": (0.982, "profiles/gemm_tc_rows_prefill_E64_T4096.md",
                    "a 64-expert, 4096-token prefill capture"),
-    "gemm13_swiglu_fp8": (1.012, "profiles/gemm_fp8_E64_T4096.md",
+    "gemm13_swiglu_fp8": (1.013, "profiles/gemm_fp8_E64_T4096.md",
                           "a 64-expert, 4096-token fp8 capture"),
-    "gemm2_fp8": (0.978, "profiles/gemm_fp8_E64_T4096.md", "a 64-expert, 4096-token fp8 capture"),
+    "gemm2_fp8": (0.973, "profiles/gemm_fp8_E64_T4096.md", "a 64-expert, 4096-token fp8 capture"),
     "gemm13_swiglu_w4": (1.010, "profiles/gemm_w4_decode_E32.md", "a 32-expert INT4 decode capture"),
     "gemm2_w4": (0.966, "profiles/gemm_w4_decode_E32.md", "a 32-expert INT4 decode capture"),
 }
