@@ -57,7 +57,9 @@ constexpr int kF8Stages = 3;  // measured as fast as four (2.71 vs 2.75 ms at 81
 constexpr int kF8SPK = 1;
 constexpr int kF8SlotCols = 256 / kF8SPK;
 constexpr int kF8Slots = 512 / kF8SlotCols;
-constexpr int kF8WarpStaging = 8192;                 // per epilogue warp, for row stores
+// per epilogue warp, for row stores: 32 rows x 256 bytes of fp32 with two parts (the W2
+// epilogue stages a whole weight box per row), 32 rows x 64 bytes with four
+constexpr int kF8WarpStaging = kF8PartCols == 64 ? 8192 : 2048;
 constexpr int kF8Staging = kF8PromoWarps * kF8WarpStaging;
 constexpr int kF8Acc = 2 * kF8PartCols;            // fp32 accumulators per promotion thread
 constexpr int kF8Smem = 1024 + kF8Stages * kF8Stage + kF8Bars + kF8Xchg + kF8Table + kF8Staging;
