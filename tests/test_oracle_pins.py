@@ -199,6 +199,23 @@ def test_bias_selects_but_does_not_weight(orc):
     assert np.array_equal(gates, gates2)
 
 
+def test_gates_closed_form_from_rational_sigmoids(orc):
+    """Logits ln 3, 0, -ln 3, -ln 9 have sigmoids 3/4, 1/2, 1/4, 1/10 exactly, so the gates have
+    closed forms: with no bias the top two are experts 0 and 1 with 2.827 * (3/5, 2/5); a bias of
+    0.6 on expert 2 lifts its key to 0.85 above expert 0's 0.75, and the gates, taken from the
+    unbiased sigmoids, are 2.827 * (1/4, 3/4) in key order.  A sign slip in the sigmoid, a gate
+    taken from the biased key, or a missing renormalisation fails one of these."""
+    ln3 = math.log(3.0)
+    z = np.array([[ln3, 0.0, -ln3, -math.log(9.0)]], np.float32)
+    cfg = orc.Config(T=1, d=1, E=4, k=2, I=1)
+    idx, gates, _ = orc.route_from_logits(cfg, z, np.zeros(4, np.float32))
+    assert list(idx[0]) == [0, 1]
+    np.testing.assert_allclose(gates[0], [2.827 * 0.6, 2.827 * 0.4], rtol=1e-6)
+    idx, gates, _ = orc.route_from_logits(cfg, z, np.array([0, 0, 0.6, 0], np.float32))
+    assert list(idx[0]) == [2, 0]
+    np.testing.assert_allclose(gates[0], [2.827 * 0.25, 2.827 * 0.75], rtol=1e-6)
+
+
 def _tiny_layer(T=64, seed=0, **over):
     from mixture_experts_ffn_gemm_gb300 import synthetic as S
     w = S.WORKLOADS["tiny_fp32"].with_tokens(T)
