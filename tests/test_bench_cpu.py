@@ -1,6 +1,9 @@
-"""The benchmark's reference arm times the fp64 oracle on the host cores; it needs no GPU, so its
-JSON line is checked here: the same metric and config as the kernels' arm, the oracle named as
-the baseline, and no host-device bytes.  Under a multi-rank launch only rank 0 prints."""
+"""The parts of the benchmark that need no GPU.
+
+The reference arm times the fp64 oracle on the host cores: its JSON line carries the same metric
+and config as the kernels' arm, names the oracle as the baseline and moves no host-device bytes;
+under a multi-rank launch only rank 0 prints.  The roofline's algorithmic FLOPs and bytes are
+checked against their closed forms."""
 import json
 import os
 import subprocess
@@ -39,3 +42,44 @@ def test_reference_prints_nothing_on_other_ranks():
     p = _run({"RANK": "1", "WORLD_SIZE": "2", "LOCAL_RANK": "1"})
     assert p.returncode == 0, p.stderr
     assert not [l for l in p.stdout.splitlines() if l.startswith("{")]
+
+
+def test_algorithmic_flops_match_the_closed_forms():
+    """Per token, the K2 layer is 2dE (router) + (k + 1) * 6dI (eight routed experts and the
+    shared one) = 798,228,480 FLOPs; the K3 latent layer adds the down- and up-projections (4dL)
+    and runs the routed experts at width L: 2dE + 4dL + k * 6LI + 6dI = 548,667,392."""
+    import bench
+    from mixture_experts_ffn_gemm_gb300 import synthetic as S
+    d, E, k, I, L = 7168, 384, 8, 2048, 3584
+    assert 2 * d * E + (k + 1) * 6 * d * I == 798_228_480
+    assert 2 * d * E + 4 * d * L + k * 6 * L * I + 6 * d * I == 548_667_392
+    assert bench.flops(S.WORKLOADS["k2_decode_bf16"], 1)["layer"] == 798_228_480
+    assert bench.flops(S.WORKLOADS["k2_prefill_bf16"], 3)["layer"] == 3 * 798_228_480
+    assert bench.flops(S.WORKLOADS["k3_latent_bf16"], 1)["layer"] == 548_667_392
+    f = bench.flops(S.WORKLOADS["k2_decode_bf16"], 1)
+    assert f["router"] + f["gemm13"] + f["gemm2"] == 798_228_480
+
+
+def test_algorithmic_bytes_count_each_touched_expert_once():
+    """A bf16 K2 expert is 3 * I * d * 2 = 88,080,384 bytes and an e4m3 one 44,040,192 bytes plus
+    2,688 fp32 block scales; the layer's bytes are the touched experts, the shared expert, the fp32
+    router weight, x in and the output out -- whatever the number of tokens that share an
+    expert."""
+    import numpy as np
+    import bench
+    from mixture_experts_ffn_gemm_gb300 import synthetic as S
+    d, E, I = 7168, 384, 2048
+    w = S.WORKLOADS["k2_decode_bf16"]
+    T = 128
+    idx = np.tile(np.arange(8, dtype=np.int32), (T, 1))  # every token on experts 0..7
+    by = bench.touched_bytes(w, idx)
+    assert by["touched_experts"] == 8
+    assert by["layer"] == (8 + 1) * 88_080_384 + E * d * 4 + 2 * T * d * 2
+    idx_all = (np.arange(T * 8, dtype=np.int32) % E).reshape(T, 8)
+    by_all = bench.touched_bytes(w, idx_all)
+    assert by_all["touched_experts"] == E
+    assert by_all["layer"] == (E + 1) * 88_080_384 + E * d * 4 + 2 * T * d * 2
+    wq = S.WORKLOADS["k2_fp8"]
+    byq = bench.touched_bytes(wq, idx)
+    assert 3 * I * d * 4.0 / (128 * 128) == 2688 * 4
+    assert byq["layer"] == (8 + 1) * (44_040_192 + 2688 * 4) + E * d * 4 + 2 * T * d * 2
