@@ -4,7 +4,8 @@ The dense MLP of the first block is y = (SiLU(x W1) * (x W3)) W2 per token (nnte
 "Printout": layer 0's DeepseekV3MLP).  The library runs it as one dense group through the expert
 GEMMs: token-rows tensor-core tiles for bf16 (W2 in 128-column tiles at T <= 256), CUDA cores for
 fp32.
-Bounds as for the layer: max |GPU - oracle| <= tol * rms(oracle), tol 1e-4 (fp32) / 2e-2 (bf16)."""
+The parity rule of the layer (parity_lib): tol 1e-4 (fp32) / 2e-2 (bf16) of rms(oracle), for bf16
+beyond the output's own rounding, the plain figure reported beside it."""
 from dataclasses import replace
 
 import numpy as np
@@ -48,7 +49,8 @@ def _check(L, rows=None, act=None):
     got = out.float().cpu().numpy()
     if rows_t is not None:
         got = got[rows_t.numpy()]
-    return compare(got, ref, act or ("f32" if L.x.dtype == torch.float32 else "bf16"))
+    act = act or ("f32" if L.x.dtype == torch.float32 else "bf16")
+    return compare(got, ref, act, rounded=act != "f32")
 
 
 @pytest.mark.parametrize("T", [1, 48, 131])
