@@ -154,8 +154,12 @@ moe_status_t moe_permute(const moe_config_t* cfg, const int32_t* topk_idx, int32
  *   Limits: T*k <= 262144 and E <= 1023; larger sizes return MOE_ERR_UNSUPPORTED and enqueue
  *   nothing.  There is no status word: an expert index outside [0, E) is skipped (not counted)
  *   and its perm_dst entry is set to -1.
- *   The first call on each device looks up the array's device address (cudaGetSymbolAddress)
- *   with that device current; make that first call before any stream capture.
+ *   Every call made outside stream capture looks up the array's device address
+ *   (cudaGetSymbolAddress) with the current device, so the address stays right after a
+ *   cudaDeviceReset.  A call made during capture uses the address found by the last call outside
+ *   capture on that device: make at least one call on each device before any stream capture
+ *   (otherwise the captured call returns MOE_ERR_CUDA and enqueues nothing).  CUDA errors leave
+ *   their text for moe_last_error_string().
  *   Every call on a device shares the one array: calls whose GPU work overlaps (for example on
  *   two streams at once) race on it and produce wrong results, so serialise them. */
 moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_idx,

@@ -195,6 +195,10 @@ cudaError_t launch_latent_combine(const void* y_perm, const int32_t* perm_dst,
                                   const float* weight, int64_t T, int k, int L, int norm,
                                   float eps, void* u_hat, int num_sms, cudaStream_t st);
 
+// A failed CUDA call as a status: MOE_OK for cudaSuccess, else MOE_ERR_CUDA with the error's name
+// and text kept for moe_last_error_string() (per host thread).
+moe_status_t status_from_cuda(cudaError_t e);
+
 // Brackets one kernel launch: counts it (per host thread) and, while profiling is enabled
 // (moe_profile_enable), records a CUDA event pair around it on the launch stream.
 class LaunchScope {

@@ -226,6 +226,8 @@ static moe_status_t from_cuda(cudaError_t e) {
   return MOE_ERR_CUDA;
 }
 
+moe_status_t status_from_cuda(cudaError_t e) { return from_cuda(e); }
+
 template <typename T>
 static T* at(void* ws, size_t off) {
   return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);

@@ -26,9 +26,13 @@ constexpr int kMaxDevices = 64;
 // The scratch: chunk counts [chunks][E], 1 MiB.
 static __device__ __align__(256) int32_t g_permute_scratch[kNoAllocMaxChunks * kNoAllocMaxExperts];
 
-// Device address of g_permute_scratch, looked up once per device with that device current.  In
-// host code the array's name is only a host-side stand-in, never a device address.
-static int32_t* scratch_for_current_device(cudaError_t* err) {
+// Device address of g_permute_scratch for the current device.  In host code the array's name is
+// only a host-side stand-in, never a device address, so the address is asked of the runtime with
+// that device current.  It is looked up again on every call made outside stream capture (a
+// cudaDeviceReset reloads the module, and the array may then sit elsewhere); during capture the
+// address found by the last call outside capture on that device is used, since a lookup may have
+// to load the module, which capture does not allow.
+static int32_t* scratch_for_current_device(cudaStream_t st, cudaError_t* err) {
   static std::mutex mu;
   static int32_t* ptr[kMaxDevices] = {nullptr};
   int dev = 0;
@@ -38,12 +42,18 @@ static int32_t* scratch_for_current_device(cudaError_t* err) {
     *err = cudaErrorInvalidDevice;
     return nullptr;
   }
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  *err = cudaStreamIsCapturing(st, &cap);
+  if (*err != cudaSuccess) return nullptr;
   std::lock_guard<std::mutex> lk(mu);
-  if (!ptr[dev]) {
+  if (cap == cudaStreamCaptureStatusNone) {
     void* p = nullptr;
     *err = cudaGetSymbolAddress(&p, g_permute_scratch);
     if (*err != cudaSuccess) return nullptr;
     ptr[dev] = static_cast<int32_t*>(p);
+  } else if (!ptr[dev]) {
+    *err = cudaErrorStreamCaptureUnsupported;  // no call outside capture on this device yet
+    return nullptr;
   }
   return ptr[dev];
 }
@@ -63,13 +73,14 @@ extern "C" moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const int32
     return MOE_ERR_UNSUPPORTED;
   if (cfg->T == 0) return MOE_OK;
   if (!topk_idx || !counts || !offsets || !perm_src || !perm_dst) return MOE_ERR_INVALID_ARG;
-  cudaError_t e;
-  int32_t* scratch = scratch_for_current_device(&e);
-  if (!scratch) return MOE_ERR_CUDA;
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  int32_t* scratch = scratch_for_current_device(st, &e);
+  if (!scratch) return status_from_cuda(e);
   (void)cudaGetLastError();
   // No status word: an expert index outside [0, E) is skipped (not counted) and its perm_dst
   // entry is set to -1.
   e = launch_permute(topk_idx, cfg->T, cfg->k, cfg->E, cfg->n_shared, scratch, counts, offsets,
-                     perm_src, perm_dst, nullptr, static_cast<cudaStream_t>(stream));
-  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+                     perm_src, perm_dst, nullptr, st);
+  return status_from_cuda(e);
 }

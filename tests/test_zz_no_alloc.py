@@ -44,6 +44,45 @@ def test_noalloc_permute_matches_workspace_permute(cuda_device, T, E, k):
         assert int(got[0][:E].sum()) == T * k
 
 
+def _compare(cfg, ws, idx, T, E, k, what):
+    ref = _outputs(T, E, k)
+    got = _outputs(T, E, k)
+    B.moe_permute(cfg, idx, *ref, ws)
+    B.moe_permute_noalloc(cfg, idx, *got)
+    torch.cuda.synchronize()
+    for name, a, b in zip(("counts", "offsets", "perm_src", "perm_dst"), ref, got):
+        assert torch.equal(a, b), f"{what}: {name} differs"
+    return got
+
+
+def test_noalloc_permute_after_a_larger_expert_count(cuda_device):
+    """The shared array holds [chunks][E] counts, so its row stride follows E.  A call with many
+    chunks and E = 1000 leaves counts at that stride; the next call, with fewer experts (E = 40,
+    another stride) and a ragged last chunk, must not read any of them."""
+    for T, E, k, seed in ((24000, 1000, 8, 31), (5000, 40, 6, 32), (1500, 7, 3, 33)):
+        cfg = B.make_config(T=T, d=256, E=E, k=k, I=128)  # small widths: a small workspace
+        ws = B.alloc_workspace(cfg)
+        got = _compare(cfg, ws, _routing(T, E, k, seed), T, E, k, f"T={T} E={E}")
+        assert int(got[0][:E].sum()) == T * k
+
+
+@pytest.mark.parametrize("T", [100, 3000])
+def test_noalloc_permute_skips_out_of_range_ids(cuda_device, T):
+    """Expert ids outside [0, E) are not counted and their perm_dst entries are -1, exactly as
+    moe_permute leaves them (one CTA up to 1024 pairs, the chunked kernels above)."""
+    E, k = 64, 4
+    cfg = B.make_config(T=T, d=256, E=E, k=k, I=128)
+    ws = B.alloc_workspace(cfg)
+    idx = _routing(T, E, k, 40 + T)
+    bad = [(3, 1, E), (T // 2, 0, -1), (T - 1, 3, E + 77)]
+    for t, j, v in bad:
+        idx[t, j] = v
+    got = _compare(cfg, ws, idx, T, E, k, f"T={T} with out-of-range ids")
+    assert int(got[0][:E].sum()) == T * k - len(bad)
+    for t, j, _ in bad:
+        assert int(got[3][t * k + j]) == -1
+
+
 def test_noalloc_permute_refuses_sizes_beyond_its_scratch(cuda_device):
     too_many_pairs = B.make_config(T=262144 // 8 + 1, d=7168, E=384, k=8, I=2048)
     out = _outputs(1, 384, 8)
