@@ -61,6 +61,7 @@ struct TcParams {
   uint32_t* err;
   uint64_t wait_ns;     // limit of every mbarrier wait
   int32_t test_stall;   // test hook: the producer issues no copy, so the MMA's wait expires
+  int32_t dense_band;   // the dense group's tiles in bands of this many row tiles (0: one band)
 };
 
 template <bool kSwap, int kBN, int kEpi>
@@ -187,7 +188,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
-                                        p.dense_rows, p.dense_act_row0, S::RPT);
+                                        p.dense_rows, p.dense_act_row0, S::RPT, p.dense_band);
         const CUtensorMap* ma = ti.dense ? &p.map_act_d : &p.map_act;
         const CUtensorMap* mw = ti.dense ? &p.map_w_d : &p.map_w;
         const int act_y = ti.grp_row0 + ti.rt * S::RPT;
@@ -250,7 +251,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
-                                        p.dense_rows, p.dense_act_row0, S::RPT);
+                                        p.dense_rows, p.dense_act_row0, S::RPT, p.dense_band);
         const int nkb = ti.dense ? nkb_d : nkb_r;
         // swap-AB tiles: the MMA's N is the tile's token count rounded up to 16, so a group's
         // last, partial tile costs only the tokens it holds
@@ -308,7 +309,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
       const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
-                                      p.dense_rows, p.dense_act_row0, S::RPT);
+                                      p.dense_rows, p.dense_act_row0, S::RPT, p.dense_band);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err, p.wait_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -660,6 +661,23 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
   p.addend = (const float*)g.addend;
   p.ld_add = g.ld_add;
   p.err = g.err;
+  // Tile order of the dense group.  Activations that fit in L2 are re-read from there by every
+  // feature tile (one band: the weights stream once).  Larger activations with weights that fit in
+  // L2 stream once, row tile by row tile (the K3 down-projection: 117 MB of x, 51 MB of W_down;
+  // the prefill shared expert: 235 MB of x, 58 MB of W1|W3).  When neither fits, bands of 16 row
+  // tiles: the CTAs running at once then share 16 activation row tiles and about 152 / 16 weight
+  // tiles, near the fewest distinct bytes in flight for 128 x 256 tiles.
+  if (g.dense_rows > 0) {
+    const int64_t act_bytes = (int64_t)g.dense_rows * K_d * 2;
+    const int64_t w_bytes = (int64_t)p.F_d * (g.epi == EPI_SWIGLU ? 2 : 1) * K_d * 2;
+    const int64_t l2_share = 48ll << 20;
+    if (swap || act_bytes <= l2_share)
+      p.dense_band = 0;
+    else if (w_bytes <= 64ll << 20)
+      p.dense_band = 1;
+    else
+      p.dense_band = 16;
+  }
   p.test_stall = g.test_stall ? 1 : 0;
   p.wait_ns = g.test_stall ? 50000000ull : kWaitLimitNs;
   const int grid = num_sms;

@@ -5,7 +5,11 @@
 // dense GEMM) has dense_rows rows.  Every group is cut into row tiles of RPT rows and feature tiles
 // of FPT output features; a group's tiles are numbered feature-tile-major, row-tile-minor, so that
 // consecutive tile numbers (run at the same time by neighbouring CTAs) share one weight tile and
-// the weights stream from HBM once.
+// the weights stream from HBM once.  The dense group may instead be numbered in bands of
+// `dense_band` row tiles, feature-tile-major inside a band: a projection of every token of a large
+// batch has more activation bytes than fit in L2, and with bands the running CTAs share both a few
+// activation row tiles and a few weight tiles (a band of one row tile is row-tile-major order: the
+// activations stream from HBM once and a weight matrix that fits in L2 is re-read from there).
 #pragma once
 
 #include <stdint.h>
@@ -76,7 +80,7 @@ __device__ __forceinline__ void build_tile_table(int* tile_start, int* row_start
 __device__ __forceinline__ TileInfo decode_tile(int tile, const int* tile_start,
                                                 const int* row_start, const int32_t* offsets,
                                                 int n_routed, int dense_rows, int dense_row0,
-                                                int rpt) {
+                                                int rpt, int dense_band = 0) {
   const int G = n_routed + (dense_rows > 0 ? 1 : 0);
   int lo = 0, hi = G - 1;  // largest g with tile_start[g] <= tile (empty groups share starts)
   while (lo < hi) {
@@ -98,8 +102,17 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const int* tile_start,
   }
   const int nrt = (ti.rows + rpt - 1) / rpt;
   const int local = tile - tile_start[lo];
-  ti.ft = local / nrt;
-  ti.rt = local - ti.ft * nrt;
+  if (ti.dense && dense_band > 0 && dense_band < nrt) {
+    const int nft = (tile_start[G] - tile_start[lo]) / nrt;  // the dense group is the last
+    const int band = local / (dense_band * nft);
+    const int rem = local - band * dense_band * nft;
+    const int in_band = min(dense_band, nrt - band * dense_band);  // the last band may be short
+    ti.ft = rem / in_band;
+    ti.rt = band * dense_band + (rem - ti.ft * in_band);
+  } else {
+    ti.ft = local / nrt;
+    ti.rt = local - ti.ft * nrt;
+  }
   ti.valid = min(rpt, ti.rows - ti.rt * rpt);
   return ti;
 }
