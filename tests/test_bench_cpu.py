@@ -83,3 +83,55 @@ def test_algorithmic_bytes_count_each_touched_expert_once():
     byq = bench.touched_bytes(wq, idx)
     assert 3 * I * d * 4.0 / (128 * 128) == 2688 * 4
     assert byq["layer"] == (8 + 1) * (44_040_192 + 2688 * 4) + E * d * 4 + 2 * T * d * 2
+
+
+def test_traffic_ratio_is_refused_once_its_sources_change(tmp_path, monkeypatch):
+    """A traffic ratio belongs to the kernel source it was measured on: with the current digests
+    it is used, with any other digest it is dropped (traffic null)."""
+    import bench
+    srcs = ["csrc/gemm_tc.cu", "csrc/common.cuh"]
+    good = bench.source_digest(srcs)
+    stale = dict(good, **{"csrc/common.cuh": "0" * 64})
+    f = tmp_path / "traffic.json"
+    f.write_text(json.dumps({"entries": [
+        {"kernel": "gemm13_swiglu_rows", "ratio": 1.05, "capture": "a test case", "sources": good},
+        {"kernel": "gemm2_rows", "ratio": 0.98, "capture": "a test case", "sources": stale}]}))
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    assert bench.traffic_ratio("gemm13_swiglu_rows", False)[0] == 1.05
+    assert bench.traffic_ratio("gemm13_swiglu_rows", True)[0] is None  # no latent capture
+    r, note = bench.traffic_ratio("gemm2_rows", False)
+    assert r is None and "changed" in note
+    assert bench.traffic_ratio("gemm13_swiglu_swap", False)[0] is None
+
+
+def test_default_run_is_the_prefill_layer_with_the_other_configurations(monkeypatch):
+    import bench
+    monkeypatch.setattr(sys, "argv", ["bench.py"])
+    a = bench.parse_args()
+    assert a.workload == "k2_prefill_bf16" and a.others
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--workload", "k2_decode_bf16"])
+    a = bench.parse_args()
+    assert a.workload == "k2_decode_bf16" and not a.others
+    names = [n for n, _, _ in bench.OTHER_WORKLOADS]
+    assert set(names) == {"k2_decode_bf16", "k3_latent_bf16", "k2_fp8", "k2_int4_decode"}
+
+
+def test_oracle_check_reports_plain_and_beyond_rounding_errors():
+    """On a tiny bf16 layer (CPU), an 'output' that is the oracle's own result rounded to bf16 has
+    a plain error of up to half a bf16 ulp and nothing beyond its rounding."""
+    from dataclasses import replace
+    import numpy as np
+    import torch
+    import bench
+    from oracle import torch_bridge as OB
+    from mixture_experts_ffn_gemm_gb300 import synthetic as S
+    w = replace(S.WORKLOADS["tiny_fp32"], name="tiny_bf16", act="bf16", T=40)
+    layer = S.make_layer(w, seed=3, device="cpu")
+    ref = OB.forward(layer)
+    out = torch.tensor(ref["out"], dtype=torch.float32).to(torch.bfloat16)
+    rows = torch.arange(0, 40, 3)
+    chk = bench.oracle_check(layer, out, rows, 2)
+    assert chk["tokens"] == len(rows) and chk["compared"] + chk["near_tie_tokens"] == len(rows)
+    assert chk["max_err_rms_beyond_rounding"] <= 1e-9
+    assert 0 < chk["max_err_rms"] <= 2.0 ** -8 * np.abs(ref["out"]).max() / np.sqrt(
+        np.mean(ref["out"][rows.numpy()] ** 2))
