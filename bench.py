@@ -195,6 +195,10 @@ def touched_bytes(w, idx: np.ndarray) -> dict:
         + (P + rows_sh) * de * 4,
         "layer": len(touched) * (w13 + w2) + sh13 + sh2 + lat + w.E * w.d * 4
         + 2 * T * w.d * ab,
+        # both expert GEMMs in one launch: h stays inside it (written and read back on chip or
+        # through L2), so only the weights, the activations in and the fp32 outputs count
+        "experts_fused": len(touched) * (w13 + w2) + (0 if w.d_latent else sh13 + sh2)
+        + P * de * hb + rows_sh * w.d * hb + (P + rows_sh) * de * 4,
     }
 
 
@@ -210,6 +214,7 @@ def flops(w, T: int) -> dict:
     }
     f["layer"] = (2 * T * w.d * w.E + P * 6 * de * w.I + T * w.n_shared * 6 * w.d * w.I_shared
                   + (4 * T * w.d * w.d_latent if w.d_latent else 0))
+    f["experts_fused"] = f["gemm13"] + f["gemm2"]
     return f
 
 
@@ -370,7 +375,8 @@ def rooflines(w, idx_np, prof, ms_step) -> tuple:
     roof = None
     if dom is not None:
         ms_launch = kernels[dom]["ms_per_launch"]
-        unit_key = "gemm2" if dom.startswith("gemm2") else "gemm13"
+        unit_key = ("gemm2" if dom.startswith("gemm2") else
+                    "experts_fused" if dom.startswith("experts_fused") else "gemm13")
         # the kernel's bound: the larger of its algorithmic time at tensor peak and at HBM peak
         t_tc_k = fl.get(unit_key, 0) / (tc_peak * 1e12)
         t_hbm_k = by[unit_key] / (peaks["hbm_gbs"] * 1e9)
@@ -396,7 +402,9 @@ def rooflines(w, idx_np, prof, ms_step) -> tuple:
                   "frac_of_sustained_peak": 1000 * max(fl["layer"] / (tc_sus * 1e12), t_hbm)
                   / ms_step, "tensor_peak_tflops": tc_peak, "hbm_peak_gbs": peaks["hbm_gbs"],
                   "algorithmic_bytes": by["layer"], "algorithmic_flops": fl["layer"],
-                  "touched_experts": by["touched_experts"]}
+                  "touched_experts": by["touched_experts"],
+                  "kernel_algorithmic_bytes": {k: by[k] for k in ("gemm13", "gemm2",
+                                                                  "experts_fused")}}
     return roof, layer_roof, kernels
 
 

@@ -83,6 +83,13 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2, MOE_INT4 = 3 } moe_d
 #define MOE_FLAG_ROUTER_TC 0x8u       /* force the tensor-core (3 x bf16 split) router GEMM      */
 #define MOE_FLAG_GEMM_N128 0x10u      /* token-rows tiles of the store GEMMs with N = 128 columns  */
 #define MOE_FLAG_GEMM_SWAP_WIDE 0x20u /* force weight-rows-as-M tiles of 256 tokens (runtime N)  */
+#define MOE_FLAG_GEMM_M1 0x40u        /* token-rows SwiGLU tiles of one 128-row M half            */
+#define MOE_FLAG_GEMM_M2 0x80u        /* token-rows SwiGLU tiles of two 128-row M halves (256 rows)
+                                       * sharing each weight K-block (slower: kept for comparison) */
+#define MOE_FLAG_DECODE_FUSED 0x200u  /* decode batches (32-token swap-AB tiles): the expert
+                                       * GEMMs in one persistent launch (W1|W3 + SwiGLU tiles,
+                                       * then W2 tiles that wait for their h rows) instead of two
+                                       * launches; same results bit for bit, measured slower      */
 /* Test hook for the failure path: the tensor-core W1|W3 expert GEMM's copy producer issues no
  * copy, so its MMA issuer's bounded wait (shortened to 50 ms under this flag) expires; the kernel
  * flags MOE_ERR_TIMEOUT in the device status, drains, frees its tensor memory and returns, and

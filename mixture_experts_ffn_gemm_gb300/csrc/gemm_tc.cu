@@ -19,6 +19,12 @@
 //   rows  (swap = 0): MMA M = 128 token rows, N = 256 weight rows.  SwiGLU tiles load 128 W1 rows and
 //                     the matching 128 W3 rows, so each thread (= one token row) holds g and u of the
 //                     same features in its own TMEM lane and the epilogue needs no exchange.
+//                     With two M halves (kMH = 2) a tile is 256 token rows: two M = 128 MMAs share
+//                     each staged weight K-block, so a CTA copies 64 KB per 1024 MMA cycles instead
+//                     of 48 KB per 512, and three 64 KB stages hide about 3000 cycles of copy
+//                     latency.  A tile whose rows end within its first half issues only that half
+//                     (the padding stays at 128 rows).  The two halves fill all 512 TMEM columns,
+//                     so the epilogue of a tile no longer overlaps the next tile's mainloop.
 //   swap  (swap = 1): MMA M = 128 weight rows, N = 32 tokens, for groups with few rows (decode):
 //                     the weights stream once per 32 tokens instead of once per 128-row tile padded
 //                     with empty rows.  SwiGLU keeps a W1 accumulator and a W3 accumulator.
@@ -64,18 +70,21 @@ struct TcParams {
   int32_t dense_band;   // the dense group's tiles in bands of this many row tiles (0: one band)
 };
 
-template <bool kSwap, int kBN, int kEpi>
+template <bool kSwap, int kBN, int kEpi, int kMH = 1>
 struct TcShape {
+  static_assert(kMH == 1 || (kMH == 2 && !kSwap && kBN == 256), "two M halves: token rows, N = 256");
   static constexpr bool kSwiGLU = kEpi == EPI_SWIGLU;
   // 256-token swap-AB SwiGLU tiles stack 64 W1 rows over the matching 64 W3 rows in one M = 128
   // operand, so that one 256-column accumulator holds both and two of them fit in TMEM
   static constexpr bool kStack = kSwap && kSwiGLU && kBN == 256;
-  static constexpr int RPT = kSwap ? kBN : 128;                         // token rows per tile
+  static constexpr int RPT = kSwap ? kBN : 128 * kMH;                   // token rows per tile
   static constexpr int FPT = kSwap ? (kStack ? 64 : 128) : (kSwiGLU ? kBN / 2 : kBN);  // features
-  static constexpr int OPA = (kSwap && kSwiGLU && !kStack) ? 2 * kBoxBytes : kBoxBytes;  // A / stage
+  static constexpr int OPA =
+      (kSwap && kSwiGLU && !kStack) ? 2 * kBoxBytes : kMH * kBoxBytes;  // A bytes / stage
   static constexpr int OPB = kBN * 128;                                       // B bytes / stage
   static constexpr int STAGE = OPA + OPB;
-  static constexpr int ACC_COLS = (kSwap && kSwiGLU && !kStack) ? 2 * kBN : kBN;  // fp32 columns
+  static constexpr int ACC_COLS =
+      (kSwap && kSwiGLU && !kStack) ? 2 * kBN : kMH * kBN;  // fp32 columns of one accumulator
   // two accumulators (the epilogue of tile i overlaps the mainloop of tile i+1) when they fit
   static constexpr int NACC = 2 * ACC_COLS <= 512 ? 2 : 1;
   static constexpr int TMEM_NEED = NACC * ACC_COLS;
@@ -121,9 +130,9 @@ __device__ __forceinline__ void store_rows_128B(uint8_t* buf, int lane, const ui
   }
 }
 
-template <bool kSwap, int kBN, int kEpi>
+template <bool kSwap, int kBN, int kEpi, int kMH = 1>
 __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid_constant__ TcParams p) {
-  using S = TcShape<kSwap, kBN, kEpi>;
+  using S = TcShape<kSwap, kBN, kEpi, kMH>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -196,6 +205,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
         const int u_off = ti.dense ? p.u_off_d : p.u_off;
         const int nkb = ti.dense ? nkb_d : nkb_r;
         const int kwrap = ti.dense ? p.k_wrap_d : p.k_wrap;
+        // the second M half's rows are copied only when the tile has rows there
+        const bool half1 = kMH == 2 && ti.valid > 128;
+        const uint32_t tx = (kMH == 2 && !half1) ? S::STAGE - kBoxBytes : S::STAGE;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, p.wait_ns)) {
             ok = false;
@@ -203,11 +215,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
           }
           uint8_t* sa = smem + stage * S::STAGE;
           uint8_t* sb = sa + S::OPA;
-          mbar_arrive_expect_tx(&full[stage], S::STAGE);
+          mbar_arrive_expect_tx(&full[stage], tx);
           const int kx = kb * kBK;
           const int ax = kx % kwrap;
           if (!kSwap) {
             tma_load_2d(sa, ma, &full[stage], ax, act_y);
+            if (half1) tma_load_2d(sa + kBoxBytes, ma, &full[stage], ax, act_y + 128);
             if (S::kSwiGLU) {
               tma_load_2d(sb, mw, &full[stage], kx, w_y);
               tma_load_2d(sb + kBoxBytes, mw, &full[stage], kx, w_y + u_off);
@@ -260,6 +273,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
           const int n = ti.valid >= kBN ? kBN : ((ti.valid + 15) & ~15);
           idesc = idesc_bf16_f32_n(n);
         }
+        const bool half1 = kMH == 2 && ti.valid > 128;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, p.wait_ns)) break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * S::ACC_COLS;
@@ -283,6 +297,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
               continue;
             }
             mma_bf16(d0, sw128_kmajor_desc(sa + k16 * 32), bdesc, idesc, accum);
+            if (half1)  // the second 128 token rows against the same weight K-block
+              mma_bf16(d0 + kBN, sw128_kmajor_desc(sa + kBoxBytes + k16 * 32), bdesc, idesc, accum);
             if (kSwap && S::kSwiGLU && !S::kStack)
               mma_bf16(d0 + kBN, sw128_kmajor_desc(sa + kBoxBytes + k16 * 32), bdesc, idesc,
                        accum);
@@ -324,89 +340,94 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
       const int64_t ldo = ti.dense ? p.ldo_d : p.ldo;
       if (!kSwap && S::kStaged) {
         uint8_t* buf = staging + (warp - 2) * 4096;
-        const int vrows = min(32, max(0, ti.valid - quarter * 32));
-        const int64_t row0 = out_row0 + quarter * 32;
-        if (S::kSwiGLU) {  // h in bf16: chunks of 64 features = 128 bytes per row
 #pragma unroll 1
-          for (int c = 0; c < S::FPT; c += 64) {
-            uint4 v[8];
+        for (int mh = 0; mh < kMH && mh * 128 < ti.valid; ++mh) {
+          const uint32_t th = tmem_base + acc * S::ACC_COLS + mh * kBN +
+                              ((uint32_t)(quarter * 32) << 16);  // this M half's columns
+          const int vrows = min(32, max(0, ti.valid - mh * 128 - quarter * 32));
+          const int64_t row0 = out_row0 + mh * 128 + quarter * 32;
+          if (S::kSwiGLU) {  // h in bf16: chunks of 64 features = 128 bytes per row
+#pragma unroll 1
+            for (int c = 0; c < S::FPT; c += 64) {
+              uint4 v[8];
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              uint32_t g0[16], u0[16], g1[16], u1[16];
-              tmem_ld16(tb + c + 32 * h, g0);
-              tmem_ld16(tb + S::FPT + c + 32 * h, u0);
-              tmem_ld16(tb + c + 32 * h + 16, g1);
-              tmem_ld16(tb + S::FPT + c + 32 * h + 16, u1);
-              tmem_ld_wait();
-              uint32_t pk[16];
+              for (int h = 0; h < 2; ++h) {
+                uint32_t g0[16], u0[16], g1[16], u1[16];
+                tmem_ld16(th + c + 32 * h, g0);
+                tmem_ld16(th + S::FPT + c + 32 * h, u0);
+                tmem_ld16(th + c + 32 * h + 16, g1);
+                tmem_ld16(th + S::FPT + c + 32 * h + 16, u1);
+                tmem_ld_wait();
+                uint32_t pk[16];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                pk[i] = pack_bf16x2(
-                    silu_fast(__uint_as_float(g0[2 * i])) * __uint_as_float(u0[2 * i]),
-                    silu_fast(__uint_as_float(g0[2 * i + 1])) * __uint_as_float(u0[2 * i + 1]));
-                pk[8 + i] = pack_bf16x2(
-                    silu_fast(__uint_as_float(g1[2 * i])) * __uint_as_float(u1[2 * i]),
-                    silu_fast(__uint_as_float(g1[2 * i + 1])) * __uint_as_float(u1[2 * i + 1]));
+                for (int i = 0; i < 8; ++i) {
+                  pk[i] = pack_bf16x2(
+                      silu_fast(__uint_as_float(g0[2 * i])) * __uint_as_float(u0[2 * i]),
+                      silu_fast(__uint_as_float(g0[2 * i + 1])) * __uint_as_float(u0[2 * i + 1]));
+                  pk[8 + i] = pack_bf16x2(
+                      silu_fast(__uint_as_float(g1[2 * i])) * __uint_as_float(u1[2 * i]),
+                      silu_fast(__uint_as_float(g1[2 * i + 1])) * __uint_as_float(u1[2 * i + 1]));
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  v[4 * h + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
               }
-#pragma unroll
-              for (int q = 0; q < 4; ++q)
-                v[4 * h + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+              uint8_t* dst = (uint8_t*)out + (row0 * ldo + (int64_t)ti.ft * S::FPT + c) * 2;
+              store_rows_128B(buf, lane, v, dst, ldo * 2, vrows);
             }
-            uint8_t* dst = (uint8_t*)out + (row0 * ldo + (int64_t)ti.ft * S::FPT + c) * 2;
-            store_rows_128B(buf, lane, v, dst, ldo * 2, vrows);
-          }
-        } else if (p.out_f32) {  // fp32: chunks of 32 columns
+          } else if (p.out_f32) {  // fp32: chunks of 32 columns
 #pragma unroll 1
-          for (int c = 0; c < S::FPT; c += 32) {
-            uint32_t a[16], b[16];
-            tmem_ld16(tb + c, a);
-            tmem_ld16(tb + c + 16, b);
-            tmem_ld_wait();
-            uint4 v[8];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              v[q] = make_uint4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
-              v[4 + q] = make_uint4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
-            }
-            if (p.tma_out && vrows == 32) {
-              // the chunk in the 128-byte swizzled layout; the TMA unswizzles it on the way out
-              if (lane == 0) tma_store_wait_read();  // the previous chunk has left the buffer
-              __syncwarp();
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = v[j];
-              asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-              __syncwarp();
-              if (lane == 0) tma_store_2d_stream(&p.map_out, buf, ti.ft * S::FPT + c, (int)row0);
-            } else {
-              if (p.tma_out && lane == 0) tma_store_wait_read();
-              __syncwarp();
-              uint8_t* dst = (uint8_t*)out + (row0 * ldo + (int64_t)ti.ft * S::FPT + c) * 4;
-              store_rows_128B(buf, lane, v, dst, ldo * 4, vrows);
-            }
-          }
-        } else {  // bf16: chunks of 64 columns
-#pragma unroll 1
-          for (int c = 0; c < S::FPT; c += 64) {
-            uint4 v[8];
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
+            for (int c = 0; c < S::FPT; c += 32) {
               uint32_t a[16], b[16];
-              tmem_ld16(tb + c + 32 * h, a);
-              tmem_ld16(tb + c + 32 * h + 16, b);
+              tmem_ld16(th + c, a);
+              tmem_ld16(th + c + 16, b);
               tmem_ld_wait();
-              uint32_t pk[16];
+              uint4 v[8];
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
-                pk[8 + i] = pack_bf16x2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
+              for (int q = 0; q < 4; ++q) {
+                v[q] = make_uint4(a[4 * q], a[4 * q + 1], a[4 * q + 2], a[4 * q + 3]);
+                v[4 + q] = make_uint4(b[4 * q], b[4 * q + 1], b[4 * q + 2], b[4 * q + 3]);
               }
+              if (p.tma_out && vrows == 32) {
+                // the chunk in the 128-byte swizzled layout; the TMA unswizzles it on the way out
+                if (lane == 0) tma_store_wait_read();  // the previous chunk has left the buffer
+                __syncwarp();
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                v[4 * h + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+                for (int j = 0; j < 8; ++j)
+                  *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = v[j];
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) tma_store_2d_stream(&p.map_out, buf, ti.ft * S::FPT + c, (int)row0);
+              } else {
+                if (p.tma_out && lane == 0) tma_store_wait_read();
+                __syncwarp();
+                uint8_t* dst = (uint8_t*)out + (row0 * ldo + (int64_t)ti.ft * S::FPT + c) * 4;
+                store_rows_128B(buf, lane, v, dst, ldo * 4, vrows);
+              }
             }
-            uint8_t* dst = (uint8_t*)out + (row0 * ldo + (int64_t)ti.ft * S::FPT + c) * 2;
-            store_rows_128B(buf, lane, v, dst, ldo * 2, vrows);
+          } else {  // bf16: chunks of 64 columns
+#pragma unroll 1
+            for (int c = 0; c < S::FPT; c += 64) {
+              uint4 v[8];
+#pragma unroll
+              for (int h = 0; h < 2; ++h) {
+                uint32_t a[16], b[16];
+                tmem_ld16(th + c + 32 * h, a);
+                tmem_ld16(th + c + 32 * h + 16, b);
+                tmem_ld_wait();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  pk[i] = pack_bf16x2(__uint_as_float(a[2 * i]), __uint_as_float(a[2 * i + 1]));
+                  pk[8 + i] = pack_bf16x2(__uint_as_float(b[2 * i]), __uint_as_float(b[2 * i + 1]));
+                }
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                  v[4 * h + q] = make_uint4(pk[4 * q], pk[4 * q + 1], pk[4 * q + 2], pk[4 * q + 3]);
+              }
+              uint8_t* dst = (uint8_t*)out + (row0 * ldo + (int64_t)ti.ft * S::FPT + c) * 2;
+              store_rows_128B(buf, lane, v, dst, ldo * 2, vrows);
+            }
           }
         }
       } else if (!kSwap) {
@@ -534,7 +555,7 @@ static EncodeTiledFn encode_fn() {
 
 // 2D bf16 map over [rows][cols] (cols contiguous), box {64 cols, box_rows rows}, 128-byte swizzle,
 // out-of-range elements read as zero.
-static bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
+bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
                           int box_rows) {
   EncodeTiledFn enc = encode_fn();
   if (!enc || !base || rows <= 0 || cols <= 0) return false;
@@ -561,10 +582,10 @@ static bool make_map_f32_out(CUtensorMap* m, void* base, int64_t rows, int64_t c
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kSwap, int kBN, int kEpi>
+template <bool kSwap, int kBN, int kEpi, int kMH = 1>
 static cudaError_t launch_variant(const TcParams& p, int grid, cudaStream_t st, const char* label) {
-  using S = TcShape<kSwap, kBN, kEpi>;
-  auto kern = moe_gemm_tc_kernel<kSwap, kBN, kEpi>;
+  using S = TcShape<kSwap, kBN, kEpi, kMH>;
+  auto kern = moe_gemm_tc_kernel<kSwap, kBN, kEpi, kMH>;
   static int attr_set_device = -1;  // the attribute is per device; refreshed when it changes
   int dev = 0;
   cudaGetDevice(&dev);
@@ -682,7 +703,12 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
   p.wait_ns = g.test_stall ? 50000000ull : kWaitLimitNs;
   const int grid = num_sms;
   if (!swap) {
-    if (g.epi == EPI_SWIGLU) return launch_variant<false, 256, EPI_SWIGLU>(p, grid, st, g.label);
+    if (g.epi == EPI_SWIGLU) {
+      // two M halves per tile only on request: measured slower at prefill (gemm13 6.6 -> 8.1 ms)
+      // and K3 (2.4 -> 3.1 ms), the SwiGLU epilogue no longer hidden behind the next mainloop
+      if (g.m_halves == 2) return launch_variant<false, 256, EPI_SWIGLU, 2>(p, grid, st, g.label);
+      return launch_variant<false, 256, EPI_SWIGLU>(p, grid, st, g.label);
+    }
     if (f32_router && g.F % 384 == 0) return launch_variant<false, 384, EPI_STORE>(p, grid, st, g.label);
     if (f32_router || (g.n128 && g.epi == EPI_STORE))
       return launch_variant<false, 128, EPI_STORE>(p, grid, st, g.label);

@@ -67,6 +67,7 @@ struct GroupedGemm {
   const char* label = "gemm";  // kernel name for the launch profiler
   bool test_stall = false;     // test hook (MOE_FLAG_TEST_STALL_EXPERTS): see moe.h
   bool n128 = false;           // token-rows store tiles with N = 128 (MOE_FLAG_GEMM_N128)
+  int m_halves = 0;            // token-rows SwiGLU tiles of 1 or 2 M halves (0: one)
 };
 
 // Tensor-core grouped GEMM (tcgen05 + TMA), bf16 operands, fp32 accumulation in TMEM.
@@ -78,6 +79,38 @@ struct GroupedGemm {
 // cudaErrorInvalidValue when the shapes are not supported (nothing launched).
 cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStream_t st);
 bool gemm_tc_supported(const GroupedGemm& g, int swap);
+// A TMA map over a bf16 [rows][cols] matrix (cols contiguous): box {64 cols, box_rows rows},
+// 128-byte swizzle, out-of-range elements read as zero.  False when the driver refuses it.
+bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols, int box_rows);
+
+// The decode experts in one persistent launch (bf16, 32-token swap-AB tiles): W1|W3 + SwiGLU into
+// h, then W2 into the fp32 expert outputs, each W2 tile starting once the h tiles of its rows are
+// written.  Routed groups by offsets plus the shared expert as a trailing dense group of T rows.
+//   x_perm [P][d], x [T][d], W13 [E][2I][d], Ws13 [2I][d], W2 [E][d][I], Ws2 [d][I],
+//   h [P+T][I] (out, then in), y [P+T][d] fp32 (out), ready [fused_ready_count(T, k, E)] zeroed.
+// Needs d % 128 == 0, I % 128 == 0 and a cooperative launch of one CTA per SM (the W2 tiles wait
+// on W1|W3 tiles of other CTAs); returns cudaErrorCooperativeLaunchTooLarge when that is refused.
+struct FusedDecode {
+  const void* x_perm = nullptr;
+  const void* x = nullptr;
+  const void* W13 = nullptr;
+  const void* Ws13 = nullptr;
+  const void* W2 = nullptr;
+  const void* Ws2 = nullptr;
+  const int32_t* offsets = nullptr;
+  int n_routed = 0;
+  int64_t T = 0;   // tokens (the shared expert's rows; 0 without a shared expert)
+  int64_t P = 0;   // routed rows (T * k)
+  int d = 0;
+  int I = 0;
+  void* h = nullptr;
+  float* y = nullptr;
+  uint32_t* ready = nullptr;
+  uint32_t* err = nullptr;
+  const char* label = "experts_fused_swap";
+};
+int64_t fused_ready_count(int64_t T, int k, int E);
+cudaError_t launch_decode_fused(const FusedDecode& f, int num_sms, cudaStream_t st);
 
 // Grouped GEMM with e4m3 operands and fp32 block scales (tcgen05 kind::f8f6f4), token-rows tiles
 // M = 128 x 256 weight rows.  Activation scales per row per 128 channels, stored [K/128][ld];

@@ -90,11 +90,13 @@ struct Plan {
   bool tc;            // tensor-core expert GEMMs
   bool fp8;           // e4m3 experts with block scales
   bool w4;            // 4-bit integer group-quantised experts
+  bool fused;         // decode experts in one persistent launch (32-token swap-AB tiles)
 };
 
 struct Layout {
   size_t status, zbuf, wsplit, idx, weight, chunk_counts, counts, offsets, perm_src, perm_dst,
       x_lat, x_perm, h, y_perm, u_hat, x_io, out_io;
+  size_t ready;       // fused decode experts: W1|W3 tiles done per row tile
   size_t xq, xq_s, xpq, xpq_s, hq, hq_s;  // fp8 experts: e4m3 activations + [K/128][rows] scales
   size_t total;
 };
@@ -176,6 +178,10 @@ static Plan make_plan(const moe_config_t* c) {
     p.swap = 0;
   else
     p.swap = c->T <= 512 ? 1 : 0;
+  // the one-launch decode experts on request only: measured slower than the two launches
+  p.fused = p.tc && !p.fp8 && !p.w4 && !p.latent && p.swap == 1 &&
+            (c->flags & MOE_FLAG_DECODE_FUSED) && !(c->flags & MOE_FLAG_TEST_STALL_EXPERTS) &&
+            c->I % 128 == 0;
   return p;
 }
 
@@ -210,6 +216,7 @@ static Layout make_layout(const moe_config_t* c, const Plan& pl) {
   L.hq = take(pl.fp8 ? (size_t)(P + shared_rows) * I : 0);
   L.hq_s = take(pl.fp8 ? (size_t)(I / 128) * (P + shared_rows) * 4 : 0);
   L.y_perm = take(((size_t)P * pl.de + (size_t)shared_rows * d) * 4);  // fp32 expert outputs
+  L.ready = take(pl.fused ? (size_t)fused_ready_count(T, c->k, E) * 4 : 0);
   L.u_hat = take(pl.latent ? (size_t)T * c->d_latent * 2 : 0);
   L.x_io = take((size_t)T * d * ab);
   L.out_io = take((size_t)T * d * ab);
@@ -535,6 +542,32 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
   e = launch_gather_rows(route_src, perm_src, P, c->k, de, (int)ab, x_perm, x.sms, x.st);
   if (e != cudaSuccess) return from_cuda(e);
 
+  if (x.pl.fused) {  // decode: both expert GEMMs in one persistent launch
+    uint32_t* ready = at<uint32_t>(x.ws, x.L.ready);
+    e = cudaMemsetAsync(ready, 0, (size_t)fused_ready_count(T, c->k, E) * 4, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+    FusedDecode f;
+    f.x_perm = x_perm;
+    f.x = xin;
+    f.W13 = W13;
+    f.Ws13 = Ws13;
+    f.W2 = W2;
+    f.Ws2 = Ws2;
+    f.offsets = offsets;
+    f.n_routed = E;
+    f.T = c->n_shared ? T : 0;
+    f.P = P;
+    f.d = d;
+    f.I = I;
+    f.h = h;
+    f.y = static_cast<float*>(y_perm);
+    f.ready = ready;
+    f.err = x.err;
+    e = launch_decode_fused(f, x.sms, x.st);
+    if (e != cudaErrorCooperativeLaunchTooLarge) return from_cuda(e);
+    (void)cudaGetLastError();  // not every SM free for a cooperative launch: two launches instead
+  }
+
   // W1 | W3 with the SwiGLU epilogue -> h [P + T][I]; the shared expert is the trailing dense
   // group of the same launch (on the K3 path with its own reduction length d, since it reads the
   // full-width x while the routed experts read the latent)
@@ -570,6 +603,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.out_dtype = c->act_dtype;
     g.err = x.err;
     g.test_stall = (c->flags & MOE_FLAG_TEST_STALL_EXPERTS) != 0;
+    g.m_halves = (c->flags & MOE_FLAG_GEMM_M1) ? 1 : (c->flags & MOE_FLAG_GEMM_M2) ? 2 : 0;
     e = gemm(x, g, "gemm13_swiglu_rows", "gemm13_swiglu_swap", "gemm13_swiglu_swap256",
              "gemm13_swiglu_simt");
     if (e != cudaSuccess) return from_cuda(e);

@@ -41,9 +41,11 @@ def _mlp(x: np.ndarray, W13: np.ndarray, W2: np.ndarray, I: int, round_h: bool) 
 
 
 def ideal_forward(layer, rows=None, round_h=True, round_out=True, round_xlat=True,
-                  round_uhat=True) -> dict:
+                  round_uhat=True, round_y=False) -> dict:
     """The layer on ``rows`` (all by default) with only the listed bf16 roundings; returns the
-    output and the oracle's routing it used."""
+    output and the oracle's routing it used.  ``round_y`` also rounds every expert's output
+    E_i(x) (and the shared expert's) to bf16 before the gate-weighted sum, as a pipeline that
+    keeps its expert outputs in bf16 does."""
     w = layer.w
     T = layer.x.shape[0]
     rows = np.arange(T) if rows is None else np.asarray(rows)
@@ -59,10 +61,10 @@ def ideal_forward(layer, rows=None, round_h=True, round_out=True, round_xlat=Tru
     y = np.zeros((len(rows), w.d_expert), np.float64)
     for e in np.unique(rt["idx"]):
         t, j = np.nonzero(rt["idx"] == e)
-        ye = _mlp(x_e[t], _f64(layer.W13[e]), _f64(layer.W2[e]), w.I, round_h)
+        ye = _rn(_mlp(x_e[t], _f64(layer.W13[e]), _f64(layer.W2[e]), w.I, round_h), round_y)
         y[t] += rt["gates"][t, j][:, None] * ye
-    shared = (_mlp(x, _f64(layer.Ws13), _f64(layer.Ws2), w.I_shared, round_h) if w.n_shared
-              else np.zeros((len(rows), w.d)))
+    shared = (_rn(_mlp(x, _f64(layer.Ws13), _f64(layer.Ws2), w.I_shared, round_h), round_y)
+              if w.n_shared else np.zeros((len(rows), w.d)))
     if w.d_latent:
         if w.latent_norm:
             y = y / np.sqrt(np.mean(y * y, axis=1, keepdims=True) + w.rms_eps)

@@ -135,3 +135,18 @@ def test_oracle_check_reports_plain_and_beyond_rounding_errors():
     assert chk["max_err_rms_beyond_rounding"] <= 1e-9
     assert 0 < chk["max_err_rms"] <= 2.0 ** -8 * np.abs(ref["out"]).max() / np.sqrt(
         np.mean(ref["out"][rows.numpy()] ** 2))
+
+
+def test_fused_decode_work_is_both_expert_gemms_without_h():
+    """The persistent decode launch is credited with both expert GEMMs' FLOPs and with their
+    bytes less h, which never leaves the launch: gemm13 + gemm2 - 2 (T k + T) I * 2 bytes."""
+    import numpy as np
+    import bench
+    from mixture_experts_ffn_gemm_gb300 import synthetic as S
+    w = S.WORKLOADS["k2_decode_bf16"]
+    T, I = 128, 2048
+    idx = (np.arange(T * 8, dtype=np.int32) % 300).reshape(T, 8)
+    by = bench.touched_bytes(w, idx)
+    assert by["experts_fused"] == by["gemm13"] + by["gemm2"] - 2 * (T * 8 + T) * I * 2
+    f = bench.flops(w, T)
+    assert f["experts_fused"] == f["gemm13"] + f["gemm2"]

@@ -22,6 +22,10 @@ pytestmark = pytest.mark.gpu
 ROWS = B.MOE_FLAG_GEMM_ROWS_MAJOR
 SWAP = B.MOE_FLAG_GEMM_SWAP_AB
 WIDE = B.MOE_FLAG_GEMM_SWAP_WIDE  # 256-token swap-AB tiles with a run-time MMA N
+ROWS2 = B.MOE_FLAG_GEMM_ROWS_MAJOR | B.MOE_FLAG_GEMM_M2  # 256-row tiles of two M halves
+FUSED = SWAP | B.MOE_FLAG_DECODE_FUSED  # decode expert GEMMs in one persistent launch
+VARIANTS = [ROWS, ROWS2, SWAP, FUSED, WIDE]
+VARIANT_IDS = ["rows", "rows_m2", "swap", "swap_fused", "wide"]
 
 
 def _lib():
@@ -76,12 +80,12 @@ def test_zero_tokens_is_a_no_op(cuda_device):
 SMALL_BF16 = replace(S.WORKLOADS["tiny_fp32"], name="small_bf16", act="bf16", T=300)
 
 
-@pytest.mark.parametrize("flags", [ROWS, SWAP, WIDE], ids=["rows", "swap", "wide"])
+@pytest.mark.parametrize("flags", VARIANTS, ids=VARIANT_IDS)
 def test_bf16_small_all_tokens(cuda_device, flags):
     _full_check(_layer(SMALL_BF16, seed=1), flags)
 
 
-@pytest.mark.parametrize("flags", [ROWS, SWAP, WIDE], ids=["rows", "swap", "wide"])
+@pytest.mark.parametrize("flags", VARIANTS, ids=VARIANT_IDS)
 def test_bf16_one_expert_takes_every_token(cuda_device, flags):
     """k = 1 and a bias that forces expert 5: one group of T rows, every other group empty.
 
@@ -98,11 +102,38 @@ def test_bf16_one_expert_takes_every_token(cuda_device, flags):
     print(_full_check(layer, flags, expert_rows=64))
 
 
-@pytest.mark.parametrize("flags", [ROWS, SWAP, WIDE], ids=["rows", "swap", "wide"])
+@pytest.mark.parametrize("flags", VARIANTS, ids=VARIANT_IDS)
 def test_bf16_every_expert_selected(cuda_device, flags):
     """k == E: every token visits every expert."""
     w = replace(SMALL_BF16, E=4, k=4, T=130)
     _full_check(_layer(w, seed=3), flags)
+
+
+@pytest.mark.parametrize("flags", [SWAP, FUSED], ids=["two_launches", "fused"])
+def test_bf16_decode_without_shared_expert(cuda_device, flags):
+    """n_shared = 0: the decode expert launches with no trailing dense group."""
+    w = replace(SMALL_BF16, name="small_bf16_noshared", n_shared=0, T=90)
+    _full_check(_layer(w, seed=13), flags)
+
+
+def test_fused_and_unfused_decode_agree_bit_for_bit(cuda_device):
+    """The persistent decode launch computes every tile as the two launches do (same MMAs, same
+    epilogues), so the layer outputs agree bit for bit."""
+    w = replace(S.WORKLOADS["k2_decode_bf16"], name="k2_e48", E=48, T=100)
+    layer = _layer(w, seed=14)
+    a, _, _ = B.forward_layer(layer, flags=FUSED)
+    b, _, _ = B.forward_layer(layer, flags=SWAP)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+
+
+def test_bf16_tensor_core_router_top3(cuda_device):
+    """The tensor-core router's fused selection with k = 3 < 8 (the epilogue keeps eight
+    candidates and emits the first k) and a ragged last 128-token tile."""
+    w = replace(SMALL_BF16, E=128, k=3, T=1100)
+    res = _full_check(_layer(w, seed=15), ROWS | B.MOE_FLAG_ROUTER_TC,
+                      rows=np.arange(0, 1100, 11))
+    assert res["compared"] > 80
 
 
 def test_bf16_tensor_core_router(cuda_device):
@@ -139,6 +170,14 @@ def test_latent_small_wide_swap_tiles(cuda_device):
     w = replace(SMALL_BF16, name="latent_small", d=512, d_latent=256, latent_norm=1, T=700,
                 w_init="fan_in")
     _full_check(_layer(w, seed=9), WIDE)
+
+
+def test_latent_small_two_m_halves(cuda_device):
+    """The latent path with 256-row SwiGLU tiles: routed groups at width L (ragged, many end in
+    their first M half) and the full-width shared expert in the same launch."""
+    w = replace(SMALL_BF16, name="latent_small", d=512, d_latent=256, latent_norm=1, T=700,
+                w_init="fan_in")
+    _full_check(_layer(w, seed=12), ROWS2)
 
 
 def test_latent_small_without_norm(cuda_device):
@@ -209,7 +248,7 @@ def test_fp8_zero_activation_group_gets_unit_scale(cuda_device):
 # K2 widths (d = 7168, I = 2048) with fewer experts: every token checked
 # ---------------------------------------------------------------------------------------------
 
-@pytest.mark.parametrize("flags", [ROWS, SWAP, WIDE], ids=["rows", "swap", "wide"])
+@pytest.mark.parametrize("flags", VARIANTS, ids=VARIANT_IDS)
 def test_k2_widths_32_experts(cuda_device, flags):
     w = replace(S.WORKLOADS["k2_decode_bf16"], name="k2_e32", E=32, T=72)
     _full_check(_layer(w, seed=8), flags)
