@@ -184,21 +184,21 @@ def touched_bytes(w, idx: np.ndarray) -> dict:
     sh13 = 2 * w.I_shared * w.d * (wb + sb) if w.n_shared else 0
     sh2 = w.d * w.I_shared * (wb + sb) if w.n_shared else 0
     lat = 2 * w.d_latent * w.d * ab if w.d_latent else 0
-    rows_sh = 0 if w.d_latent else T * w.n_shared
+    rows_sh = T * w.n_shared  # the shared expert rides in both expert launches, at width d
     return {
         "touched_experts": int(touched.size),
-        # gemm13: W1|W3 of the touched experts (+ shared), activations in, h out
-        "gemm13": len(touched) * w13 + (0 if w.d_latent else sh13) + P * de * hb
-        + rows_sh * w.d * hb + (P + rows_sh) * w.I * hb,
-        # gemm2: W2 of the touched experts (+ shared), h in, fp32 y out
-        "gemm2": len(touched) * w2 + (0 if w.d_latent else sh2) + (P + rows_sh) * w.I * hb
-        + (P + rows_sh) * de * 4,
+        # gemm13: W1|W3 of the touched experts and of the shared expert, activations in, h out
+        "gemm13": len(touched) * w13 + sh13 + P * de * hb + rows_sh * w.d * hb
+        + (P + rows_sh) * w.I * hb,
+        # gemm2: W2 of the touched experts and of the shared expert, h in, fp32 outputs out
+        "gemm2": len(touched) * w2 + sh2 + (P + rows_sh) * w.I * hb + P * de * 4
+        + rows_sh * w.d * 4,
         "layer": len(touched) * (w13 + w2) + sh13 + sh2 + lat + w.E * w.d * 4
         + 2 * T * w.d * ab,
         # both expert GEMMs in one launch: h stays inside it (written and read back on chip or
         # through L2), so only the weights, the activations in and the fp32 outputs count
-        "experts_fused": len(touched) * (w13 + w2) + (0 if w.d_latent else sh13 + sh2)
-        + P * de * hb + rows_sh * w.d * hb + (P + rows_sh) * de * 4,
+        "experts_fused": len(touched) * (w13 + w2) + sh13 + sh2 + P * de * hb
+        + rows_sh * w.d * hb + P * de * 4 + rows_sh * w.d * 4,
     }
 
 
