@@ -63,7 +63,9 @@ def build(force: bool = False, verbose: bool = False, extra=()) -> str:
     with cf.ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(lambda s: _compile(nvcc, s, verbose, list(extra)), srcs))
     tmp = LIB + f".tmp{os.getpid()}"
-    r = subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], capture_output=True, text=True)
+    # every symbol resolved at link time: a missing definition fails here, not at load time
+    r = subprocess.run([nvcc, *ARCH, "-shared", "-Xlinker", "--no-undefined", "-o", tmp, *objs],
+                       capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)

@@ -187,10 +187,6 @@ cudaError_t launch_gemm_w4(const W4Gemm& g, int num_sms, cudaStream_t st);
 // x bf16 [rows][d] -> e4m3 codes [rows][d] and scales sT [d/128][rows] (amax / 448 per 128).
 cudaError_t launch_quantize_rows(const void* x, int64_t rows, int d, uint8_t* q, float* sT,
                                  cudaStream_t st);
-// dst[r] = src[perm_src[r] / k] for e4m3 rows of d bytes, with their scales (transposed layout).
-cudaError_t launch_gather_q(const uint8_t* src, const float* src_sT, int64_t src_rows,
-                            const int32_t* perm_src, int64_t P, int k, int d, uint8_t* dst,
-                            float* dst_sT, int num_sms, cudaStream_t st);
 
 // CUDA-core grouped GEMM (fp32 or bf16 operands, fp32 accumulation), 64x64 tiles.
 cudaError_t launch_gemm_simt(const GroupedGemm& g, int num_sms, cudaStream_t st);
@@ -208,9 +204,19 @@ int permute_chunks(int64_t P);
 cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int E, int n_shared,
                            int32_t* chunk_counts, int32_t* counts, int32_t* offsets,
                            int32_t* perm_src, int32_t* perm_dst, uint32_t* err, cudaStream_t st);
-// dst[r] = src[perm_src[r] / k] for r < P (rows of `width` elements of elem_bytes each).
-cudaError_t launch_gather_rows(const void* src, const int32_t* perm_src, int64_t P, int k,
-                               int width, int elem_bytes, void* dst, int num_sms, cudaStream_t st);
+// dst[perm_dst[t*k + j]] = src[t] for every token and slot: the activation rows in the
+// expert-major order, each source row read once (rows of `width` elements of elem_bytes each);
+// destinations outside [0, P) are skipped.
+cudaError_t launch_scatter_rows(const void* src, const int32_t* perm_dst, int64_t T, int k,
+                                int64_t P, int width, int elem_bytes, void* dst, int num_sms,
+                                cudaStream_t st);
+// e4m3 rows of d bytes with their scales (transposed layouts), token-major likewise.
+cudaError_t launch_scatter_q(const uint8_t* src, const float* src_sT, int64_t T,
+                             const int32_t* perm_dst, int k, int64_t P, int d, uint8_t* dst,
+                             float* dst_sT, int num_sms, cudaStream_t st);
+// perm_dst = the inverse of perm_src (-1 where no pair lands).
+cudaError_t launch_invert_perm(const int32_t* perm_src, int64_t P, int32_t* perm_dst, int num_sms,
+                               cudaStream_t st);
 
 // Combine: out[t] = sum_j w[t,j] * y[perm_dst[t*k+j]] + y_shared[t] (+ resid[t]); y fp32, fp32
 // sum, one rounding to act_dtype.  resid (act_dtype) and y_shared may be null.

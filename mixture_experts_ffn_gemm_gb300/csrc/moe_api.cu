@@ -360,13 +360,21 @@ static cudaError_t gemm(Ctx& x, GroupedGemm g, const char* rows_label, const cha
   return launch_gemm_simt(g, x.sms, x.st);
 }
 
+// perm_dst may be null (the experts' stage entry point receives only perm_src): its inverse is
+// then rebuilt in the workspace, since the activation rows are copied token by token.
 static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
-                                const int32_t* perm_src, const void* W13, const void* W2,
-                                const float* W13_scale, const float* W2_scale, const void* Ws13,
-                                const void* Ws2, const float* Ws13_scale, const float* Ws2_scale,
-                                const void* W_down, void* y_perm) {
+                                const int32_t* perm_src, const int32_t* perm_dst, const void* W13,
+                                const void* W2, const float* W13_scale, const float* W2_scale,
+                                const void* Ws13, const void* Ws2, const float* Ws13_scale,
+                                const float* Ws2_scale, const void* W_down, void* y_perm) {
   const moe_config_t* c = x.c;
   if (c->T == 0) return MOE_OK;
+  if (!perm_dst) {
+    int32_t* inv = at<int32_t>(x.ws, x.L.perm_dst);
+    cudaError_t ei = launch_invert_perm(perm_src, c->T * c->k, inv, x.sms, x.st);
+    if (ei != cudaSuccess) return from_cuda(ei);
+    perm_dst = inv;
+  }
   const int64_t T = c->T, P = T * c->k;
   const int de = x.pl.de, I = c->I, d = c->d, E = c->E;
   const size_t ab = dtype_bytes(c->act_dtype);
@@ -384,7 +392,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     const int64_t rows_h = P + (c->n_shared ? T : 0);
     e = launch_quantize_rows(xin, T, d, xq, xq_s, x.st);
     if (e != cudaSuccess) return from_cuda(e);
-    e = launch_gather_q(xq, xq_s, T, perm_src, P, c->k, d, xpq, xpq_s, x.sms, x.st);
+    e = launch_scatter_q(xq, xq_s, T, perm_dst, c->k, P, d, xpq, xpq_s, x.sms, x.st);
     if (e != cudaSuccess) return from_cuda(e);
     Fp8Gemm g;
     g.act = xpq;
@@ -455,7 +463,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
   }
 
   if (x.pl.w4) {  // 4-bit experts: gather bf16 x, two grouped GEMMs that expand the weights
-    e = launch_gather_rows(xin, perm_src, P, c->k, d, (int)ab, x_perm, x.sms, x.st);
+    e = launch_scatter_rows(xin, perm_dst, T, c->k, P, d, (int)ab, x_perm, x.sms, x.st);
     if (e != cudaSuccess) return from_cuda(e);
     const bool sh = c->n_shared != 0;
     W4Gemm g;
@@ -539,7 +547,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     if (e != cudaSuccess) return from_cuda(e);
     route_src = x_lat;
   }
-  e = launch_gather_rows(route_src, perm_src, P, c->k, de, (int)ab, x_perm, x.sms, x.st);
+  e = launch_scatter_rows(route_src, perm_dst, T, c->k, P, de, (int)ab, x_perm, x.sms, x.st);
   if (e != cudaSuccess) return from_cuda(e);
 
   if (x.pl.fused) {  // decode: both expert GEMMs in one persistent launch
@@ -752,7 +760,7 @@ moe_status_t moe_experts(const moe_config_t* cfg, const void* x, const int32_t* 
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
   ready(c);
-  return run_experts(c, x, offsets, perm_src, W13, W2, W13_scale, W2_scale, Ws13, Ws2,
+  return run_experts(c, x, offsets, perm_src, nullptr, W13, W2, W13_scale, W2_scale, Ws13, Ws2,
                      Ws13_scale, Ws2_scale, W_down, y_perm);
 }
 
@@ -801,7 +809,7 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const float* W_
   if ((s = run_router(c, x, W_r, b, nullptr, idx, wgt)) != MOE_OK) return s;
   if ((s = run_permute(c, idx, at<int32_t>(ws, L.counts), offsets, perm_src, perm_dst)) != MOE_OK)
     return s;
-  if ((s = run_experts(c, x, offsets, perm_src, W13, W2, W13_scale, W2_scale, Ws13, Ws2,
+  if ((s = run_experts(c, x, offsets, perm_src, perm_dst, W13, W2, W13_scale, W2_scale, Ws13, Ws2,
                        Ws13_scale, Ws2_scale, W_down, y_perm)) != MOE_OK)
     return s;
   return run_combine(c, y_perm, perm_dst, wgt, W_up, out);
@@ -844,7 +852,7 @@ moe_status_t moe_forward_block(const moe_config_t* cfg, const void* x_resid, con
   if ((s = run_router(c, x_ffn, W_r, b, nullptr, idx, wgt)) != MOE_OK) return s;
   if ((s = run_permute(c, idx, at<int32_t>(ws, L.counts), offsets, perm_src, perm_dst)) != MOE_OK)
     return s;
-  if ((s = run_experts(c, x_ffn, offsets, perm_src, W13, W2, W13_scale, W2_scale, Ws13, Ws2,
+  if ((s = run_experts(c, x_ffn, offsets, perm_src, perm_dst, W13, W2, W13_scale, W2_scale, Ws13, Ws2,
                        Ws13_scale, Ws2_scale, W_down, y_perm)) != MOE_OK)
     return s;
   return run_combine(c, y_perm, perm_dst, wgt, W_up, out, x_resid);

@@ -9,7 +9,7 @@
 //   3. scatter: per chunk, one warp walks the pairs in order; lanes with the same expert get
 //               consecutive slots (__match_any_sync ranks), so each expert's rows stay in
 //               increasing pair order -- a deterministic layout.
-// The gather copies token rows into the permuted order (16-byte vectors).
+// The scatter copies token rows into the permuted order (16-byte vectors), token by token.
 #include "common.cuh"
 #include "internal.h"
 
@@ -220,32 +220,64 @@ cudaError_t launch_permute(const int32_t* idx, int64_t T, int k, int E, int n_sh
   return cudaGetLastError();
 }
 
-// dst[r][:] = src[perm_src[r] / k][:]; rows are `row_bytes` long (a multiple of 16).
+// dst[perm_dst[t*k + j]][:] = src[t][:] for every token t and slot j: each source row is read
+// once and written k times, where a copy in permuted-row order reads every row k times (the K2
+// prefill x, 235 MB, is larger than L2, so those reads reach DRAM).  A pair whose destination is
+// outside [0, P) (a skipped, out-of-range expert index) is not written; neither are the rows it
+// would have filled, which lie past every expert's group.
 __global__ void __launch_bounds__(256)
-    gather_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ perm_src,
-                       int64_t P, int k, int vec_per_row, uint4* __restrict__ dst) {
-  for (int64_t r = blockIdx.x; r < P; r += gridDim.x) {
-    const int p = perm_src[r];
-    uint4* dd = dst + r * vec_per_row;
-    if (p < 0 || p >= P) {  // a row left unset by skipped (out-of-range) pairs
-      for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dd[v] = make_uint4(0, 0, 0, 0);
-      continue;
+    scatter_rows_kernel(const uint4* __restrict__ src, const int32_t* __restrict__ perm_dst,
+                        int64_t T, int k, int64_t P, int vec_per_row, uint4* __restrict__ dst) {
+  __shared__ int64_t rows[32];
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    __syncthreads();
+    if (threadIdx.x < k) {
+      const int r = perm_dst[t * k + threadIdx.x];
+      rows[threadIdx.x] = (r >= 0 && r < P) ? (int64_t)r : -1;
     }
-    const uint4* s = src + (int64_t)(p / k) * vec_per_row;
-    for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) dd[v] = __ldg(s + v);
+    __syncthreads();
+    const uint4* s = src + t * vec_per_row;
+#pragma unroll 4
+    for (int v = threadIdx.x; v < vec_per_row; v += blockDim.x) {
+      const uint4 val = __ldg(s + v);
+      for (int j = 0; j < k; ++j)
+        if (rows[j] >= 0) dst[rows[j] * vec_per_row + v] = val;
+    }
   }
 }
 
-cudaError_t launch_gather_rows(const void* src, const int32_t* perm_src, int64_t P, int k,
-                               int width, int elem_bytes, void* dst, int num_sms,
+cudaError_t launch_scatter_rows(const void* src, const int32_t* perm_dst, int64_t T, int k,
+                                int64_t P, int width, int elem_bytes, void* dst, int num_sms,
+                                cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  const int64_t row_bytes = (int64_t)width * elem_bytes;
+  if (row_bytes % 16 || k > 32) return cudaErrorInvalidValue;
+  const int64_t blocks = T < (int64_t)num_sms * 8 ? T : (int64_t)num_sms * 8;
+  LaunchScope ls("scatter_rows", st);
+  scatter_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>((const uint4*)src, perm_dst, T, k, P,
+                                                        (int)(row_bytes / 16), (uint4*)dst);
+  return cudaGetLastError();
+}
+
+// perm_dst[perm_src[r]] = r for r < P: the inverse of the expert-major order (the layer's own
+// permute writes both; the stage entry point for the experts receives only perm_src).
+__global__ void invert_perm_kernel(const int32_t* __restrict__ perm_src, int64_t P,
+                                   int32_t* __restrict__ perm_dst) {
+  for (int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; r < P;
+       r += (int64_t)gridDim.x * blockDim.x) {
+    const int p = perm_src[r];
+    if (p >= 0 && p < P) perm_dst[p] = (int32_t)r;
+  }
+}
+
+cudaError_t launch_invert_perm(const int32_t* perm_src, int64_t P, int32_t* perm_dst, int num_sms,
                                cudaStream_t st) {
   if (P <= 0) return cudaSuccess;
-  const int64_t row_bytes = (int64_t)width * elem_bytes;
-  if (row_bytes % 16) return cudaErrorInvalidValue;
-  const int64_t blocks = P < (int64_t)num_sms * 16 ? P : (int64_t)num_sms * 16;
-  LaunchScope ls("gather_rows", st);
-  gather_rows_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-      (const uint4*)src, perm_src, P, k, (int)(row_bytes / 16), (uint4*)dst);
+  cudaError_t e = cudaMemsetAsync(perm_dst, 0xff, (size_t)P * 4, st);  // -1: no pair
+  if (e != cudaSuccess) return e;
+  const int64_t blocks = (P + 255) / 256 < (int64_t)num_sms * 8 ? (P + 255) / 256 : num_sms * 8;
+  LaunchScope ls("invert_perm", st);
+  invert_perm_kernel<<<(unsigned)blocks, 256, 0, st>>>(perm_src, P, perm_dst);
   return cudaGetLastError();
 }
 

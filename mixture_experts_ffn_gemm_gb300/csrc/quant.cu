@@ -1,5 +1,5 @@
-// quant.cu -- e4m3 activation quantisation for the fp8 expert path, and the permuted gather of the
-// quantised rows with their scales.
+// quant.cu -- e4m3 activation quantisation for the fp8 expert path, and the copy of the quantised
+// rows with their scales into the expert-major order.
 //
 // Expert weights stored as e4m3 with block scales, the form the nnterp "kimi_k2" note gives for the
 // K2 checkpoints ("FP8 blocks"); activations entering the expert GEMMs are quantised per token per
@@ -59,36 +59,45 @@ cudaError_t launch_quantize_rows(const void* x, int64_t rows, int d, uint8_t* q,
 }
 
 // dst[r] = src[perm_src[r] / k] (d bytes of e4m3 codes) and dst_sT[g][r] = src_sT[g][t].
+// The e4m3 rows in the permuted order, token by token: each token's codes and scales are read
+// once and written to its k permuted rows (perm_dst); pairs whose destination is outside [0, P)
+// are skipped.
 __global__ void __launch_bounds__(256)
-    gather_q_kernel(const uint8_t* __restrict__ src, const float* __restrict__ src_sT,
-                    int64_t src_rows, const int32_t* __restrict__ perm_src, int64_t P, int k,
-                    int d, uint8_t* __restrict__ dst, float* __restrict__ dst_sT) {
+    scatter_q_kernel(const uint8_t* __restrict__ src, const float* __restrict__ src_sT, int64_t T,
+                     const int32_t* __restrict__ perm_dst, int k, int64_t P, int d,
+                     uint8_t* __restrict__ dst, float* __restrict__ dst_sT) {
+  __shared__ int64_t rows[32];
   const int vec = d / 16;
   const int groups = d / 128;
-  for (int64_t r = blockIdx.x; r < P; r += gridDim.x) {
-    const int p = perm_src[r];
-    uint4* out = reinterpret_cast<uint4*>(dst + r * d);
-    if (p < 0 || p >= P) {
-      for (int v = threadIdx.x; v < vec; v += blockDim.x) out[v] = make_uint4(0, 0, 0, 0);
-      for (int g = threadIdx.x; g < groups; g += blockDim.x) dst_sT[(int64_t)g * P + r] = 1.0f;
-      continue;
+  for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
+    __syncthreads();
+    if (threadIdx.x < k) {
+      const int r = perm_dst[t * k + threadIdx.x];
+      rows[threadIdx.x] = (r >= 0 && r < P) ? (int64_t)r : -1;
     }
-    const int64_t t = p / k;
+    __syncthreads();
     const uint4* in = reinterpret_cast<const uint4*>(src + t * d);
-    for (int v = threadIdx.x; v < vec; v += blockDim.x) out[v] = __ldg(in + v);
-    for (int g = threadIdx.x; g < groups; g += blockDim.x)
-      dst_sT[(int64_t)g * P + r] = src_sT[(int64_t)g * src_rows + t];
+    for (int v = threadIdx.x; v < vec; v += blockDim.x) {
+      const uint4 val = __ldg(in + v);
+      for (int j = 0; j < k; ++j)
+        if (rows[j] >= 0) reinterpret_cast<uint4*>(dst + rows[j] * d)[v] = val;
+    }
+    for (int g = threadIdx.x; g < groups; g += blockDim.x) {
+      const float sc = src_sT[(int64_t)g * T + t];
+      for (int j = 0; j < k; ++j)
+        if (rows[j] >= 0) dst_sT[(int64_t)g * P + rows[j]] = sc;
+    }
   }
 }
 
-cudaError_t launch_gather_q(const uint8_t* src, const float* src_sT, int64_t src_rows,
-                            const int32_t* perm_src, int64_t P, int k, int d, uint8_t* dst,
-                            float* dst_sT, int num_sms, cudaStream_t st) {
-  if (P <= 0) return cudaSuccess;
-  if (d % 128) return cudaErrorInvalidValue;
-  const int64_t blocks = P < (int64_t)num_sms * 16 ? P : (int64_t)num_sms * 16;
-  LaunchScope ls("gather_rows_e4m3", st);
-  gather_q_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, src_sT, src_rows, perm_src, P, k, d, dst,
+cudaError_t launch_scatter_q(const uint8_t* src, const float* src_sT, int64_t T,
+                             const int32_t* perm_dst, int k, int64_t P, int d, uint8_t* dst,
+                             float* dst_sT, int num_sms, cudaStream_t st) {
+  if (T <= 0) return cudaSuccess;
+  if (d % 128 || k > 32) return cudaErrorInvalidValue;
+  const int64_t blocks = T < (int64_t)num_sms * 8 ? T : (int64_t)num_sms * 8;
+  LaunchScope ls("scatter_rows_e4m3", st);
+  scatter_q_kernel<<<(unsigned)blocks, 256, 0, st>>>(src, src_sT, T, perm_dst, k, P, d, dst,
                                                      dst_sT);
   return cudaGetLastError();
 }
