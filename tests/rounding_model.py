@@ -73,6 +73,34 @@ def ideal_forward(layer, rows=None, round_h=True, round_out=True, round_xlat=Tru
     return {"out": out, "margin": rt["margin"], "idx": rt["idx"]}
 
 
+def pages_combine_forward(layer, rows=None) -> dict:
+    """The K2 layer with the rounding sequence of the pages' own code ("Kimi K3 · Latent
+    up-projection", `moe_infer` back half, and the block's `forward`): h rounded to bf16 (the W2
+    operand), each expert's output rounded to bf16 (the module's output type), cast to the gate
+    type (fp32) and multiplied by its gate, summed over the slots, cast back to bf16; the shared
+    expert's output in bf16; the two added in bf16.  Everything else exact, as in
+    ideal_forward."""
+    w = layer.w
+    assert not w.d_latent, "the K2 path"
+    T = layer.x.shape[0]
+    rows = np.arange(T) if rows is None else np.asarray(rows)
+    xr = layer.x[torch.as_tensor(rows, device=layer.x.device)]
+    xm, W_r, b = OB.route_inputs(layer, torch.as_tensor(rows))
+    cfg = OB.config(layer, len(rows))
+    rt = oracle.route(cfg, xm, W_r, b)
+    x = _f64(xr)
+    y = np.zeros((len(rows), w.d), np.float64)
+    for e in np.unique(rt["idx"]):
+        t, j = np.nonzero(rt["idx"] == e)
+        ye = OB.round_bf16(_mlp(x[t], _f64(layer.W13[e]), _f64(layer.W2[e]), w.I, True))
+        gates = rt["gates"][t, j].astype(np.float32).astype(np.float64)  # the gate type
+        y[t] += gates[:, None] * ye
+    routed = OB.round_bf16(y)
+    shared = (OB.round_bf16(_mlp(x, _f64(layer.Ws13), _f64(layer.Ws2), w.I_shared, True))
+              if w.n_shared else np.zeros_like(routed))
+    return {"out": OB.round_bf16(routed + shared), "margin": rt["margin"], "idx": rt["idx"]}
+
+
 def errors(got: np.ndarray, ref: np.ndarray) -> dict:
     """Plain max error, max error beyond the result's own bf16 rounding, rms error; each over
     rms(ref)."""

@@ -89,3 +89,21 @@ def test_ideal_bf16_pipeline_against_the_bounds(cases, name):
         assert e["plain"] <= 2e-2
     assert e["beyond_rounding"] <= 1.5e-2  # inside the bound the parity tests apply
     assert e["rms"] <= 5e-3
+
+
+@pytest.mark.parametrize("name", ["k2_top4", "k1_forced"])
+def test_pages_rounding_sequence_against_the_one_rounding_sum(cases, name):
+    """The pages' `moe_infer` rounds each expert's output to bf16, casts it to the gate type,
+    multiplies, sums over the slots and casts back, then adds the bf16 shared output in bf16.  The
+    library sums the fp32 expert outputs with the shared one and rounds once.  Against the fp64
+    oracle: the pages' sequence is itself inside the parity rule (so the rule does not reject the
+    pages' own arithmetic), and the one-rounding sum is the more accurate of the two, in the rms
+    and in the error beyond the output's rounding."""
+    layer, ref, keep = cases[name]
+    pages = R.errors(R.pages_combine_forward(layer)["out"][keep], ref["out"][keep])
+    ours = R.errors(R.ideal_forward(layer)["out"][keep], ref["out"][keep])
+    print(name, "pages", {k: f"{v:.3e}" for k, v in pages.items()},
+          "one rounding", {k: f"{v:.3e}" for k, v in ours.items()})
+    assert pages["beyond_rounding"] <= 2e-2 and pages["rms"] <= 5e-3
+    assert ours["rms"] < pages["rms"]
+    assert ours["beyond_rounding"] < pages["beyond_rounding"]

@@ -215,6 +215,28 @@ def test_error_is_the_ideal_bf16_pipelines(cuda_device, case):
     assert gpu["beyond_rounding"] <= 2e-2
 
 
+@pytest.mark.parametrize("case", ["k2_top4", "k2_widths"])
+def test_outputs_within_the_rule_of_the_pages_rounding_sequence(cuda_device, case):
+    """The kernels' outputs against an emulation of the pages' own combine rounding (bf16 expert
+    outputs cast to the gate type, multiplied, summed, cast back, plus the bf16 shared output;
+    rounding_model.pages_combine_forward) on the same GPU-drawn inputs: within the bf16 rule, so
+    the one-rounding fp32 sum the library uses agrees with the pages' arithmetic to the same
+    tolerance it keeps against the fp64 oracle."""
+    import rounding_model as R
+    L = _lib()
+    if case == "k2_top4":
+        layer = _layer(SMALL_BF16, seed=1)
+    else:
+        layer = _layer(replace(S.WORKLOADS["k2_prefill_bf16"], name="k2_e32", E=32, T=256), seed=3)
+    g = L.run_gpu(layer)
+    pages = R.pages_combine_forward(layer)
+    keep = pages["margin"] >= L.NEAR_TIE
+    e = R.errors(g.out.float().cpu().numpy()[keep], pages["out"][keep])
+    print(case, "gpu vs pages' sequence", {k: f"{v:.3e}" for k, v in e.items()})
+    assert e["beyond_rounding"] <= 2e-2
+    assert e["rms"] <= 5e-3
+
+
 # ---------------------------------------------------------------------------------------------
 # fp8 experts: e4m3 weights with 128 x 128 block scales, activations per token per 128 channels
 # ---------------------------------------------------------------------------------------------
