@@ -90,6 +90,8 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2, MOE_INT4 = 3 } moe_d
                                        * GEMMs in one persistent launch (W1|W3 + SwiGLU tiles,
                                        * then W2 tiles that wait for their h rows) instead of two
                                        * launches; same results bit for bit, measured slower      */
+#define MOE_FLAG_GEMM_PAIR 0x400u     /* token-rows expert GEMM tiles of 256 rows on a pair of SMs
+                                       * (one M = 256 tensor-core MMA over both SMs' operands)     */
 /* Test hook for the failure path: the tensor-core W1|W3 expert GEMM's copy producer issues no
  * copy, so its MMA issuer's bounded wait (shortened to 50 ms under this flag) expires; the kernel
  * flags MOE_ERR_TIMEOUT in the device status, drains, frees its tensor memory and returns, and

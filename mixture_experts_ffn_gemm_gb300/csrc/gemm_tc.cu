@@ -70,18 +70,20 @@ struct TcParams {
   int32_t dense_band;   // the dense group's tiles in bands of this many row tiles (0: one band)
 };
 
-template <bool kSwap, int kBN, int kEpi, int kMH = 1>
+template <bool kSwap, int kBN, int kEpi, int kMH = 1, bool kPair = false>
 struct TcShape {
   static_assert(kMH == 1 || (kMH == 2 && !kSwap && kBN == 256), "two M halves: token rows, N = 256");
+  static_assert(!kPair || (!kSwap && kBN == 256 && kMH == 1 && kEpi != EPI_STORE_ADD),
+                "CTA pairs: token-rows SwiGLU / store tiles, N = 256");
   static constexpr bool kSwiGLU = kEpi == EPI_SWIGLU;
   // 256-token swap-AB SwiGLU tiles stack 64 W1 rows over the matching 64 W3 rows in one M = 128
   // operand, so that one 256-column accumulator holds both and two of them fit in TMEM
   static constexpr bool kStack = kSwap && kSwiGLU && kBN == 256;
-  static constexpr int RPT = kSwap ? kBN : 128 * kMH;                   // token rows per tile
+  static constexpr int RPT = kSwap ? kBN : 128 * kMH * (kPair ? 2 : 1);  // token rows per tile
   static constexpr int FPT = kSwap ? (kStack ? 64 : 128) : (kSwiGLU ? kBN / 2 : kBN);  // features
   static constexpr int OPA =
       (kSwap && kSwiGLU && !kStack) ? 2 * kBoxBytes : kMH * kBoxBytes;  // A bytes / stage
-  static constexpr int OPB = kBN * 128;                                       // B bytes / stage
+  static constexpr int OPB = (kPair ? kBN / 2 : kBN) * 128;  // B bytes / stage (a pair: half)
   static constexpr int STAGE = OPA + OPB;
   static constexpr int ACC_COLS =
       (kSwap && kSwiGLU && !kStack) ? 2 * kBN : kMH * kBN;  // fp32 columns of one accumulator
@@ -130,9 +132,17 @@ __device__ __forceinline__ void store_rows_128B(uint8_t* buf, int lane, const ui
   }
 }
 
-template <bool kSwap, int kBN, int kEpi, int kMH = 1>
+template <bool kSwap, int kBN, int kEpi, int kMH = 1, bool kPair = false>
 __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid_constant__ TcParams p) {
-  using S = TcShape<kSwap, kBN, kEpi, kMH>;
+  using S = TcShape<kSwap, kBN, kEpi, kMH, kPair>;
+  // CTA pairs: the two CTAs of a cluster share every tile (256 token rows, 128 each) and one
+  // M = 256 MMA per K-step issued by the even CTA; each CTA copies its own 128 activation rows and
+  // its half of the weight rows, so a stage is 32 KB per SM for the MMA work a 48 KB stage feeds
+  // in a CTA alone, and six stages are in flight.
+  const uint32_t rank = kPair ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int tile0 = kPair ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int tstep = kPair ? (int)(gridDim.x >> 1) : (int)gridDim.x;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -161,7 +171,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], kPair ? 256 : 128);  // a pair: both CTAs' epilogue threads
     }
     mbar_init(drain, 1);
     *abort_flag = 0;
@@ -176,13 +186,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_holder, S::TMEM_COLS);
-    tmem_relinquish();
+    if constexpr (kPair) {  // one warp of each CTA of the pair, together
+      tmem_alloc_pair(tmem_holder, S::TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(tmem_holder, S::TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   build_tile_table(tile_start, row_start, scratch, p.offsets, p.n_routed, p.dense_rows, S::RPT,
                    p.F / S::FPT, p.F_d / S::FPT);  // ends with __syncthreads
   tc_fence_before();
   __syncthreads();
+  if constexpr (kPair) cluster_sync();  // both CTAs' barriers exist before any remote arrival
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int G = p.n_routed + (p.dense_rows > 0 ? 1 : 0);
@@ -195,7 +211,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
       uint32_t stage = 0, phase = 0;
       int armed = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = tile0; tile < total && ok; tile += tstep) {
         const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
                                         p.dense_rows, p.dense_act_row0, S::RPT, p.dense_band);
         const CUtensorMap* ma = ti.dense ? &p.map_act_d : &p.map_act;
@@ -215,9 +231,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
           }
           uint8_t* sa = smem + stage * S::STAGE;
           uint8_t* sb = sa + S::OPA;
-          mbar_arrive_expect_tx(&full[stage], tx);
           const int kx = kb * kBK;
           const int ax = kx % kwrap;
+          if constexpr (kPair) {
+            // this CTA's 128 activation rows and its half of the weight rows (SwiGLU: the W1 rows
+            // on the even CTA, the matching W3 rows on the odd one); both CTAs' copies complete
+            // on the even CTA's barrier, which expects the bytes of both
+            const uint32_t bar = cluster_addr(&full[stage], 0);
+            if (leader) mbar_arrive_expect_tx(&full[stage], 2 * S::STAGE);
+            tma_load_2d_pair(sa, ma, bar, ax, act_y + (int)rank * 128);
+            tma_load_2d_pair(sb, mw, bar, kx,
+                             S::kSwiGLU ? (rank ? w_y + u_off : w_y) : w_y + (int)rank * 128);
+          } else {
+          mbar_arrive_expect_tx(&full[stage], tx);
           if (!kSwap) {
             tma_load_2d(sa, ma, &full[stage], ax, act_y);
             if (half1) tma_load_2d(sa + kBoxBytes, ma, &full[stage], ax, act_y + 128);
@@ -237,6 +263,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
                           w_y + u_off);
             tma_load_2d(sb, ma, &full[stage], ax, act_y);
           }
+          }
           if (armed < S::STAGES) ++armed;
           if (++stage == S::STAGES) {
             stage = 0;
@@ -244,8 +271,9 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
           }
         }
       }
-      if (!ok) {
-        // drain: wait (briefly) for the copies of the most recent stage uses to land
+      if (!ok && leader) {
+        // drain: wait (briefly) for the copies of the most recent stage uses to land (a pair's
+        // copies all complete on the even CTA's barriers)
         for (int i = 0; i < armed; ++i) {
           if (stage == 0) {
             stage = S::STAGES;
@@ -258,11 +286,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    if (lane == 0 && leader) {  // a pair's MMAs are issued by its even CTA
       constexpr uint32_t kIdesc = idesc_bf16_f32<128, (kBN > 256 ? 256 : kBN)>();
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = tile0; tile < total && ok; tile += tstep) {
         const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
                                         p.dense_rows, p.dense_act_row0, S::RPT, p.dense_band);
         const int nkb = ti.dense ? nkb_d : nkb_r;
@@ -274,7 +302,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
           idesc = idesc_bf16_f32_n(n);
         }
         const bool half1 = kMH == 2 && ti.valid > 128;
-        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, p.wait_ns)) break;
+        // the accumulator is free once both CTAs' epilogues have read it (a pair: arrivals from
+        // the odd CTA, released at cluster scope)
+        if (!(kPair ? mbar_wait_cluster(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, p.wait_ns)
+                    : mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, p.err, p.wait_ns)))
+          break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * S::ACC_COLS;
         for (int kb = 0; kb < nkb; ++kb) {
@@ -296,6 +328,11 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
                        idesc_bf16_f32<128, kBN - 256>(), accum);
               continue;
             }
+            if constexpr (kPair) {  // M = 256 over both CTAs' rows, N = 256 over both halves
+              mma_bf16_pair(d0, sw128_kmajor_desc(sa + k16 * 32), bdesc, idesc_bf16_f32_pair(256),
+                            accum);
+              continue;
+            }
             mma_bf16(d0, sw128_kmajor_desc(sa + k16 * 32), bdesc, idesc, accum);
             if (half1)  // the second 128 token rows against the same weight K-block
               mma_bf16(d0 + kBN, sw128_kmajor_desc(sa + kBoxBytes + k16 * 32), bdesc, idesc, accum);
@@ -303,19 +340,28 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
               mma_bf16(d0 + kBN, sw128_kmajor_desc(sa + kBoxBytes + k16 * 32), bdesc, idesc,
                        accum);
           }
-          mma_commit(&empty[stage]);
+          if constexpr (kPair)
+            mma_commit_pair(&empty[stage]);  // frees the stage in both CTAs
+          else
+            mma_commit(&empty[stage]);
           if (++stage == S::STAGES) {
             stage = 0;
             phase ^= 1u;
           }
         }
         if (!ok) break;
-        mma_commit(&tfull[acc]);
+        if constexpr (kPair)
+          mma_commit_pair(&tfull[acc]);  // both CTAs' epilogues may read their rows
+        else
+          mma_commit(&tfull[acc]);
         if (S::NACC == 2) acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       // every MMA issued above has completed once this commit arrives
-      mma_commit(drain);
+      if constexpr (kPair)
+        mma_commit_pair(drain);
+      else
+        mma_commit(drain);
       mbar_wait(drain, 0, nullptr, nullptr, kDrainLimitNs);
     }
   } else {
@@ -323,7 +369,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
     const int quarter = warp & 3;       // TMEM lanes this warp may read: 32 * quarter + [0, 32)
     const int r = quarter * 32 + lane;  // tile row (rows) or tile feature (swap)
     uint32_t acc = 0, acc_phase = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+    for (int tile = tile0; tile < total; tile += tstep) {
       const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
                                       p.dense_rows, p.dense_act_row0, S::RPT, p.dense_band);
       int ok = 1;
@@ -334,17 +380,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
       if (!ok) break;
       tc_fence_after();
       const uint32_t tb = tmem_base + acc * S::ACC_COLS + ((uint32_t)(quarter * 32) << 16);
+      // a pair: this CTA's accumulator holds the tile's rows 128 * rank .. +127
       const int64_t out_row0 = (ti.dense ? (int64_t)p.dense_out_row0 : (int64_t)ti.grp_row0) +
-                               (int64_t)ti.rt * S::RPT;
+                               (int64_t)ti.rt * S::RPT + (kPair ? (int64_t)rank * 128 : 0);
+      const int vt = kPair ? ti.valid - (int)rank * 128 : ti.valid;  // rows of this CTA's part
       void* const out = ti.dense ? p.out_d : p.out;
       const int64_t ldo = ti.dense ? p.ldo_d : p.ldo;
       if (!kSwap && S::kStaged) {
         uint8_t* buf = staging + (warp - 2) * 4096;
 #pragma unroll 1
-        for (int mh = 0; mh < kMH && mh * 128 < ti.valid; ++mh) {
+        for (int mh = 0; mh < kMH && mh * 128 < vt; ++mh) {
           const uint32_t th = tmem_base + acc * S::ACC_COLS + mh * kBN +
                               ((uint32_t)(quarter * 32) << 16);  // this M half's columns
-          const int vrows = min(32, max(0, ti.valid - mh * 128 - quarter * 32));
+          const int vrows = min(32, max(0, vt - mh * 128 - quarter * 32));
           const int64_t row0 = out_row0 + mh * 128 + quarter * 32;
           if (S::kSwiGLU) {  // h in bf16: chunks of 64 features = 128 bytes per row
 #pragma unroll 1
@@ -516,7 +564,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      if constexpr (kPair)
+        mbar_arrive_cluster(cluster_addr(&tempty[acc], 0));  // the even CTA's accumulator barrier
+      else
+        mbar_arrive(&tempty[acc]);
       if (S::NACC == 2) acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -525,9 +576,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
   if (S::kStaged && p.tma_out && warp >= 2 && lane == 0) tma_store_wait_all();
   tc_fence_before();
   __syncthreads();
+  // a pair: no arrival on the peer's barriers and no MMA into the peer's TMEM after this point
+  if constexpr (kPair) cluster_sync();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, S::TMEM_COLS);
+    if constexpr (kPair)
+      tmem_dealloc_pair(tmem_base, S::TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, S::TMEM_COLS);
   }
 }
 
@@ -582,10 +638,10 @@ static bool make_map_f32_out(CUtensorMap* m, void* base, int64_t rows, int64_t c
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool kSwap, int kBN, int kEpi, int kMH = 1>
+template <bool kSwap, int kBN, int kEpi, int kMH = 1, bool kPair = false>
 static cudaError_t launch_variant(const TcParams& p, int grid, cudaStream_t st, const char* label) {
-  using S = TcShape<kSwap, kBN, kEpi, kMH>;
-  auto kern = moe_gemm_tc_kernel<kSwap, kBN, kEpi, kMH>;
+  using S = TcShape<kSwap, kBN, kEpi, kMH, kPair>;
+  auto kern = moe_gemm_tc_kernel<kSwap, kBN, kEpi, kMH, kPair>;
   static int attr_set_device = -1;  // the attribute is per device; refreshed when it changes
   int dev = 0;
   cudaGetDevice(&dev);
@@ -596,6 +652,22 @@ static cudaError_t launch_variant(const TcParams& p, int grid, cudaStream_t st, 
     attr_set_device = dev;
   }
   LaunchScope ls(label, st);
+  if constexpr (kPair) {  // clusters of two CTAs (one pair each), one CTA per SM
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3((unsigned)(grid & ~1));
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = S::SMEM;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+  }
   kern<<<grid, kTcThreads, S::SMEM, st>>>(p);
   return cudaGetLastError();
 }
@@ -707,8 +779,11 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
       // two M halves per tile only on request: measured slower at prefill (gemm13 6.6 -> 8.1 ms)
       // and K3 (2.4 -> 3.1 ms), the SwiGLU epilogue no longer hidden behind the next mainloop
       if (g.m_halves == 2) return launch_variant<false, 256, EPI_SWIGLU, 2>(p, grid, st, g.label);
+      if (g.pair) return launch_variant<false, 256, EPI_SWIGLU, 1, true>(p, grid, st, g.label);
       return launch_variant<false, 256, EPI_SWIGLU>(p, grid, st, g.label);
     }
+    if (g.pair && g.epi == EPI_STORE && !f32_router && !g.n128)
+      return launch_variant<false, 256, EPI_STORE, 1, true>(p, grid, st, g.label);
     if (f32_router && g.F % 384 == 0) return launch_variant<false, 384, EPI_STORE>(p, grid, st, g.label);
     if (f32_router || (g.n128 && g.epi == EPI_STORE))
       return launch_variant<false, 128, EPI_STORE>(p, grid, st, g.label);

@@ -612,6 +612,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.err = x.err;
     g.test_stall = (c->flags & MOE_FLAG_TEST_STALL_EXPERTS) != 0;
     g.m_halves = (c->flags & MOE_FLAG_GEMM_M1) ? 1 : (c->flags & MOE_FLAG_GEMM_M2) ? 2 : 0;
+    g.pair = (c->flags & MOE_FLAG_GEMM_PAIR) && !g.test_stall && g.m_halves != 2;
     e = gemm(x, g, "gemm13_swiglu_rows", "gemm13_swiglu_swap", "gemm13_swiglu_swap256",
              "gemm13_swiglu_simt");
     if (e != cudaSuccess) return from_cuda(e);
@@ -651,6 +652,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.out_dtype = MOE_F32;
     g.err = x.err;
     g.n128 = (c->flags & MOE_FLAG_GEMM_N128) != 0;
+    g.pair = (c->flags & MOE_FLAG_GEMM_PAIR) && !g.n128;
     e = gemm(x, g, "gemm2_rows", "gemm2_swap", "gemm2_swap256", "gemm2_simt");
     if (e != cudaSuccess) return from_cuda(e);
   }

@@ -24,8 +24,9 @@ SWAP = B.MOE_FLAG_GEMM_SWAP_AB
 WIDE = B.MOE_FLAG_GEMM_SWAP_WIDE  # 256-token swap-AB tiles with a run-time MMA N
 ROWS2 = B.MOE_FLAG_GEMM_ROWS_MAJOR | B.MOE_FLAG_GEMM_M2  # 256-row tiles of two M halves
 FUSED = SWAP | B.MOE_FLAG_DECODE_FUSED  # decode expert GEMMs in one persistent launch
-VARIANTS = [ROWS, ROWS2, SWAP, FUSED, WIDE]
-VARIANT_IDS = ["rows", "rows_m2", "swap", "swap_fused", "wide"]
+PAIR = B.MOE_FLAG_GEMM_ROWS_MAJOR | B.MOE_FLAG_GEMM_PAIR  # 256-row tiles on a pair of SMs
+VARIANTS = [ROWS, ROWS2, PAIR, SWAP, FUSED, WIDE]
+VARIANT_IDS = ["rows", "rows_m2", "rows_pair", "swap", "swap_fused", "wide"]
 
 
 def _lib():
@@ -180,6 +181,14 @@ def test_latent_small_two_m_halves(cuda_device):
     _full_check(_layer(w, seed=12), ROWS2)
 
 
+def test_latent_small_sm_pairs(cuda_device):
+    """The latent path with 256-row tiles on SM pairs: routed groups at width L, many ending in
+    the first SM's 128 rows, and the full-width shared expert in the same launches."""
+    w = replace(SMALL_BF16, name="latent_small", d=512, d_latent=256, latent_norm=1, T=700,
+                w_init="fan_in")
+    _full_check(_layer(w, seed=12), PAIR)
+
+
 def test_latent_small_without_norm(cuda_device):
     w = replace(SMALL_BF16, name="latent_small", d=512, d_latent=256, latent_norm=0, T=70,
                 w_init="fan_in")
@@ -325,14 +334,14 @@ def _sample(T, n=512, seed=1):
     return S.subset_rows(T, n, seed=seed).numpy()
 
 
-def _full_workload(name):
-    """One benchmark workload in the bench's launch configuration: routing and permutation on
-    every token; 64 seeded rows of the fp32 expert outputs plus the last row of every expert;
-    the outputs of every token for decode-sized batches (128 tokens), else of 512 seeded
-    tokens."""
+def _full_workload(name, flags=0):
+    """One benchmark workload in the bench's launch configuration (or the given GEMM flags):
+    routing and permutation on every token; 64 seeded rows of the fp32 expert outputs plus the
+    last row of every expert; the outputs of every token for decode-sized batches (128 tokens),
+    else of 512 seeded tokens."""
     w = S.WORKLOADS[name]
     layer = _layer(w)
-    res = _full_check(layer, 0, rows=None if w.T <= 128 else _sample(w.T))
+    res = _full_check(layer, flags, rows=None if w.T <= 128 else _sample(w.T))
     del layer
     torch.cuda.empty_cache()
     assert res["compared"] + res["sample_near_ties"] == min(w.T, 512)
@@ -347,6 +356,11 @@ def test_full_k2_decode(cuda_device):
 def test_full_k2_prefill(cuda_device):
     res = _full_workload("k2_prefill_bf16")
     print("k2_prefill", res)
+
+
+def test_full_k2_prefill_sm_pairs(cuda_device):
+    res = _full_workload("k2_prefill_bf16", PAIR)
+    print("k2_prefill_pairs", res)
 
 
 def test_k2_prefill_65536_tokens_offsets_past_2_31(cuda_device):
