@@ -17,7 +17,9 @@ namespace moe {
 constexpr int kMaxK = 32;
 
 // y_perm and y_shared hold fp32 expert outputs; resid (optional, the block's residual stream) is
-// in the output type; out is bf16 or fp32, rounded once from the fp32 sum.
+// in the output type; out is bf16 or fp32, rounded once from the fp32 sum.  T tokens (a chunk of
+// the batch when the caller offsets perm_dst, weight, y_shared, resid and out); P is the number of
+// rows of y_perm, so that perm_dst entries outside [0, P) read nothing.
 // acc[0..7] += sum over the token's k slots of gw[j] * y[rows[j]][c .. c+7], in slot order.
 // Four rows are loaded before any is used (a skipped slot, rows[j] < 0, reads nothing and adds
 // zero), so each thread has four row loads in flight instead of one.
@@ -49,11 +51,10 @@ template <typename TO>
 __global__ void __launch_bounds__(256)
     combine_kernel(const float* __restrict__ y_perm, const float* __restrict__ y_shared,
                    const int32_t* __restrict__ perm_dst, const float* __restrict__ weight,
-                   int64_t T, int k, int d, const TO* __restrict__ resid, TO* __restrict__ out,
-                   int cols_per_block) {
+                   int64_t T, int k, int64_t P, int d, const TO* __restrict__ resid,
+                   TO* __restrict__ out, int cols_per_block) {
   __shared__ int64_t rows[kMaxK];
   __shared__ float gw[kMaxK];
-  const int64_t P = T * k;
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
     __syncthreads();
     if (threadIdx.x < k) {
@@ -89,8 +90,9 @@ __global__ void __launch_bounds__(256)
 }
 
 cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* y_shared,
-                           const int32_t* perm_dst, const float* weight, int64_t T, int k, int d,
-                           const void* resid, void* out, int num_sms, cudaStream_t st) {
+                           const int32_t* perm_dst, const float* weight, int64_t T, int k,
+                           int64_t P, int d, const void* resid, void* out, int num_sms,
+                           cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   if (k > kMaxK || d % 8) return cudaErrorInvalidValue;
   const int64_t blocks = T < (int64_t)num_sms * 8 ? T : (int64_t)num_sms * 8;
@@ -102,11 +104,11 @@ cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* y_shar
   LaunchScope ls("combine", st);
   if (act_dtype == MOE_BF16)
     combine_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(
-        (const float*)y_perm, (const float*)y_shared, perm_dst, weight, T, k, d,
+        (const float*)y_perm, (const float*)y_shared, perm_dst, weight, T, k, P, d,
         (const __nv_bfloat16*)resid, (__nv_bfloat16*)out, cols);
   else
     combine_kernel<float><<<grid, 256, 0, st>>>(
-        (const float*)y_perm, (const float*)y_shared, perm_dst, weight, T, k, d,
+        (const float*)y_perm, (const float*)y_shared, perm_dst, weight, T, k, P, d,
         (const float*)resid, (float*)out, cols);
   return cudaGetLastError();
 }
@@ -118,13 +120,12 @@ constexpr int kMaxLatent = 8192;
 __global__ void __launch_bounds__(256)
     latent_combine_kernel(const float* __restrict__ y_perm,
                           const int32_t* __restrict__ perm_dst, const float* __restrict__ weight,
-                          int64_t T, int k, int L, int norm, float eps,
+                          int64_t T, int k, int64_t P, int L, int norm, float eps,
                           __nv_bfloat16* __restrict__ u_hat) {
   __shared__ float ysum[kMaxLatent];
   __shared__ int64_t rows[kMaxK];
   __shared__ float gw[kMaxK];
   __shared__ float red[32];
-  const int64_t P = T * k;
   for (int64_t t = blockIdx.x; t < T; t += gridDim.x) {
     __syncthreads();
     if (threadIdx.x < k) {
@@ -170,14 +171,15 @@ __global__ void __launch_bounds__(256)
 }
 
 cudaError_t launch_latent_combine(const void* y_perm, const int32_t* perm_dst,
-                                  const float* weight, int64_t T, int k, int L, int norm,
-                                  float eps, void* u_hat, int num_sms, cudaStream_t st) {
+                                  const float* weight, int64_t T, int k, int64_t P, int L,
+                                  int norm, float eps, void* u_hat, int num_sms,
+                                  cudaStream_t st) {
   if (T <= 0) return cudaSuccess;
   if (k > kMaxK || L > kMaxLatent || L % 8) return cudaErrorInvalidValue;
   const int64_t blocks = T < (int64_t)num_sms * 8 ? T : (int64_t)num_sms * 8;
   LaunchScope ls("latent_combine", st);
   latent_combine_kernel<<<(unsigned)blocks, 256, 0, st>>>(
-      (const float*)y_perm, perm_dst, weight, T, k, L, norm, eps,
+      (const float*)y_perm, perm_dst, weight, T, k, P, L, norm, eps,
       (__nv_bfloat16*)u_hat);
   return cudaGetLastError();
 }

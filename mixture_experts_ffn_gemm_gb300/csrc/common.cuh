@@ -373,12 +373,16 @@ __device__ __forceinline__ void mma_bf16_pair(uint32_t d_tmem, uint64_t a_desc, 
       : "memory");
 }
 // Arrive once on the barrier at `bar`'s offset in both CTAs of the pair when every tcgen05
-// operation this thread issued before has completed.
+// operation this thread issued before has completed: one commit to this CTA's barrier and one to
+// the peer's (its shared::cluster address).
 __device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  const uint32_t own = smem_u32(bar);
+  uint32_t peer;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(peer) : "r"(own), "r"(1u));
   asm volatile(
-      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 "
-      "[%0], %1;" ::"r"(smem_u32(bar)),
-      "h"((uint16_t)3)
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t"
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%1];" ::"r"(own),
+      "r"(peer)
       : "memory");
 }
 // TMA tile load into this CTA's shared memory whose completion is counted on the barrier at

@@ -222,18 +222,20 @@ cudaError_t launch_invert_perm(const int32_t* perm_src, int64_t P, int32_t* perm
 // Combine: out[t] = sum_j w[t,j] * y[perm_dst[t*k+j]] + y_shared[t] (+ resid[t]); y fp32, fp32
 // sum, one rounding to act_dtype.  resid (act_dtype) and y_shared may be null.
 cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* y_shared,
-                           const int32_t* perm_dst, const float* weight, int64_t T, int k, int d,
-                           const void* resid, void* out, int num_sms, cudaStream_t st);
+                           const int32_t* perm_dst, const float* weight, int64_t T, int k,
+                           int64_t P, int d, const void* resid, void* out, int num_sms,
+                           cudaStream_t st);
 // Block steps: y = w * x / sqrt(mean(x^2) + eps) per row (fp32, one rounding to act_dtype); and
 // y_f32 += r (r in act_dtype, n elements, n % 8 == 0).
 cudaError_t launch_rmsnorm_rows(int act_dtype, const void* x, const void* w, float eps, int64_t T,
                                 int d, void* y, int num_sms, cudaStream_t st);
 cudaError_t launch_add_residual(float* y, int act_dtype, const void* r, int64_t n, int num_sms,
                                 cudaStream_t st);
-// K3: u_hat[t] = RMSNorm?( sum_j w[t,j] * y[perm_dst[t*k+j]] ) in bf16, width L, y fp32.
+// K3: u_hat[t] = RMSNorm?( sum_j w[t,j] * y[perm_dst[t*k+j]] ) in bf16, width L, y fp32 [P][L].
 cudaError_t launch_latent_combine(const void* y_perm, const int32_t* perm_dst,
-                                  const float* weight, int64_t T, int k, int L, int norm,
-                                  float eps, void* u_hat, int num_sms, cudaStream_t st);
+                                  const float* weight, int64_t T, int k, int64_t P, int L,
+                                  int norm, float eps, void* u_hat, int num_sms,
+                                  cudaStream_t st);
 
 // A failed CUDA call as a status: MOE_OK for cudaSuccess, else MOE_ERR_CUDA with the error's name
 // and text kept for moe_last_error_string() (per host thread).

@@ -279,6 +279,54 @@ static void ready(Ctx& x) {
   (void)cudaGetLastError();  // start from a clean launch-error state
 }
 
+// Host-I/O overlap: inputs of at least kIoOverlapBytes arrive in kIoStreams pieces at once; the
+// output leaves in kIoChunks chunks, each behind its part of the combine.
+constexpr size_t kIoOverlapBytes = 32u << 20;
+constexpr int kIoStreams = 2;
+constexpr int kIoChunks = 8;
+constexpr int kIoMaxDevices = 64;
+
+struct OutCopy {
+  void* host;
+  int n;
+  cudaStream_t cs[kIoStreams];
+  cudaEvent_t ev[kIoChunks];
+};
+
+struct IoStreams {
+  bool ok = false;
+  cudaStream_t cs[kIoStreams] = {};
+  cudaEvent_t ev_start = nullptr;
+  cudaEvent_t ev_in[kIoStreams] = {};
+  cudaEvent_t ev_out[kIoStreams] = {};
+  cudaEvent_t ev_chunk[kIoChunks] = {};
+};
+static std::mutex g_io_mutex;
+static IoStreams g_io[kIoMaxDevices];
+
+// Creates the current device's copy streams and events (kept for the life of the process).
+static moe_status_t io_streams_init(IoStreams& io) {
+  const unsigned ef = cudaEventDisableTiming;
+  for (int i = 0; i < kIoStreams; ++i) {
+    if (cudaStreamCreateWithFlags(&io.cs[i], cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&io.ev_in[i], ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&io.ev_out[i], ef) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  if (cudaEventCreateWithFlags(&io.ev_start, ef) != cudaSuccess) return MOE_ERR_CUDA;
+  for (int i = 0; i < kIoChunks; ++i)
+    if (cudaEventCreateWithFlags(&io.ev_chunk[i], ef) != cudaSuccess) return MOE_ERR_CUDA;
+  io.ok = true;
+  return MOE_OK;
+}
+
+static moe_status_t forward_impl(Ctx& c, const void* x, const float* W_r, const float* b,
+                                 const void* W13, const void* W2, const float* W13_scale,
+                                 const float* W2_scale, const void* Ws13, const void* Ws2,
+                                 const float* Ws13_scale, const float* Ws2_scale,
+                                 const void* W_down, const void* W_up, void* out,
+                                 const OutCopy* oc);
+
 // ---------------------------------------------------------------------------------------------
 // Stages
 // ---------------------------------------------------------------------------------------------
@@ -659,27 +707,36 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
   return MOE_OK;
 }
 
+// The combine of tokens [t0, t0 + nt) (all tokens by default): every step of it is per token.
 static moe_status_t run_combine(Ctx& x, const void* y_perm, const int32_t* perm_dst,
                                 const float* weight, const void* W_up, void* out,
-                                const void* resid = nullptr) {
+                                const void* resid = nullptr, int64_t t0 = 0, int64_t nt = -1) {
   const moe_config_t* c = x.c;
-  if (c->T == 0) return MOE_OK;
-  const int64_t T = c->T, P = T * c->k;
+  if (nt < 0) nt = c->T - t0;
+  if (nt <= 0) return MOE_OK;
+  const int64_t T = nt, P = c->T * c->k;
   const int de = x.pl.de, d = c->d;
-  const void* y_sh =
-      c->n_shared ? static_cast<const uint8_t*>(y_perm) + (size_t)P * de * 4 : nullptr;
+  const size_t ab = dtype_bytes(c->act_dtype);
+  perm_dst += t0 * c->k;
+  weight += t0 * c->k;
+  out = static_cast<uint8_t*>(out) + (size_t)t0 * d * ab;
+  if (resid) resid = static_cast<const uint8_t*>(resid) + (size_t)t0 * d * ab;
+  // the shared expert's fp32 rows [T][d] follow the routed rows
+  const void* y_sh = c->n_shared ? static_cast<const uint8_t*>(y_perm) + (size_t)P * de * 4 +
+                                       (size_t)t0 * d * 4
+                                 : nullptr;
   if (!x.pl.latent)
-    return from_cuda(launch_combine(c->act_dtype, y_perm, y_sh, perm_dst, weight, T, c->k, d,
-                                    resid, out, x.sms, x.st));
+    return from_cuda(launch_combine(c->act_dtype, y_perm, y_sh, perm_dst, weight, T, c->k, P,
+                                    d, resid, out, x.sms, x.st));
   if (resid) {  // the residual joins the fp32 shared-expert rows the up-projection adds
     if (!y_sh) return MOE_ERR_UNSUPPORTED;
     cudaError_t e = launch_add_residual(static_cast<float*>(const_cast<void*>(y_sh)),
                                         c->act_dtype, resid, T * d, x.sms, x.st);
     if (e != cudaSuccess) return from_cuda(e);
   }
-  void* u_hat = at<void>(x.ws, x.L.u_hat);
-  cudaError_t e = launch_latent_combine(y_perm, perm_dst, weight, T, c->k, de, c->latent_norm,
-                                        c->rms_eps, u_hat, x.sms, x.st);
+  void* u_hat = at<uint8_t>(x.ws, x.L.u_hat) + (size_t)t0 * de * 2;
+  cudaError_t e = launch_latent_combine(y_perm, perm_dst, weight, T, c->k, P, de,
+                                        c->latent_norm, c->rms_eps, u_hat, x.sms, x.st);
   if (e != cudaSuccess) return from_cuda(e);
   GroupedGemm g;  // y_routed = u_hat W_up^T (+ y_shared)
   g.act_d = u_hat;
@@ -790,6 +847,23 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const float* W_
   moe_status_t s = begin(c, cfg, ws, ws_bytes, stream);
   if (s != MOE_OK) return s;
   MOE_RETURN_IF_EMPTY(cfg);
+  return forward_impl(c, x, W_r, b, W13, W2, W13_scale, W2_scale, Ws13, Ws2, Ws13_scale,
+                      Ws2_scale, W_down, W_up, out, nullptr);
+}
+
+}  // extern "C"
+
+namespace moe {
+
+static moe_status_t forward_impl(Ctx& c, const void* x, const float* W_r, const float* b,
+                                 const void* W13, const void* W2, const float* W13_scale,
+                                 const float* W2_scale, const void* Ws13, const void* Ws2,
+                                 const float* Ws13_scale, const float* Ws2_scale,
+                                 const void* W_down, const void* W_up, void* out,
+                                 const OutCopy* oc) {
+  const moe_config_t* cfg = c.c;
+  moe_status_t s;
+  void* ws = c.ws;
   if (!x || !W_r || !b || !W13 || !W2 || !out) return MOE_ERR_INVALID_ARG;
   if (cfg->n_shared && (!Ws13 || !Ws2)) return MOE_ERR_INVALID_ARG;
   if ((cfg->w_dtype == MOE_FP8_E4M3 || cfg->w_dtype == MOE_INT4) &&
@@ -814,8 +888,30 @@ moe_status_t moe_forward(const moe_config_t* cfg, const void* x, const float* W_
   if ((s = run_experts(c, x, offsets, perm_src, perm_dst, W13, W2, W13_scale, W2_scale, Ws13, Ws2,
                        Ws13_scale, Ws2_scale, W_down, y_perm)) != MOE_OK)
     return s;
-  return run_combine(c, y_perm, perm_dst, wgt, W_up, out);
+  if (!oc) return run_combine(c, y_perm, perm_dst, wgt, W_up, out);
+  // the combine in token chunks; each chunk's output leaves for the host on a copy stream while
+  // the next chunk is combined
+  const int64_t T = cfg->T;
+  const size_t row = (size_t)cfg->d * dtype_bytes(cfg->act_dtype);
+  const int64_t chunk = (T + oc->n - 1) / oc->n;
+  for (int i = 0; i * chunk < T; ++i) {
+    const int64_t t0 = i * chunk, nt = T - t0 < chunk ? T - t0 : chunk;
+    if ((s = run_combine(c, y_perm, perm_dst, wgt, W_up, out, nullptr, t0, nt)) != MOE_OK)
+      return s;
+    cudaStream_t cs = oc->cs[i % kIoStreams];
+    if (cudaEventRecord(oc->ev[i], c.st) != cudaSuccess ||
+        cudaStreamWaitEvent(cs, oc->ev[i], 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<uint8_t*>(oc->host) + (size_t)t0 * row,
+                        static_cast<const uint8_t*>(out) + (size_t)t0 * row, (size_t)nt * row,
+                        cudaMemcpyDeviceToHost, cs) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
+
+}  // namespace moe
+
+extern "C" {
 
 moe_status_t moe_forward_block(const moe_config_t* cfg, const void* x_resid, const void* norm_w,
                                const float* W_r, const float* b, const void* W13, const void* W2,
@@ -876,14 +972,53 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
   const size_t bytes = (size_t)cfg->T * cfg->d * dtype_bytes(cfg->act_dtype);
   void* x_dev = at<void>(ws, c.L.x_io);
   void* out_dev = at<void>(ws, c.L.out_io);
-  if (bytes && cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, c.st) != cudaSuccess)
-    return MOE_ERR_CUDA;
-  s = moe_forward(cfg, x_dev, W_r, b, W13, W2, W13_scale, W2_scale, Ws13, Ws2, Ws13_scale,
-                  Ws2_scale, W_down, W_up, out_dev, ws, ws_bytes, stream);
+  if (bytes < kIoOverlapBytes) {  // one copy each way on the caller's stream
+    if (cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, c.st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    s = forward_impl(c, x_dev, W_r, b, W13, W2, W13_scale, W2_scale, Ws13, Ws2, Ws13_scale,
+                     Ws2_scale, W_down, W_up, out_dev, nullptr);
+    if (s != MOE_OK) return s;
+    if (cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, c.st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return from_cuda(cudaStreamSynchronize(c.st));
+  }
+  // Large batches: the input arrives in kIoStreams pieces on as many copy streams at once, and
+  // the output leaves in chunks behind the combine.  The copy streams and their events belong to
+  // the device; one such call per device runs at a time (the call synchronises before returning).
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kIoMaxDevices) return MOE_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_io_mutex);
+  IoStreams& io = g_io[dev];
+  if (!io.ok && (s = io_streams_init(io)) != MOE_OK) return s;
+  // the copies start after the work already queued on the caller's stream (the workspace may
+  // still be in use there), and the layer starts after the input copies
+  if (cudaEventRecord(io.ev_start, c.st) != cudaSuccess) return MOE_ERR_CUDA;
+  const size_t piece = (bytes / kIoStreams + 255) & ~size_t(255);
+  for (int i = 0; i < kIoStreams; ++i) {
+    const size_t o = (size_t)i * piece;
+    if (o >= bytes) break;
+    const size_t n = bytes - o < piece ? bytes - o : piece;
+    if (cudaStreamWaitEvent(io.cs[i], io.ev_start, 0) != cudaSuccess ||
+        cudaMemcpyAsync(static_cast<uint8_t*>(x_dev) + o, static_cast<const uint8_t*>(x_host) + o,
+                        n, cudaMemcpyHostToDevice, io.cs[i]) != cudaSuccess ||
+        cudaEventRecord(io.ev_in[i], io.cs[i]) != cudaSuccess ||
+        cudaStreamWaitEvent(c.st, io.ev_in[i], 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  OutCopy oc;
+  oc.host = out_host;
+  oc.n = kIoChunks;
+  for (int i = 0; i < kIoStreams; ++i) oc.cs[i] = io.cs[i];
+  for (int i = 0; i < kIoChunks; ++i) oc.ev[i] = io.ev_chunk[i];
+  s = forward_impl(c, x_dev, W_r, b, W13, W2, W13_scale, W2_scale, Ws13, Ws2, Ws13_scale,
+                   Ws2_scale, W_down, W_up, out_dev, &oc);
+  // whatever was queued on the copy streams finishes before the caller's stream goes on
+  for (int i = 0; i < kIoStreams; ++i) {
+    if (cudaEventRecord(io.ev_out[i], io.cs[i]) != cudaSuccess ||
+        cudaStreamWaitEvent(c.st, io.ev_out[i], 0) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
   if (s != MOE_OK) return s;
-  if (bytes &&
-      cudaMemcpyAsync(out_host, out_dev, bytes, cudaMemcpyDeviceToHost, c.st) != cudaSuccess)
-    return MOE_ERR_CUDA;
   return from_cuda(cudaStreamSynchronize(c.st));
 }
 

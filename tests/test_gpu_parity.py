@@ -408,6 +408,29 @@ def test_host_io_entry_point_matches_device_path(cuda_device):
     assert torch.equal(out_host, out_dev.cpu())
 
 
+@pytest.mark.parametrize("latent", [False, True], ids=["k2", "k3_latent"])
+def test_host_io_overlapped_copies_match_device_path(cuda_device, latent):
+    """Inputs of 32 MB and more take the overlapped host-I/O path: the input in two pieces on two
+    copy streams, the combine (K3: latent combine and up-projection) in eight token chunks, each
+    copied out behind its part.  The output must equal moe_forward's bit for bit, with a ragged
+    last chunk (3001 tokens)."""
+    base = S.WORKLOADS["k3_latent_bf16" if latent else "k2_prefill_bf16"]
+    w = replace(base, name="host_io_large", E=32, T=3001)
+    layer = _layer(w, seed=21)
+    cfg = B.config_for(w)
+    ws = B.alloc_workspace(cfg)
+    assert w.T * w.d * 2 >= 32 << 20
+    out_dev = torch.empty(w.T, w.d, dtype=torch.bfloat16, device="cuda")
+    B.moe_forward(cfg, layer.x, *B.layer_weights(layer), out_dev, ws)
+    x_host = layer.x.cpu().pin_memory()
+    for _ in range(2):  # the copy streams and events are reused by a second call
+        out_host = torch.full((w.T, w.d), float("nan"), dtype=torch.bfloat16).pin_memory()
+        B.moe_forward_host_io(cfg, x_host, *B.layer_weights(layer), out_host, ws)
+        assert torch.equal(out_host, out_dev.cpu())
+    del layer, ws
+    torch.cuda.empty_cache()
+
+
 def test_forward_replays_from_a_cuda_graph(cuda_device):
     """moe_forward allocates nothing and never synchronises, so it can be captured into a CUDA
     graph; every replay must give the eager result bit for bit (decode shapes, 32 experts)."""
