@@ -196,6 +196,14 @@ cudaError_t launch_gemm_simt(const GroupedGemm& g, int num_sms, cudaStream_t st)
 cudaError_t launch_router_topk(const float* partial, int S, int64_t split_stride, int64_t T,
                                int E, int k, const float* b, float gate_scale, float* logits_out,
                                int32_t* idx, float* weight, cudaStream_t st);
+// Router logits of a small batch on the tensor cores: bf16 x [T][d] times fp32 W_r [E][d] (split
+// into three bf16 parts inside the kernel), K cut into S slices of partial logits at
+// z + s * split_stride ([T][E] each), summed in order by launch_router_topk.
+bool router_splitk_tc_supported(int64_t T, int E, int d);
+int router_splitk_tc_slices(int64_t T, int E, int d, int num_sms);
+cudaError_t launch_router_splitk_tc(const void* x, const float* W_r, int64_t T, int E, int d,
+                                    int S, float* z, int64_t split_stride, uint32_t* err,
+                                    cudaStream_t st);
 // fp32 [E][d] -> bf16 [E][3d] (hi | mid | lo) so that hi + mid + lo reproduces each weight.
 cudaError_t launch_split_router_weights(const float* W_r, int E, int d, __nv_bfloat16* out,
                                         cudaStream_t st);

@@ -84,7 +84,8 @@ struct Plan {
   bool latent;
   int de;             // expert width: d or d_latent
   bool router_tc;     // tensor-core router (3 x bf16 split weights)
-  int router_splits;  // split-K slices of the CUDA-core router
+  bool router_splitk; // tensor-core router for small batches, split over K (weights split inside)
+  int router_splits;  // split-K slices of the CUDA-core or split-K tensor-core router
   int swap;           // expert GEMM tiles: 0 token rows as M; 1 weight rows as M with 32-token
                       // tiles; 2 the same with 256-token tiles
   bool tc;            // tensor-core expert GEMMs
@@ -157,7 +158,12 @@ static Plan make_plan(const moe_config_t* c) {
   else
     p.router_tc = tc_ok && c->T >= 1024;
   p.router_splits = 1;
-  if (!p.router_tc) {
+  // small bf16 batches: the split-K tensor-core router, slices for one wave of CTAs on 152 SMs
+  p.router_splitk = !p.router_tc && !(c->flags & MOE_FLAG_ROUTER_SIMT) &&
+                    c->act_dtype == MOE_BF16 && router_splitk_tc_supported(c->T, c->E, c->d);
+  if (p.router_splitk) {
+    p.router_splits = router_splitk_tc_slices(c->T, c->E, c->d, 152);
+  } else if (!p.router_tc) {
     const int64_t tiles = ((c->T + 63) / 64) * ((c->E + 63) / 64);
     int s = (int)((304 + (tiles > 0 ? tiles : 1) - 1) / (tiles > 0 ? tiles : 1));
     if (s > 32) s = 32;
@@ -362,6 +368,14 @@ static moe_status_t run_router(Ctx& x, const void* xin, const float* W_r, const 
     return from_cuda(e);
   }
   float* zp = at<float>(x.ws, x.L.zbuf);
+  if (x.pl.router_splitk) {
+    e = launch_router_splitk_tc(xin, W_r, c->T, c->E, c->d, x.pl.router_splits, zp,
+                                c->T * c->E, x.err, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+    e = launch_router_topk(zp, x.pl.router_splits, c->T * c->E, c->T, c->E, c->k, b,
+                           c->gate_scale, logits, idx, weight, x.st);
+    return from_cuda(e);
+  }
   GroupedGemm g;
   g.act_d = xin;
   g.act_d_rows = c->T;

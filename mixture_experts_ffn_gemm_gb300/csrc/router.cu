@@ -32,11 +32,27 @@ __global__ void __launch_bounds__(kTopkWarps * 32)
 
   float key[EPL];
   float sig[EPL];
-  // the split-K slices in order; each slice's EPL loads of a lane are issued together
+  // the split-K slices summed in slice order; the loads of U slices are issued before any of
+  // them is added, so that a lane has U * EPL loads in flight
+  constexpr int U = EPL <= 12 ? 4 : 1;
   float zs[EPL];
 #pragma unroll
   for (int j = 0; j < EPL; ++j) zs[j] = 0.0f;
-  for (int s = 0; s < S; ++s) {
+  int s = 0;
+  for (; s + U <= S; s += U) {
+    float v[U][EPL];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const float* ps = partial + (s + u) * split_stride + t * E;
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) v[u][j] = lane + 32 * j < E ? ps[lane + 32 * j] : 0.0f;
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+#pragma unroll
+      for (int j = 0; j < EPL; ++j) zs[j] += v[u][j];
+  }
+  for (; s < S; ++s) {
     const float* ps = partial + s * split_stride + t * E;
 #pragma unroll
     for (int j = 0; j < EPL; ++j)

@@ -129,8 +129,7 @@ def test_fused_and_unfused_decode_agree_bit_for_bit(cuda_device):
 
 
 def test_bf16_tensor_core_router_top3(cuda_device):
-    """The tensor-core router's fused selection with k = 3 < 8 (the epilogue keeps eight
-    candidates and emits the first k) and a ragged last 128-token tile."""
+    """The tensor-core router with k = 3 < 8 and a ragged last 128-token tile."""
     w = replace(SMALL_BF16, E=128, k=3, T=1100)
     res = _full_check(_layer(w, seed=15), ROWS | B.MOE_FLAG_ROUTER_TC,
                       rows=np.arange(0, 1100, 11))
@@ -146,17 +145,41 @@ def test_bf16_tensor_core_router(cuda_device):
 
 
 def test_bf16_router_paths_agree(cuda_device):
-    """The CUDA-core split-K router and the tensor-core split router give the same selections
-    (away from near ties) and logits within fp32 accumulation error."""
+    """The CUDA-core split-K router, the tensor-core split router and the split-K tensor-core
+    router (the default below 1024 tokens) give the same selections (away from near ties) and
+    logits within fp32 accumulation error."""
     w = replace(SMALL_BF16, E=128, k=8, T=257, d=512)
     layer = _layer(w, seed=5)
     L = _lib()
     a = L.run_gpu(layer, B.MOE_FLAG_ROUTER_SIMT)
     b = L.run_gpu(layer, B.MOE_FLAG_ROUTER_TC)
-    za, zb = a.logits.cpu().double(), b.logits.cpu().double()
+    c = L.run_gpu(layer, 0)
+    za, zb, zc = (r.logits.cpu().double() for r in (a, b, c))
     assert float((za - zb).abs().max()) <= 1e-5 * float(za.abs().max())
-    L.check_routing(layer, a)
-    L.check_routing(layer, b)
+    assert float((za - zc).abs().max()) <= 1e-5 * float(za.abs().max())
+    for r in (a, b, c):
+        L.check_routing(layer, r)
+
+
+@pytest.mark.parametrize("T,E,d", [(1, 64, 256), (37, 128, 512), (128, 384, 1024),
+                                   (300, 192, 7168), (1000, 64, 512)])
+def test_splitk_tensor_core_router(cuda_device, T, E, d):
+    """The split-K tensor-core router at one token, ragged token tiles, several 64-expert
+    blocks and K slices (the slice count depends on T and E): logits against the fp64 oracle's
+    within fp32 accumulation error, selections and gates by the oracle's rule."""
+    import oracle
+    from oracle import torch_bridge as OB
+    w = replace(SMALL_BF16, E=E, k=min(8, E), T=T, d=d, I=128, I_shared=128)
+    layer = _layer(w, seed=T + E)
+    L = _lib()
+    g = L.run_gpu(layer, 0)
+    xm, W_r, b = OB.route_inputs(layer, torch.arange(T))
+    z_ref = oracle.route(OB.config(layer, T), xm, W_r, b)["logits"]
+    z = g.logits.cpu().double().numpy()
+    # fp32 accumulation of d products: bound by the sum of |x| |w| per logit
+    bound = (layer.x.double().abs() @ layer.W_r.double().abs().T).cpu().numpy()
+    assert (np.abs(z - z_ref) <= 2e-6 * bound + 1e-30).all()
+    L.check_routing(layer, g)
 
 
 def test_latent_small_all_tokens(cuda_device):
