@@ -229,7 +229,8 @@ cudaError_t launch_invert_perm(const int32_t* perm_src, int64_t P, int32_t* perm
 
 // Combine: out[t] = sum_j w[t,j] * y[perm_dst[t*k+j]] + y_shared[t] (+ resid[t]); y fp32, fp32
 // sum, one rounding to act_dtype.  resid (act_dtype) and y_shared may be null.
-cudaError_t launch_combine(int act_dtype, const void* y_perm, const void* y_shared,
+// y_perm and y_shared in fp32, or in bf16 when y_bf16 is set.
+cudaError_t launch_combine(int act_dtype, bool y_bf16, const void* y_perm, const void* y_shared,
                            const int32_t* perm_dst, const float* weight, int64_t T, int k,
                            int64_t P, int d, const void* resid, void* out, int num_sms,
                            cudaStream_t st);

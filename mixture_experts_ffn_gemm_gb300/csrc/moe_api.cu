@@ -92,6 +92,7 @@ struct Plan {
   bool fp8;           // e4m3 experts with block scales
   bool w4;            // 4-bit integer group-quantised experts
   bool fused;         // decode experts in one persistent launch (32-token swap-AB tiles)
+  bool y_bf16;        // expert outputs (y_perm and the shared rows) in bf16 instead of fp32
 };
 
 struct Layout {
@@ -115,6 +116,10 @@ static moe_status_t validate(const moe_config_t* c) {
       c->w_dtype != MOE_INT4)
     return MOE_ERR_INVALID_ARG;
   if (c->k > 32 || c->E > 1023) return MOE_ERR_UNSUPPORTED;
+  // bf16 expert outputs: bf16 experts on the K2 path
+  if ((c->flags & MOE_FLAG_EXPERT_OUT_BF16) &&
+      (c->act_dtype != MOE_BF16 || c->w_dtype != MOE_BF16 || c->d_latent > 0))
+    return MOE_ERR_UNSUPPORTED;
   if (c->n_shared && c->I_shared != c->I) return MOE_ERR_UNSUPPORTED;
   if (c->T * c->k + c->T >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
   if (c->w_dtype == MOE_FP8_E4M3) {
@@ -185,7 +190,8 @@ static Plan make_plan(const moe_config_t* c) {
   else
     p.swap = c->T <= 512 ? 1 : 0;
   // the one-launch decode experts on request only: measured slower than the two launches
-  p.fused = p.tc && !p.fp8 && !p.w4 && !p.latent && p.swap == 1 &&
+  p.y_bf16 = (c->flags & MOE_FLAG_EXPERT_OUT_BF16) != 0;
+  p.fused = p.tc && !p.fp8 && !p.w4 && !p.latent && p.swap == 1 && !p.y_bf16 &&
             (c->flags & MOE_FLAG_DECODE_FUSED) && !(c->flags & MOE_FLAG_TEST_STALL_EXPERTS) &&
             c->I % 128 == 0;
   return p;
@@ -642,7 +648,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
   // group of the same launch (on the K3 path with its own reduction length d, since it reads the
   // full-width x while the routed experts read the latent)
   const bool fuse_shared = c->n_shared && (x.pl.tc || !x.pl.latent);
-  void* y_sh = static_cast<uint8_t*>(y_perm) + (size_t)P * de * 4;
+  void* y_sh = static_cast<uint8_t*>(y_perm) + (size_t)P * de * (x.pl.y_bf16 ? 2 : 4);
   {
     GroupedGemm g;
     g.act = x_perm;
@@ -711,7 +717,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.act_dtype = g.w_dtype = c->act_dtype;
     g.out = y_perm;
     g.ldo = de;
-    g.out_dtype = MOE_F32;
+    g.out_dtype = x.pl.y_bf16 ? MOE_BF16 : MOE_F32;
     g.err = x.err;
     g.n128 = (c->flags & MOE_FLAG_GEMM_N128) != 0;
     g.pair = (c->flags & MOE_FLAG_GEMM_PAIR) && !g.n128;
@@ -736,12 +742,13 @@ static moe_status_t run_combine(Ctx& x, const void* y_perm, const int32_t* perm_
   out = static_cast<uint8_t*>(out) + (size_t)t0 * d * ab;
   if (resid) resid = static_cast<const uint8_t*>(resid) + (size_t)t0 * d * ab;
   // the shared expert's fp32 rows [T][d] follow the routed rows
-  const void* y_sh = c->n_shared ? static_cast<const uint8_t*>(y_perm) + (size_t)P * de * 4 +
-                                       (size_t)t0 * d * 4
+  const size_t yb = x.pl.y_bf16 ? 2 : 4;  // bytes per expert output
+  const void* y_sh = c->n_shared ? static_cast<const uint8_t*>(y_perm) + (size_t)P * de * yb +
+                                       (size_t)t0 * d * yb
                                  : nullptr;
   if (!x.pl.latent)
-    return from_cuda(launch_combine(c->act_dtype, y_perm, y_sh, perm_dst, weight, T, c->k, P,
-                                    d, resid, out, x.sms, x.st));
+    return from_cuda(launch_combine(c->act_dtype, x.pl.y_bf16, y_perm, y_sh, perm_dst, weight, T,
+                                    c->k, P, d, resid, out, x.sms, x.st));
   if (resid) {  // the residual joins the fp32 shared-expert rows the up-projection adds
     if (!y_sh) return MOE_ERR_UNSUPPORTED;
     cudaError_t e = launch_add_residual(static_cast<float*>(const_cast<void*>(y_sh)),

@@ -7,7 +7,8 @@ The rule, the same for every workload and every test:
     counted and reported, not compared);
   * fp32 values (the fp32 layer's outputs, the fp32 expert rows of y_perm, the shared expert's
     rows): max |GPU - oracle| <= tol * rms(oracle);
-  * values rounded to bf16 as the layer's result (bf16 and fp8-expert outputs): the same bound on
+  * values rounded to bf16 as the layer's result (bf16 and fp8-expert outputs, and the expert
+    rows of y_perm when they are bf16 on request): the same bound on
     the error beyond the result's own rounding, max(|GPU - oracle| - 2^-8 |oracle|) <= tol *
     rms(oracle).  2^-8 |v| bounds half a bf16 ulp of v, the representation error of the output
     type itself, which no bf16 result can avoid; an output near 5 rms already carries up to
@@ -72,7 +73,8 @@ def run_gpu(layer, flags: int = 0) -> GpuResult:
     perm_src = torch.full((T * k,), -7, dtype=torch.int32, device=dev)
     perm_dst = torch.full((T * k,), -7, dtype=torch.int32, device=dev)
     B.moe_permute(cfg, idx, counts, offsets, perm_src, perm_dst, ws)
-    y_perm = torch.full((T * k * de + T * w.n_shared * d,), float("nan"), dtype=torch.float32,
+    y_dtype = torch.bfloat16 if flags & B.MOE_FLAG_EXPERT_OUT_BF16 else torch.float32
+    y_perm = torch.full((T * k * de + T * w.n_shared * d,), float("nan"), dtype=y_dtype,
                         device=dev)
     B.moe_experts(cfg, layer.x, offsets, perm_src, layer.W13, layer.W2, layer.W13_scale,
                   layer.W2_scale, layer.Ws13, layer.Ws2, layer.Ws13_scale, layer.Ws2_scale,
@@ -224,7 +226,8 @@ def check_outputs(layer, g: GpuResult, rows=None, tol=None, host: HostExperts = 
     if w.n_shared:
         P, de, d = T * w.k, w.d_expert, w.d
         ysh = g.y_perm[P * de:].view(T, d).float().cpu().numpy()[rows_np]
-        res["shared_err"] = compare(ysh, ref["shared"], act, tol)["err"]
+        res["shared_err"] = compare(ysh, ref["shared"], act, tol,
+                                    rounded=g.y_perm.dtype == torch.bfloat16)["err"]
     return res
 
 
@@ -275,7 +278,8 @@ def check_expert_rows(layer, g: GpuResult, nrows: int = 64, seed: int = 0, tol=N
     with ThreadPoolExecutor(max_workers=NTHREADS) as ex:
         ref = np.stack(list(ex.map(one, range(rows.size))))
     worst = {"err": 0.0, "err_plain": 0.0, "rms_err": 0.0}
+    rounded = g.y_perm.dtype == torch.bfloat16  # bf16 expert outputs on request
     for i in range(rows.size):
-        r = compare(got[i], ref[i], kind(w), tol)
+        r = compare(got[i], ref[i], kind(w), tol, rounded=rounded)
         worst = {kk: max(worst[kk], r[kk]) for kk in worst}
     return {"expert_rows": int(rows.size), "expert_rows_err": worst["err"]}

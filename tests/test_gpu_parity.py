@@ -386,6 +386,29 @@ def test_full_k2_prefill_sm_pairs(cuda_device):
     print("k2_prefill_pairs", res)
 
 
+YBF16 = B.MOE_FLAG_EXPERT_OUT_BF16  # bf16 expert outputs (one more rounding, half the bytes)
+
+
+@pytest.mark.parametrize("flags", [ROWS | YBF16, SWAP | YBF16], ids=["rows", "swap"])
+def test_bf16_expert_outputs_small(cuda_device, flags):
+    """Expert outputs in bf16 on request: within the same parity rule (the error beyond the output
+    rounding, 2e-2 rms), with one more bf16 rounding of every expert output before the sum; the
+    sampled expert rows are compared as bf16 results under the same rule."""
+    res = _full_check(_layer(SMALL_BF16, seed=1), flags)
+    print("bf16 expert outputs", res)
+
+
+def test_full_k2_prefill_bf16_expert_outputs(cuda_device):
+    res = _full_workload("k2_prefill_bf16", YBF16)
+    print("k2_prefill_bf16_expert_outputs", res)
+
+
+def test_bf16_expert_outputs_unsupported_elsewhere(cuda_device):
+    for wl in ("k3_latent_bf16", "k2_fp8", "k2_int4_decode", "tiny_fp32"):
+        cfg = B.config_for(S.WORKLOADS[wl].with_tokens(16), flags=YBF16)
+        assert B.moe_workspace_size(cfg) == 0
+
+
 def test_k2_prefill_65536_tokens_offsets_past_2_31(cuda_device):
     """65536 tokens at the K2 widths: the permuted activations (524288 rows x 7168) and the fp32
     expert outputs hold more than 2^31 elements, so every row * width product must be 64-bit.
