@@ -389,7 +389,10 @@ def test_full_k2_prefill_sm_pairs(cuda_device):
 YBF16 = B.MOE_FLAG_EXPERT_OUT_BF16  # bf16 expert outputs (one more rounding, half the bytes)
 
 
-@pytest.mark.parametrize("flags", [ROWS | YBF16, SWAP | YBF16], ids=["rows", "swap"])
+@pytest.mark.parametrize("flags", [ROWS | YBF16, SWAP | YBF16, PAIR | YBF16, WIDE | YBF16,
+                                   ROWS | B.MOE_FLAG_GEMM_N128 | YBF16,
+                                   SWAP | B.MOE_FLAG_DECODE_FUSED | YBF16],
+                         ids=["rows", "swap", "rows_pair", "wide", "rows_n128", "swap_fused_off"])
 def test_bf16_expert_outputs_small(cuda_device, flags):
     """Expert outputs in bf16 on request: within the same parity rule (the error beyond the output
     rounding, 2e-2 rms), with one more bf16 rounding of every expert output before the sum; the
