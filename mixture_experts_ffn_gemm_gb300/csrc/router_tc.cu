@@ -150,6 +150,10 @@ __global__ void __launch_bounds__(kRtThreads, 1)
     const int kh = (t & 1) * 32;             // first of this thread's 32 channels in the K-block
     const int64_t erow = (int64_t)eb * 64 + e;
     const float* wrow = p.W_r + erow * p.d + (int64_t)kb0 * 64 + kh;
+    // the slice's later K-blocks of this row are pulled into L2 now (one 128-byte line per
+    // K-block), so that the loads below wait on L2 rather than DRAM
+    for (int i = 1; i < p.nkb; ++i)
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(wrow + i * 64));
     float4 cur[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) cur[j] = __ldg(reinterpret_cast<const float4*>(wrow) + j);
