@@ -32,7 +32,7 @@
 //                32 (w % 4) .. +31 (thread = weight row).  Per copy stage a warp reads its row's
 //                codes and scales of its two sub-blocks before any tcgen05 operation (a shared-
 //                memory read behind outstanding tcgen05 work stalls), releases the stage, then
-//                fills one TMEM sub-stage per sub-block (cfull / cempty).  Per pair of codes: one
+//                fills its group's TMEM sub-stage with both (cfull / cempty).  Per pair of codes: one
 //                mask-and-OR ((0x4300 | u) is the bf16 of 128 + u), a bf16x2 subtract of 136 and a
 //                bf16x2 multiply by the scale;
 //   warps 1, 22  MMA issuers i = 0, 1: the tile's sub-blocks of parity i (4 K-steps x 2 blocks
@@ -41,7 +41,10 @@
 //   warps 18..21 epilogue (TMEM lane quarters): reads and adds the two halves, frees the
 //                accumulator at once, then SwiGLU -> bf16 h, or plain fp32 stores.
 // TMEM columns: [0, 128) the accumulator [issuer][block] x 32 columns (one buffer: the epilogue
-// holds it only for its reads), then 6 sub-stages of 2 x 32 (sub-stage c is read by issuer c % 2).
+// holds it only for its reads), then 3 sub-stages of [block][sub-block] x 32 columns.  Per copy
+// stage each converter group fills one sub-stage with both of its 64-channel sub-blocks (one wait,
+// two TMEM stores, one release), and the two groups take the three sub-stages in turn (the group's
+// u-th use, u = 2 * copy stage + group, is sub-stage u % 3).
 // Every wait is bounded as in the other kernels.
 #include <cstring>
 #include <mutex>
@@ -74,7 +77,9 @@ struct W4Shape {
   static constexpr int TX = PSTAGE;                         // TMA bytes per copy stage
   static constexpr int ACC_COLS = 2 * 2 * kW4BN;  // [issuer][block] x 32 columns
   static constexpr int A_COL0 = ACC_COLS;
-  static constexpr int CSTAGE_COLS = 2 * kW4ACols;
+  // one sub-stage holds a converter group's two 64-channel sub-blocks of a copy stage for both
+  // blocks: [block][sub-block] x 32 columns
+  static constexpr int CSTAGE_COLS = 2 * 2 * kW4ACols;
   static constexpr int CSTAGES = (kW4TmemCols - A_COL0) / CSTAGE_COLS;
   static constexpr int TABLE_BYTES = 2 * (kW4MaxGroups + 1) * 4 + kW4Threads * 4;
   static constexpr int NBARS = 32;
@@ -83,7 +88,7 @@ struct W4Shape {
   static constexpr int RINGS = PSTAGES * PSTAGE;
   static constexpr int SMEM = 1024 + RINGS + BAR_BYTES + TABLE_BYTES;
   static_assert(PSTAGES >= 3, "not enough shared memory for the copy ring");
-  static_assert(CSTAGES >= 4 && CSTAGES % 2 == 0, "TMEM ring: even, at least 4 sub-stages");
+  static_assert(CSTAGES == 3, "TMEM ring: three sub-stages shared by the two groups in turn");
   static_assert(SMEM <= kW4SmemLimit, "shared memory");
   static_assert(2 * PSTAGES + 2 * CSTAGES + 6 <= NBARS, "barrier area too small");
   static_assert(PSTAGE % 1024 == 0 && P_PACK % 1024 == 0 && P_SCALE % 128 == 0,
@@ -253,8 +258,8 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
     const int j = ((warp - 2) >> 2) & 1;  // the block this warp expands
     const int quarter = warp & 3;         // the TMEM lanes this warp may write
     const int row = quarter * 32 + lane;
-    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + j * kW4ACols;
-    uint32_t ps = 0, pph = 0, m = 0;
+    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16) + j * 2 * kW4ACols;
+    uint32_t ps = 0, pph = 0, c = 0;  // c: copy stages seen (this group's sub-stage use 2c + grp)
     bool ok = true;
     for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
       for (int kb = 0; kb < nkb && ok; ++kb) {
@@ -286,12 +291,9 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(&pempty[ps]);
-#pragma unroll
-        for (int h = 0; h < 2; ++h, ++m) {
-          const int b = grp + 2 * h;
-          if (b >= nsub) break;
-          const uint32_t cs = grp + 2 * (m % (S::CSTAGES / 2));
-          const uint32_t cph = (m / (S::CSTAGES / 2)) & 1u;
+        {
+          // the two groups take the three sub-stages in turn: use u = 2c + grp of the ring
+          const uint32_t u = 2 * c + grp, cs = u % S::CSTAGES, cph = (u / S::CSTAGES) & 1u;
           if (lane == 0) w_ok = mbar_wait_sleep(&cempty[cs], cph ^ 1u, abort_flag, p.err) ? 1 : 0;
           w_ok = __shfl_sync(0xffffffffu, w_ok, 0);
           if (!w_ok) {
@@ -299,14 +301,19 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
             break;
           }
           tc_fence_after();
-          uint32_t a[32];
-          w4_expand_sub(q[2 * h], q[2 * h + 1], sc[2 * h], sc[2 * h + 1], a);
-          tmem_st32(t_lane + S::A_COL0 + cs * S::CSTAGE_COLS, a);
-          tmem_st_wait();
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            if (grp + 2 * h >= nsub) break;
+            uint32_t a[32];
+            w4_expand_sub(q[2 * h], q[2 * h + 1], sc[2 * h], sc[2 * h + 1], a);
+            tmem_st32(t_lane + S::A_COL0 + cs * S::CSTAGE_COLS + h * kW4ACols, a);
+          }
+          tmem_st_wait();  // both sub-blocks' stores, then one release
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&cfull[cs]);
         }
+        ++c;
         if (++ps == S::PSTAGES) {
           ps = 0;
           pph ^= 1u;
@@ -316,7 +323,7 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
   } else if (warp == 1 || warp == kW4Mma1Warp) {
     if (lane == 0) {  // ------------------------------------------------ MMA issuers
       const int me = warp == 1 ? 0 : 1;
-      uint32_t ps = 0, pph = 0, m = 0, acc_phase = 0;
+      uint32_t ps = 0, pph = 0, c = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
@@ -334,25 +341,28 @@ __global__ void __launch_bounds__(kW4Threads, 1) moe_gemm_w4_kernel(const __grid
             break;
           }
           const uint32_t tok = smem_u32(pring + ps * S::PSTAGE + S::P_TOK);
-          for (int b = me; b < nsub; b += 2, ++m) {
-            const uint32_t cs = me + 2 * (m % (S::CSTAGES / 2));
-            const uint32_t cph = (m / (S::CSTAGES / 2)) & 1u;
+          {
+            const uint32_t u = 2 * c + me, cs = u % S::CSTAGES, cph = (u / S::CSTAGES) & 1u;
             if (!mbar_wait_sleep(&cfull[cs], cph, abort_flag, p.err)) {
               ok = false;
               break;
             }
             tc_fence_after();
             const uint32_t a0 = tmem_base + S::A_COL0 + cs * S::CSTAGE_COLS;
+            for (int h = 0; h < 2 && me + 2 * h < nsub; ++h) {
+              const int b = me + 2 * h;  // this issuer's sub-blocks of the stage
 #pragma unroll
-            for (int k16 = 0; k16 < kW4Sub / 16; ++k16) {
-              const uint64_t bdesc = sw128_kmajor_desc(tok + b * kW4TokChunk + k16 * 32);
-              mma_bf16_tmem_a(d0, a0 + k16 * 8, bdesc, idesc, accum);
-              mma_bf16_tmem_a(d0 + kW4BN, a0 + kW4ACols + k16 * 8, bdesc, idesc, accum);
-              accum = 1;
+              for (int k16 = 0; k16 < kW4Sub / 16; ++k16) {
+                const uint64_t bdesc = sw128_kmajor_desc(tok + b * kW4TokChunk + k16 * 32);
+                mma_bf16_tmem_a(d0, a0 + h * kW4ACols + k16 * 8, bdesc, idesc, accum);
+                mma_bf16_tmem_a(d0 + kW4BN, a0 + 2 * kW4ACols + h * kW4ACols + k16 * 8, bdesc,
+                                idesc, accum);
+                accum = 1;
+              }
             }
             mma_commit(&cempty[cs]);
           }
-          if (!ok) break;
+          ++c;
           mma_commit(&pempty[ps]);
           if (++ps == S::PSTAGES) {
             ps = 0;
