@@ -166,11 +166,12 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power) if power else None}
 
 
-def touched_bytes(w, idx: np.ndarray) -> dict:
+def touched_bytes(w, idx: np.ndarray, y_bytes=None) -> dict:
     """Algorithmic bytes of one layer pass: the expert weights the routing touches (each once),
     the shared expert, the router weight, the input read and the output write; per kernel also the
     activations it reads and writes (h in the activation type, or e4m3 + scales for fp8 experts;
-    expert outputs in fp32)."""
+    expert outputs in fp32, or bf16 (y_bytes = 2): the library's default for e4m3 experts)."""
+    yb = y_bytes if y_bytes is not None else (2 if w.fp8 else 4)
     touched = np.unique(idx)
     ab = 4 if w.act == "f32" else 2
     int4 = getattr(w, "int4", False)
@@ -190,15 +191,15 @@ def touched_bytes(w, idx: np.ndarray) -> dict:
         # gemm13: W1|W3 of the touched experts and of the shared expert, activations in, h out
         "gemm13": len(touched) * w13 + sh13 + P * de * hb + rows_sh * w.d * hb
         + (P + rows_sh) * w.I * hb,
-        # gemm2: W2 of the touched experts and of the shared expert, h in, fp32 outputs out
-        "gemm2": len(touched) * w2 + sh2 + (P + rows_sh) * w.I * hb + P * de * 4
-        + rows_sh * w.d * 4,
+        # gemm2: W2 of the touched experts and of the shared expert, h in, expert outputs out
+        "gemm2": len(touched) * w2 + sh2 + (P + rows_sh) * w.I * hb + P * de * yb
+        + rows_sh * w.d * yb,
         "layer": len(touched) * (w13 + w2) + sh13 + sh2 + lat + w.E * w.d * 4
         + 2 * T * w.d * ab,
         # both expert GEMMs in one launch: h stays inside it (written and read back on chip or
-        # through L2), so only the weights, the activations in and the fp32 outputs count
+        # through L2), so only the weights, the activations in and the expert outputs count
         "experts_fused": len(touched) * (w13 + w2) + sh13 + sh2 + P * de * hb
-        + rows_sh * w.d * hb + P * de * 4 + rows_sh * w.d * 4,
+        + rows_sh * w.d * hb + P * de * yb + rows_sh * w.d * yb,
     }
 
 
@@ -359,11 +360,11 @@ def time_steps(step, steps: int, stream, dev, world: int):
     return ms_total, launches, prof, clocks
 
 
-def rooflines(w, idx_np, prof, ms_step) -> tuple:
+def rooflines(w, idx_np, prof, ms_step, y_bytes=None) -> tuple:
     """(dominant-kernel roofline, layer roofline, per-kernel times).  Peaks: the measured burst
     figures (the timed loop runs well under a second of tensor work), the sustained one beside."""
     peaks, peak_src = load_peaks()
-    by = touched_bytes(w, idx_np)
+    by = touched_bytes(w, idx_np, y_bytes)
     fl = flops(w, w.T)
     kernels = {k: {"ms_per_launch": v[0] / max(v[1], 1), "launches": v[1]} for k, v in prof.items()}
     ratio_fp8 = 2.0 if w.fp8 else 1.0  # an fp8 contraction: nominal dense fp8 / bf16 = 4.5 / 2.25
@@ -529,7 +530,11 @@ def measure_workload(args, w, rank: int, world: int, dev, steps: int, warmup: in
     if rank != 0:
         return res
 
-    res["roofline"], res["layer_roofline"], res["kernels"] = rooflines(w, idx_np, prof, ms_step)
+    # bytes per expert output: bf16 on request, and by default for e4m3 experts
+    y_bytes = 2 if (cfg.flags & B.MOE_FLAG_EXPERT_OUT_BF16 or
+                    (w.fp8 and not cfg.flags & B.MOE_FLAG_EXPERT_OUT_F32)) else 4
+    res["roofline"], res["layer_roofline"], res["kernels"] = rooflines(w, idx_np, prof, ms_step,
+                                                                      y_bytes)
 
     # ------------------------------------------------------------- the oracle on a sample
     if with_cpu:

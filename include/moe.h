@@ -94,9 +94,12 @@ typedef enum { MOE_F32 = 0, MOE_BF16 = 1, MOE_FP8_E4M3 = 2, MOE_INT4 = 3 } moe_d
                                        * (one M = 256 tensor-core MMA over both SMs' operands)     */
 #define MOE_FLAG_EXPERT_OUT_BF16 0x800u /* expert outputs (y_perm, the shared expert's rows) in
                                        * bf16 instead of fp32: half their bytes, one more rounding
-                                       * of every expert output before the gated sum.  bf16 experts
-                                       * on the K2 path only (else MOE_ERR_UNSUPPORTED); moe_experts
-                                       * then writes, and moe_combine reads, bf16 y_perm          */
+                                       * of every expert output before the gated sum.  bf16 or
+                                       * e4m3 experts on the K2 path only (else
+                                       * MOE_ERR_UNSUPPORTED); moe_experts then writes, and
+                                       * moe_combine reads, bf16 y_perm.  The default for e4m3
+                                       * experts                                                  */
+#define MOE_FLAG_EXPERT_OUT_F32 0x1000u /* fp32 expert outputs for e4m3 experts too            */
 /* Test hook for the failure path: the tensor-core W1|W3 expert GEMM's copy producer issues no
  * copy, so its MMA issuer's bounded wait (shortened to 50 ms under this flag) expires; the kernel
  * flags MOE_ERR_TIMEOUT in the device status, drains, frees its tensor memory and returns, and
@@ -194,8 +197,8 @@ moe_status_t moe_permute_noalloc(const moe_config_t* cfg, const int32_t* topk_id
  *   W_down    [d_latent][d] act_dtype, K3 only (else NULL)
  *   y_perm    out, fp32: [T*k][d_e] un-weighted expert outputs in permuted row order, followed
  *             by [T*n_shared][d] shared-expert outputs in token order (kept in fp32 so that the
- *             gate-weighted sum in moe_combine rounds only once; bf16, same layout, under
- *             MOE_FLAG_EXPERT_OUT_BF16).
+ *             gate-weighted sum in moe_combine rounds only once).  bf16, same layout, for e4m3
+ *             experts (unless MOE_FLAG_EXPERT_OUT_F32) and under MOE_FLAG_EXPERT_OUT_BF16.
  * fp8 (w_dtype MOE_FP8_E4M3): the activations entering both GEMMs are quantised per token per
  * quant_block channels to e4m3 with scale = amax/448 (1 for an all-zero group), accumulation in
  * fp32. */

@@ -29,6 +29,7 @@ MOE_FLAG_GEMM_M1, MOE_FLAG_GEMM_M2 = 0x40, 0x80
 MOE_FLAG_DECODE_FUSED = 0x200
 MOE_FLAG_GEMM_PAIR = 0x400
 MOE_FLAG_EXPERT_OUT_BF16 = 0x800
+MOE_FLAG_EXPERT_OUT_F32 = 0x1000
 
 EXPORTED = ("moe_workspace_size", "moe_router", "moe_permute", "moe_experts", "moe_combine",
             "moe_forward", "moe_forward_host_io", "moe_reset_device_status", "moe_device_status",

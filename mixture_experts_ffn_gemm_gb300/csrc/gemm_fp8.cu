@@ -77,8 +77,9 @@ struct F8Params {
   int32_t n_routed, w_group_rows, u_off, u_off_d;
   int32_t dense_rows, dense_act_row0, dense_out_row0;
   int32_t K, F;
-  void* out;              // SwiGLU: e4m3 h [rows][ldo]; store: fp32 [rows][ldo]
+  void* out;              // SwiGLU: e4m3 h [rows][ldo]; store: fp32 (or bf16) [rows][ldo]
   int64_t ldo;
+  int32_t out_bf16;       // store: bf16 outputs instead of fp32
   float* out_sT;          // SwiGLU: h scales [F/128][out_s_ld]
   int64_t out_s_ld;
   uint32_t* err;
@@ -156,6 +157,24 @@ __device__ __forceinline__ void store_rows_256B(uint8_t* buf, int lane, const fl
     const int r = i * 2 + (lane >> 4);
     const int j = lane & 15;
     const uint4 w = *reinterpret_cast<const uint4*>(buf + r * 256 + ((j ^ (r & 15)) << 4));
+    if (r < valid_rows) *reinterpret_cast<uint4*>(row0 + (r * pitch + j * 16)) = w;
+  }
+}
+
+// The same for 32 rows x 128 bytes (lane l holds row l: 64 bf16 as 8 x 16 bytes) through 4 KB of
+// the buffer: each read-back instruction writes four whole 128-byte row pieces.
+__device__ __forceinline__ void store_rows_128B_f8(uint8_t* buf, int lane, const uint4 (&v)[8],
+                                                   uint8_t* row0, int pitch, int valid_rows) {
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    *reinterpret_cast<uint4*>(buf + lane * 128 + ((j ^ (lane & 7)) << 4)) = v[j];
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = i * 4 + (lane >> 3);
+    const int j = lane & 7;
+    const uint4 w = *reinterpret_cast<const uint4*>(buf + r * 128 + ((j ^ (r & 7)) << 4));
     if (r < valid_rows) *reinterpret_cast<uint4*>(row0 + (r * pitch + j * 16)) = w;
   }
 }
@@ -460,7 +479,21 @@ __global__ void __launch_bounds__(kF8Threads, 1) moe_gemm_fp8_kernel(const __gri
         // acc[j], j < P, is output column ft*256 + part*P + j; acc[P + j] the same + 128
         uint8_t* dst0 = (uint8_t*)p.out +
                         ((orow - lane) * p.ldo + (int64_t)ti.ft * kF8BN + part * kF8PartCols) * 4;
-        if constexpr (kF8PartCols == 64) {
+        if (kF8PartCols == 64 && p.out_bf16) {  // bf16: 128 bytes of each row per box
+          uint8_t* b0 = (uint8_t*)p.out +
+                        ((orow - lane) * p.ldo + (int64_t)ti.ft * kF8BN + part * kF8PartCols) * 2;
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            uint4 v[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              const float* a = acc + hb * 64 + 8 * q;
+              v[q] = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                                pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+            }
+            store_rows_128B_f8(wbuf, lane, v, b0 + hb * 128 * 2, (int)p.ldo * 2, vrows);
+          }
+        } else if constexpr (kF8PartCols == 64) {
           store_rows_256B(wbuf, lane, acc, 0, dst0, (int)p.ldo * 4, vrows);
           store_rows_256B(wbuf, lane, acc, 64, dst0 + 128 * 4, (int)p.ldo * 4, vrows);
         } else {
@@ -585,6 +618,7 @@ cudaError_t launch_gemm_fp8(const Fp8Gemm& g, int num_sms, cudaStream_t st) {
   p.ldo = g.ldo;
   p.out_sT = g.out_sT;
   p.out_s_ld = g.out_s_ld;
+  p.out_bf16 = !g.swiglu && g.out_bf16 ? 1 : 0;
   p.err = g.err;
   if (g.swiglu) return launch_f8_variant<true>(p, num_sms, st, g.label);
   return launch_f8_variant<false>(p, num_sms, st, g.label);

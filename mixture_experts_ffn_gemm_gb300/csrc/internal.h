@@ -147,6 +147,7 @@ struct Fp8Gemm {
   int64_t ldo = 0;
   float* out_sT = nullptr;
   int64_t out_s_ld = 0;
+  bool out_bf16 = false;  // store mode: bf16 outputs instead of fp32
   uint32_t* err = nullptr;
   const char* label = "gemm_fp8";
 };

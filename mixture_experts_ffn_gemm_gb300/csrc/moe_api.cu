@@ -116,9 +116,10 @@ static moe_status_t validate(const moe_config_t* c) {
       c->w_dtype != MOE_INT4)
     return MOE_ERR_INVALID_ARG;
   if (c->k > 32 || c->E > 1023) return MOE_ERR_UNSUPPORTED;
-  // bf16 expert outputs: bf16 experts on the K2 path
+  // bf16 expert outputs: bf16 or e4m3 experts on the K2 path
   if ((c->flags & MOE_FLAG_EXPERT_OUT_BF16) &&
-      (c->act_dtype != MOE_BF16 || c->w_dtype != MOE_BF16 || c->d_latent > 0))
+      (c->act_dtype != MOE_BF16 || (c->w_dtype != MOE_BF16 && c->w_dtype != MOE_FP8_E4M3) ||
+       c->d_latent > 0))
     return MOE_ERR_UNSUPPORTED;
   if (c->n_shared && c->I_shared != c->I) return MOE_ERR_UNSUPPORTED;
   if (c->T * c->k + c->T >= ((int64_t)1 << 31)) return MOE_ERR_UNSUPPORTED;
@@ -190,7 +191,11 @@ static Plan make_plan(const moe_config_t* c) {
   else
     p.swap = c->T <= 512 ? 1 : 0;
   // the one-launch decode experts on request only: measured slower than the two launches
-  p.y_bf16 = (c->flags & MOE_FLAG_EXPERT_OUT_BF16) != 0;
+  // bf16 expert outputs on request, and by default for e4m3 experts: their quantisation error is
+  // far above one more bf16 rounding of each expert output, and the outputs' bytes are a large
+  // part of the W2 launch
+  p.y_bf16 = (c->flags & MOE_FLAG_EXPERT_OUT_BF16) ||
+             (p.fp8 && !(c->flags & MOE_FLAG_EXPERT_OUT_F32));
   p.fused = p.tc && !p.fp8 && !p.w4 && !p.latent && p.swap == 1 && !p.y_bf16 &&
             (c->flags & MOE_FLAG_DECODE_FUSED) && !(c->flags & MOE_FLAG_TEST_STALL_EXPERTS) &&
             c->I % 128 == 0;
@@ -525,6 +530,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g2.swiglu = false;
     g2.out = y_perm;
     g2.ldo = d;
+    g2.out_bf16 = x.pl.y_bf16;
     g2.err = x.err;
     g2.label = "gemm2_fp8";
     return from_cuda(launch_gemm_fp8(g2, x.sms, x.st));

@@ -73,7 +73,9 @@ def run_gpu(layer, flags: int = 0) -> GpuResult:
     perm_src = torch.full((T * k,), -7, dtype=torch.int32, device=dev)
     perm_dst = torch.full((T * k,), -7, dtype=torch.int32, device=dev)
     B.moe_permute(cfg, idx, counts, offsets, perm_src, perm_dst, ws)
-    y_dtype = torch.bfloat16 if flags & B.MOE_FLAG_EXPERT_OUT_BF16 else torch.float32
+    # bf16 expert outputs on request, and by default for e4m3 experts
+    y_bf16 = flags & B.MOE_FLAG_EXPERT_OUT_BF16 or (w.fp8 and not flags & B.MOE_FLAG_EXPERT_OUT_F32)
+    y_dtype = torch.bfloat16 if y_bf16 else torch.float32
     y_perm = torch.full((T * k * de + T * w.n_shared * d,), float("nan"), dtype=y_dtype,
                         device=dev)
     B.moe_experts(cfg, layer.x, offsets, perm_src, layer.W13, layer.W2, layer.W13_scale,

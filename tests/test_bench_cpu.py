@@ -83,6 +83,11 @@ def test_algorithmic_bytes_count_each_touched_expert_once():
     byq = bench.touched_bytes(wq, idx)
     assert 3 * I * d * 4.0 / (128 * 128) == 2688 * 4
     assert byq["layer"] == (8 + 1) * (44_040_192 + 2688 * 4) + E * d * 4 + 2 * T * d * 2
+    # expert outputs: bf16 by default for e4m3 experts, fp32 on request (or for bf16 experts)
+    P = T * 8
+    assert (bench.touched_bytes(wq, idx, y_bytes=4)["gemm2"] - byq["gemm2"]
+            == (P * d + T * d) * 2)
+    assert (by["gemm2"] - bench.touched_bytes(w, idx, y_bytes=2)["gemm2"] == (P * d + T * d) * 2)
 
 
 def test_traffic_ratio_is_refused_once_its_sources_change(tmp_path, monkeypatch):

@@ -406,8 +406,17 @@ def test_full_k2_prefill_bf16_expert_outputs(cuda_device):
     print("k2_prefill_bf16_expert_outputs", res)
 
 
+@pytest.mark.parametrize("flags", [0, B.MOE_FLAG_EXPERT_OUT_F32], ids=["bf16_out", "f32_out"])
+def test_fp8_experts_outputs_k2_widths(cuda_device, flags):
+    """e4m3 experts: bf16 expert outputs (the default) and fp32 ones on request, 32 experts at
+    the K2 widths, within the fp8 rule."""
+    w = replace(S.WORKLOADS["k2_fp8"], E=32, T=300)
+    res = _full_check(_layer(w, seed=23), flags)
+    print("fp8 expert outputs", flags, res)
+
+
 def test_bf16_expert_outputs_unsupported_elsewhere(cuda_device):
-    for wl in ("k3_latent_bf16", "k2_fp8", "k2_int4_decode", "tiny_fp32"):
+    for wl in ("k3_latent_bf16", "k2_int4_decode", "tiny_fp32"):
         cfg = B.config_for(S.WORKLOADS[wl].with_tokens(16), flags=YBF16)
         assert B.moe_workspace_size(cfg) == 0
 
