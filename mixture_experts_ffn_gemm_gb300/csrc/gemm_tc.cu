@@ -51,6 +51,11 @@ struct TcParams {
   CUtensorMap map_act_d;  // dense-group activations
   CUtensorMap map_w_d;    // dense-group weights
   CUtensorMap map_out;    // fp32 output [rows][ldo], box {32, 32}, 128-byte swizzle (tma_out)
+  // token-rows N = 256 tiles with one weight box per stage (big_boxes): SwiGLU, a 3D map
+  // {K, rows of one half, halves} with box {64, 128, 2} (a feature tile's W1 and W3 rows in one
+  // copy); store, a 2D map with box {64, 256}
+  CUtensorMap map_wb;
+  CUtensorMap map_wb_d;
   const int32_t* offsets;
   int32_t n_routed, w_group_rows, u_off, u_off_d;
   int32_t dense_rows, dense_act_row0, dense_out_row0;
@@ -68,7 +73,18 @@ struct TcParams {
   uint64_t wait_ns;     // limit of every mbarrier wait
   int32_t test_stall;   // test hook: the producer issues no copy, so the MMA's wait expires
   int32_t dense_band;   // the dense group's tiles in bands of this many row tiles (0: one band)
+  int32_t big_boxes;    // weights copied in one box per stage (map_wb / map_wb_d): one copy
+                        // fewer per stage, measured 1-1.5% faster at prefill
 };
+
+__device__ __forceinline__ void tma_load_3d_tc(void* smem_dst, const CUtensorMap* map,
+                                               uint64_t* bar, int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
 
 template <bool kSwap, int kBN, int kEpi, int kMH = 1, bool kPair = false>
 struct TcShape {
@@ -247,7 +263,14 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
           if (!kSwap) {
             tma_load_2d(sa, ma, &full[stage], ax, act_y);
             if (half1) tma_load_2d(sa + kBoxBytes, ma, &full[stage], ax, act_y + 128);
-            if (S::kSwiGLU) {
+            if (kBN == 256 && kMH == 1 && p.big_boxes) {
+              const CUtensorMap* mwb = ti.dense ? &p.map_wb_d : &p.map_wb;
+              if (S::kSwiGLU)  // W1 rows (half 2g) and W3 rows (half 2g + 1) of the feature tile
+                tma_load_3d_tc(sb, mwb, &full[stage], kx, ti.ft * S::FPT,
+                               ti.dense ? 0 : 2 * ti.g);
+              else
+                tma_load_2d(sb, mwb, &full[stage], kx, w_y);
+            } else if (S::kSwiGLU) {
               tma_load_2d(sb, mw, &full[stage], kx, w_y);
               tma_load_2d(sb + kBoxBytes, mw, &full[stage], kx, w_y + u_off);
             } else {
@@ -625,6 +648,22 @@ bool make_map_bf16(CUtensorMap* m, const void* base, int64_t rows, int64_t cols,
          CUDA_SUCCESS;
 }
 
+// 3D bf16 map over [halves][rows][cols] (halves rows apart), box {64 cols, 128 rows, 2 halves},
+// 128-byte swizzle: one copy of the W1 rows of a feature tile and the matching W3 rows.
+static bool make_map_bf16_3d(CUtensorMap* m, const void* base, int64_t cols, int64_t rows,
+                             int64_t halves) {
+  EncodeTiledFn enc = encode_fn();
+  if (!enc || !base || rows <= 0 || cols <= 0 || halves < 2) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)halves};
+  cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)rows * cols * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kBK, 128, 2};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 // fp32 output [rows][cols] for bulk stores of 32 x 32 chunks (128-byte swizzle in shared memory).
 static bool make_map_f32_out(CUtensorMap* m, void* base, int64_t rows, int64_t cols) {
   EncodeTiledFn enc = encode_fn();
@@ -770,6 +809,28 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
       p.dense_band = 1;
     else
       p.dense_band = 16;
+  }
+  // one weight box per stage for token-rows N = 256 tiles (not the pair / two-M-half variants)
+  if (!swap && g.big_boxes && !g.pair && g.m_halves != 2 &&
+      (g.epi == EPI_SWIGLU || (g.epi == EPI_STORE && !f32_router && !g.n128))) {
+    bool ok = true;
+    if (g.epi == EPI_SWIGLU) {
+      // W1 | W3 stacked per expert: [groups * 2 halves][half rows][K]
+      if (g.n_routed > 0)
+        ok = ok && g.u_off % 128 == 0 && g.w_group_rows == 2 * g.u_off &&
+             make_map_bf16_3d(&p.map_wb, g.w, g.K, g.u_off, g.w_rows / g.u_off);
+      if (g.dense_rows > 0)
+        ok = ok && g.u_off_d % 128 == 0 && g.w_d_rows == 2 * g.u_off_d &&
+             make_map_bf16_3d(&p.map_wb_d, g.w_d, K_d, g.u_off_d, 2);
+    } else {
+      if (g.n_routed > 0) ok = ok && make_map_bf16(&p.map_wb, g.w, g.w_rows, g.K, 256);
+      if (g.dense_rows > 0) ok = ok && make_map_bf16(&p.map_wb_d, g.w_d, g.w_d_rows, K_d, 256);
+    }
+    if (ok) {
+      if (g.n_routed == 0) p.map_wb = p.map_wb_d;
+      if (g.dense_rows == 0) p.map_wb_d = p.map_wb;
+      p.big_boxes = 1;
+    }
   }
   p.test_stall = g.test_stall ? 1 : 0;
   p.wait_ns = g.test_stall ? 50000000ull : kWaitLimitNs;

@@ -69,6 +69,7 @@ struct GroupedGemm {
   bool n128 = false;           // token-rows store tiles with N = 128 (MOE_FLAG_GEMM_N128)
   int m_halves = 0;            // token-rows SwiGLU tiles of 1 or 2 M halves (0: one)
   bool pair = false;           // token-rows tiles of 256 rows on a CTA pair (cta_group::2)
+  bool big_boxes = true;       // token-rows N = 256 tiles: the weights in one copy per stage
 };
 
 // Tensor-core grouped GEMM (tcgen05 + TMA), bf16 operands, fp32 accumulation in TMEM.
