@@ -263,8 +263,11 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
 
 /* The dense SwiGLU MLP of the first block(s), [NN-PRINT] and [K2-CODE]:
  *   y = (SiLU(x W1^T) * (x W3^T)) W2^T, with no router, experts or gates.
- * It runs on the same grouped GEMM kernels as the experts, as one dense group (token-rows tiles;
- * at T <= 256 the W2 GEMM uses 128-column tiles so that more CTAs stream its weights).
+ * It runs on the same grouped GEMM kernels as the experts, as one dense group (token-rows tiles).
+ * With bf16 and few tokens the W2 GEMM has too few output tiles to keep the GPU's memory busy: its
+ * tiles are then split over up to 8 consecutive ranges of I into fp32 partial sums, which one
+ * more kernel adds in range order and rounds once to bf16 (T <= 256 with no split: 128-column
+ * tiles instead).
  *   T, d, I     tokens, hidden width, intermediate width (d % 256 == 0 and I % 128 == 0 for
  *               bf16; d % 16 == 0 and I % 16 == 0 for fp32)
  *   act_dtype   MOE_BF16 (tensor cores, fp32 accumulation, h rounded to bf16) or MOE_F32
@@ -273,8 +276,8 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
  *   W13         [2I][d]: the I rows of W1 (gate_proj), then the I rows of W3 (up_proj)
  *   W2          [d][I]   (down_proj)
  *   out         [T][d]   y, each element rounded once from its fp32 accumulation
- *   ws          workspace of at least moe_dense_mlp_workspace_size() bytes (holds h [T][I] and the
- *               status word); ws_bytes its size
+ *   ws          workspace of at least moe_dense_mlp_workspace_size() bytes (holds h [T][I], the
+ *               status word and any fp32 partial sums of W2); ws_bytes its size
  * Errors: MOE_ERR_INVALID_ARG (null pointer, non-positive width, misalignment),
  * MOE_ERR_UNSUPPORTED (dtype or width the kernels do not take), MOE_ERR_WORKSPACE (ws too small),
  * MOE_ERR_CUDA.  T == 0 is a no-op. */

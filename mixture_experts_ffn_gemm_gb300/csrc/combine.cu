@@ -214,4 +214,49 @@ cudaError_t launch_latent_combine(const void* y_perm, const int32_t* perm_dst,
   return cudaGetLastError();
 }
 
+// out[i] = RN(sum_s part[s * n + i]) over the k-split partials in slice order (fp32 sum, one
+// rounding to bf16): the last step of a split-K dense projection.  8 values per thread; the S
+// slices' loads are issued before any is added.
+template <int S>
+__global__ void splitk_sum_kernel(const float* __restrict__ part, int64_t n,
+                                  __nv_bfloat16* __restrict__ out) {
+  for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 8; i < n;
+       i += (int64_t)gridDim.x * blockDim.x * 8) {
+    float v[S][8];
+#pragma unroll
+    for (int sl = 0; sl < S; ++sl) load8(part + (int64_t)sl * n + i, v[sl]);
+#pragma unroll
+    for (int sl = 1; sl < S; ++sl)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) v[0][j] += v[sl][j];
+    store8(out + i, v[0]);
+  }
+}
+
+cudaError_t launch_splitk_sum(const float* part, int S, int64_t n, void* out, int num_sms,
+                              cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  if (S < 1 || S > 8 || n % 8) return cudaErrorInvalidValue;
+  const int64_t want = (n / 8 + 255) / 256;
+  const unsigned blocks = (unsigned)(want < (int64_t)num_sms * 8 ? want : (int64_t)num_sms * 8);
+  LaunchScope ls("splitk_sum", st);
+  __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out);
+  switch (S) {
+#define MOE_SPLITK_CASE(NS) \
+  case NS:                  \
+    splitk_sum_kernel<NS><<<blocks, 256, 0, st>>>(part, n, o); \
+    break;
+    MOE_SPLITK_CASE(1)
+    MOE_SPLITK_CASE(2)
+    MOE_SPLITK_CASE(3)
+    MOE_SPLITK_CASE(4)
+    MOE_SPLITK_CASE(5)
+    MOE_SPLITK_CASE(6)
+    MOE_SPLITK_CASE(7)
+    MOE_SPLITK_CASE(8)
+#undef MOE_SPLITK_CASE
+  }
+  return cudaGetLastError();
+}
+
 }  // namespace moe

@@ -75,6 +75,10 @@ struct TcParams {
   int32_t dense_band;   // the dense group's tiles in bands of this many row tiles (0: one band)
   int32_t big_boxes;    // weights copied in one box per stage (map_wb / map_wb_d): one copy
                         // fewer per stage, measured 1-1.5% faster at prefill
+  // split-K (a dense-only fp32 store launch with few row tiles): every output tile is computed
+  // as ksplit partial sums over consecutive K ranges, partial s written split_rows rows further
+  int32_t ksplit;
+  int64_t split_rows;
 };
 
 __device__ __forceinline__ void tma_load_3d_tc(void* smem_dst, const CUtensorMap* map,
@@ -218,7 +222,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int G = p.n_routed + (p.dense_rows > 0 ? 1 : 0);
-  const int total = tile_start[G];
+  const int total = tile_start[G] * p.ksplit;  // (tile, K range) pairs
   const int nkb_r = p.K / kBK, nkb_d = p.K_d / kBK;
 
   if (warp == 0) {
@@ -228,19 +232,22 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
       int armed = 0;
       bool ok = true;
       for (int tile = tile0; tile < total && ok; tile += tstep) {
-        const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
-                                        p.dense_rows, p.dense_act_row0, S::RPT, p.dense_band);
+        const int ks = tile % p.ksplit;
+        const TileInfo ti = decode_tile(tile / p.ksplit, tile_start, row_start, p.offsets,
+                                        p.n_routed, p.dense_rows, p.dense_act_row0, S::RPT,
+                                        p.dense_band);
         const CUtensorMap* ma = ti.dense ? &p.map_act_d : &p.map_act;
         const CUtensorMap* mw = ti.dense ? &p.map_w_d : &p.map_w;
         const int act_y = ti.grp_row0 + ti.rt * S::RPT;
         const int w_y = (ti.dense ? 0 : ti.g * p.w_group_rows) + ti.ft * S::FPT;
         const int u_off = ti.dense ? p.u_off_d : p.u_off;
-        const int nkb = ti.dense ? nkb_d : nkb_r;
+        const int nkb_all = ti.dense ? nkb_d : nkb_r;
+        const int kb0 = ks * nkb_all / p.ksplit, nkb = (ks + 1) * nkb_all / p.ksplit;
         const int kwrap = ti.dense ? p.k_wrap_d : p.k_wrap;
         // the second M half's rows are copied only when the tile has rows there
         const bool half1 = kMH == 2 && ti.valid > 128;
         const uint32_t tx = (kMH == 2 && !half1) ? S::STAGE - kBoxBytes : S::STAGE;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = kb0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, p.err, p.wait_ns)) {
             ok = false;
             break;
@@ -314,9 +321,12 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       bool ok = true;
       for (int tile = tile0; tile < total && ok; tile += tstep) {
-        const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
-                                        p.dense_rows, p.dense_act_row0, S::RPT, p.dense_band);
-        const int nkb = ti.dense ? nkb_d : nkb_r;
+        const int ks = tile % p.ksplit;
+        const TileInfo ti = decode_tile(tile / p.ksplit, tile_start, row_start, p.offsets,
+                                        p.n_routed, p.dense_rows, p.dense_act_row0, S::RPT,
+                                        p.dense_band);
+        const int nkb_all = ti.dense ? nkb_d : nkb_r;
+        const int kb0 = ks * nkb_all / p.ksplit, nkb = (ks + 1) * nkb_all / p.ksplit;
         // swap-AB tiles: the MMA's N is the tile's token count rounded up to 16, so a group's
         // last, partial tile costs only the tokens it holds
         uint32_t idesc = kIdesc;
@@ -332,7 +342,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
           break;
         tc_fence_after();
         const uint32_t d0 = tmem_base + acc * S::ACC_COLS;
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = kb0; kb < nkb; ++kb) {
           if (!mbar_wait(&full[stage], phase, abort_flag, p.err, p.wait_ns)) {
             ok = false;
             break;
@@ -342,7 +352,7 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
           const uint32_t sb = sa + S::OPA;
 #pragma unroll
           for (int k16 = 0; k16 < kBK / 16; ++k16) {
-            const uint32_t accum = (kb | k16) != 0;
+            const uint32_t accum = ((kb - kb0) | k16) != 0;
             const uint64_t bdesc = sw128_kmajor_desc(sb + k16 * 32);
             if constexpr (kBN > 256) {  // N = 384: an N = 256 and an N = 128 MMA side by side
               const uint64_t adesc = sw128_kmajor_desc(sa + k16 * 32);
@@ -393,8 +403,10 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
     const int r = quarter * 32 + lane;  // tile row (rows) or tile feature (swap)
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = tile0; tile < total; tile += tstep) {
-      const TileInfo ti = decode_tile(tile, tile_start, row_start, p.offsets, p.n_routed,
-                                      p.dense_rows, p.dense_act_row0, S::RPT, p.dense_band);
+      const int ks = tile % p.ksplit;
+      const TileInfo ti = decode_tile(tile / p.ksplit, tile_start, row_start, p.offsets,
+                                      p.n_routed, p.dense_rows, p.dense_act_row0, S::RPT,
+                                      p.dense_band);
       int ok = 1;
       if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, abort_flag, p.err, p.wait_ns) ? 1 : 0;
       ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -405,7 +417,8 @@ __global__ void __launch_bounds__(kTcThreads, 1) moe_gemm_tc_kernel(const __grid
       const uint32_t tb = tmem_base + acc * S::ACC_COLS + ((uint32_t)(quarter * 32) << 16);
       // a pair: this CTA's accumulator holds the tile's rows 128 * rank .. +127
       const int64_t out_row0 = (ti.dense ? (int64_t)p.dense_out_row0 : (int64_t)ti.grp_row0) +
-                               (int64_t)ti.rt * S::RPT + (kPair ? (int64_t)rank * 128 : 0);
+                               (int64_t)ti.rt * S::RPT + (kPair ? (int64_t)rank * 128 : 0) +
+                               (int64_t)ks * p.split_rows;
       const int vt = kPair ? ti.valid - (int)rank * 128 : ti.valid;  // rows of this CTA's part
       void* const out = ti.dense ? p.out_d : p.out;
       const int64_t ldo = ti.dense ? p.ldo_d : p.ldo;
@@ -787,12 +800,25 @@ cudaError_t launch_gemm_tc(const GroupedGemm& g, int swap, int num_sms, cudaStre
       (reinterpret_cast<uintptr_t>(g.out) & 15) == 0) {
     const int64_t routed_end = g.n_routed > 0 ? g.act_rows : 0;
     const int64_t dense_end = g.dense_rows > 0 ? (int64_t)g.dense_out_row0 + g.dense_rows : 0;
-    const int64_t out_rows = routed_end > dense_end ? routed_end : dense_end;
+    int64_t out_rows = routed_end > dense_end ? routed_end : dense_end;
+    if (g.k_splits > 1 && g.ldo > 0)  // every partial
+      out_rows = (int64_t)g.k_splits * (g.split_stride / g.ldo);
     if (out_rows > 0 && make_map_f32_out(&p.map_out, g.out, out_rows, g.ldo)) p.tma_out = 1;
   }
   p.addend = (const float*)g.addend;
   p.ld_add = g.ld_add;
   p.err = g.err;
+  p.ksplit = 1;
+  if (g.k_splits > 1) {
+    // dense-only token-rows fp32 stores into one tensor; every K range at least one K-block;
+    // the partials a whole number of rows apart, none overlapping the next
+    if (swap || g.n_routed > 0 || g.epi != EPI_STORE || !p.out_f32 || g.pair || g.n128 ||
+        g.out_d || g.k_splits > K_d / kBK || g.ldo <= 0 || g.split_stride % g.ldo ||
+        g.split_stride / g.ldo < (int64_t)g.dense_out_row0 + g.dense_rows)
+      return cudaErrorInvalidValue;
+    p.ksplit = g.k_splits;
+    p.split_rows = g.split_stride / g.ldo;
+  }
   // Tile order of the dense group.  Activations that fit in L2 are re-read from there by every
   // feature tile (one band: the weights stream once).  Larger activations with weights that fit in
   // L2 stream once, row tile by row tile (the K3 down-projection: 117 MB of x, 51 MB of W_down;

@@ -60,7 +60,8 @@ struct GroupedGemm {
   int out_dtype = MOE_BF16;
   const void* addend = nullptr;  // EPI_STORE_ADD: fp32 [rows][ld_add], indexed like out
   int64_t ld_add = 0;
-  // split-K (SIMT router only): out slice s at out + s * split_stride elements
+  // split-K (the SIMT router; dense-only tensor-core fp32 stores): the partial sum over the s-th
+  // of k_splits consecutive K ranges at out + s * split_stride elements
   int k_splits = 1;
   int64_t split_stride = 0;
   uint32_t* err = nullptr;
@@ -242,6 +243,10 @@ cudaError_t launch_rmsnorm_rows(int act_dtype, const void* x, const void* w, flo
                                 int d, void* y, int num_sms, cudaStream_t st);
 cudaError_t launch_add_residual(float* y, int act_dtype, const void* r, int64_t n, int num_sms,
                                 cudaStream_t st);
+// out (bf16, n values) = the fp32 sum of S partials part[s * n .. s * n + n), in slice order,
+// rounded once; 1 <= S <= 8, n % 8 == 0.
+cudaError_t launch_splitk_sum(const float* part, int S, int64_t n, void* out, int num_sms,
+                              cudaStream_t st);
 // K3: u_hat[t] = RMSNorm?( sum_j w[t,j] * y[perm_dst[t*k+j]] ) in bf16, width L, y fp32 [P][L].
 cudaError_t launch_latent_combine(const void* y_perm, const int32_t* perm_dst,
                                   const float* weight, int64_t T, int k, int64_t P, int L,

@@ -1052,9 +1052,23 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
 // The dense SwiGLU MLP: one dense group through the expert GEMMs (W1|W3 + SwiGLU -> h in the
 // workspace, then W2 straight into `out`): token-rows tensor-core tiles for bf16, CUDA cores for
 // fp32.
+// K ranges of the W2 launch: with few tokens its d / 256 output tiles leave most SMs idle, so
+// each tile is computed as partial sums over consecutive K ranges (fp32 partials, then one sum
+// kernel), as many as one wave of CTAs on 152 SMs holds, at most 8.  1: no split.
+static int dense_w2_splits(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtype) {
+  if (act_dtype != MOE_BF16 || T <= 0 || d % 256 || I % 128) return 1;
+  const int64_t tiles = ((T + 127) / 128) * (d / 256);
+  int64_t s = 152 / tiles;
+  if (s > I / 64) s = I / 64;
+  if (s > 8) s = 8;
+  return s >= 2 ? (int)s : 1;
+}
+
 size_t moe_dense_mlp_workspace_size(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtype) {
   if (T < 0 || d <= 0 || I <= 0 || (act_dtype != MOE_BF16 && act_dtype != MOE_F32)) return 0;
-  return 256 + moe::align256((size_t)T * (size_t)I * moe::dtype_bytes(act_dtype));
+  const int splits = dense_w2_splits(T, d, I, act_dtype);
+  return 256 + moe::align256((size_t)T * (size_t)I * moe::dtype_bytes(act_dtype)) +
+         (splits > 1 ? moe::align256((size_t)splits * T * d * 4) : 0);
 }
 
 moe_status_t moe_dense_mlp(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtype, const void* x,
@@ -1078,12 +1092,15 @@ moe_status_t moe_dense_mlp(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtyp
   (void)cudaGetLastError();
   uint32_t* err = at<uint32_t>(ws, 0);
   void* h = at<void>(ws, 256);
+  const int splits = dense_w2_splits(T, d, I, act_dtype);
+  float* part = at<float>(ws, 256 + align256((size_t)T * (size_t)I * dtype_bytes(act_dtype)));
   if (cudaMemsetAsync(err, 0, 256, st) != cudaSuccess) return MOE_ERR_CUDA;
   // Token-rows tiles in every regime: with few tokens one CTA streams each weight tile once
   // (swap-AB tiles of 32 tokens would have several CTAs stream the same tile, so that only a
   // fraction of the bytes in flight are distinct and HBM runs latency-bound).  W2 then has only
-  // d / 256 feature tiles; at small T its 128-column variant doubles the CTAs streaming it.
-  const bool n128_2 = T <= 256;
+  // d / 256 feature tiles; at small T it is split over K (dense_w2_splits), else its 128-column
+  // variant doubles the CTAs streaming it.
+  const bool n128_2 = T <= 256 && splits == 1;
   cudaError_t e;
   {
     GroupedGemm g;
@@ -1118,14 +1135,20 @@ moe_status_t moe_dense_mlp(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtyp
     g.F = d;
     g.epi = EPI_STORE;
     g.act_dtype = g.w_dtype = act_dtype;
-    g.out = out;
+    g.out = splits > 1 ? static_cast<void*>(part) : out;
     g.ldo = d;
-    g.out_dtype = act_dtype;
+    g.out_dtype = splits > 1 ? MOE_F32 : act_dtype;
+    g.k_splits = splits;
+    g.split_stride = T * d;
     g.err = err;
     g.n128 = n128_2;
-    g.label = tc ? "dense_gemm2_rows" : "dense_gemm2_simt";
+    g.label = !tc ? "dense_gemm2_simt" : splits > 1 ? "dense_gemm2_rows_splitk" : "dense_gemm2_rows";
     e = tc ? launch_gemm_tc(g, 0, sms, st) : launch_gemm_simt(g, sms, st);
     if (e != cudaSuccess) return from_cuda(e);
+    if (splits > 1) {
+      e = launch_splitk_sum(part, splits, T * d, out, sms, st);
+      if (e != cudaSuccess) return from_cuda(e);
+    }
   }
   return MOE_OK;
 }

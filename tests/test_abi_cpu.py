@@ -129,7 +129,17 @@ def test_dense_mlp_host_validation(moelib):
     bf, f32 = B.MOE_BF16, B.MOE_F32
     T, d, I = 16, 7168, 18432
     need = moelib.moe_dense_mlp_workspace_size(T, d, I, bf)
-    assert need == 256 + ((T * I * 2 + 255) // 256) * 256
+    a256 = lambda n: (n + 255) // 256 * 256
+    # 16 tokens: the W2 GEMM's 28 output tiles are split over 5 ranges of I (fp32 partials), as
+    # many as one wave of 152 CTAs holds; 16384 tokens fill the GPU without a split; no split in fp32
+    assert need == 256 + a256(T * I * 2) + a256(5 * T * d * 4)
+    assert moelib.moe_dense_mlp_workspace_size(16384, d, I, bf) == 256 + a256(16384 * I * 2)
+    assert moelib.moe_dense_mlp_workspace_size(T, d, I, f32) == 256 + a256(T * I * 4)
+    # few output tiles: at most 8 ranges, and never more ranges than 64-wide K-blocks
+    assert moelib.moe_dense_mlp_workspace_size(T, 256, 1024, bf) == 256 + a256(T * 1024 * 2) + \
+        a256(8 * T * 256 * 4)
+    assert moelib.moe_dense_mlp_workspace_size(T, 256, 128, bf) == 256 + a256(T * 128 * 2) + \
+        a256(2 * T * 256 * 4)
     assert moelib.moe_dense_mlp_workspace_size(-1, d, I, bf) == 0
     assert moelib.moe_dense_mlp_workspace_size(T, d, I, B.MOE_FP8_E4M3) == 0
     f = moelib.moe_dense_mlp

@@ -2,8 +2,9 @@
 
 The dense MLP of the first block is y = (SiLU(x W1) * (x W3)) W2 per token (nnterp "kimi_k2",
 "Printout": layer 0's DeepseekV3MLP).  The library runs it as one dense group through the expert
-GEMMs: token-rows tensor-core tiles for bf16 (W2 in 128-column tiles at T <= 256), CUDA cores for
-fp32.
+GEMMs: token-rows tensor-core tiles for bf16, CUDA cores for fp32.  When the W2 GEMM has fewer
+output tiles than one wave of CTAs holds (few tokens, or a narrow d), each tile is computed as
+fp32 partial sums over up to 8 ranges of I that one more kernel adds in range order.
 The parity rule of the layer (parity_lib): tol 1e-4 (fp32) / 2e-2 (bf16) of rms(oracle), for bf16
 beyond the output's own rounding, the plain figure reported beside it."""
 from dataclasses import replace
@@ -60,13 +61,15 @@ def test_dense_fp32_cuda_cores(cuda_device, T):
 
 @pytest.mark.parametrize("T", [1, 33, 200, 256])
 def test_dense_bf16_few_tokens(cuda_device, T):
-    """T <= 256: one or two 128-row token tiles, W2 in 128-column store tiles, ragged tails."""
+    """T <= 256: one or two 128-row token tiles, ragged tails; W2 split over 6 ranges of I."""
     _check(_dense("k2_dense_decode_bf16", T=T, d=512, I=384))
 
 
-@pytest.mark.parametrize("T", [257, 700, 1300])
+@pytest.mark.parametrize("T", [257, 700, 1300, 5000])
 def test_dense_bf16_many_tokens(cuda_device, T):
-    """T > 256: token-rows tiles (128 rows x 256 weight rows), several tiles and a ragged tail."""
+    """T > 256: token-rows tiles (128 rows x 256 weight rows), several tiles and a ragged tail.
+    With d = 512 the W2 GEMM has 2 output tiles per row tile: split over 6 ranges of I up to 1300
+    tokens, unsplit at 5000 (80 tiles)."""
     _check(_dense("k2_dense_prefill_bf16", T=T, d=512, I=384))
 
 
@@ -84,6 +87,14 @@ def test_dense_k2_block0_decode_full_size(cuda_device):
     """The K2 block-0 widths (d = 7168, I = 18432) at the decode batch (128 tokens), compared on
     every token."""
     _check(_dense("k2_dense_decode_bf16"))
+
+
+def test_dense_k2_block0_two_row_tiles_split_in_two(cuda_device):
+    """K2 block-0 widths at 200 tokens: 56 W2 output tiles, so two ranges of I; compared on 40
+    tokens, 20 of them in the ragged second row tile."""
+    L = _dense("k2_dense_decode_bf16", T=200, seed=4)
+    rows = np.concatenate([S.subset_rows(128, 20, seed=5), 128 + S.subset_rows(72, 20, seed=6)])
+    _check(L, rows=rows)
 
 
 def test_dense_k2_block0_prefill_sampled(cuda_device):
