@@ -250,10 +250,14 @@ moe_status_t moe_forward_block(const moe_config_t* cfg, const void* x_resid, con
 /* The whole layer from HOST buffers: copies x (pinned or pageable host memory, [T][d] act_dtype)
  * to the workspace, runs moe_forward on resident device weights, and copies the output back to
  * out_host ([T][d] act_dtype).  Synchronises `stream` before returning.  Weights stay device
- * pointers.  From 32 MB of input on, the copies overlap: x arrives in two pieces on two copy
- * streams at once, and the output leaves in eight token chunks, each copied while the next is
- * combined.  Those copy streams and their events are created once per device and shared, so such
- * calls on one device are serialised by a lock for their duration. */
+ * pointers.  From 32 MB of input on, the copies overlap: x arrives in up to eight token chunks of
+ * at least 2048 tokens on two copy streams, and for bf16 layers with a shared expert (default
+ * tile shapes) each chunk's shared-expert rows are computed while the next chunk is copied, with
+ * the same kernels and results bit for bit as in moe_forward, where the shared expert rides in
+ * the routed launches; otherwise x arrives in two pieces at once.  The output leaves in eight
+ * token chunks, each copied while the next is combined.  Those copy streams and their events are
+ * created once per device and shared, so such calls on one device are serialised by a lock for
+ * their duration. */
 moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, const float* W_r,
                                  const float* b, const void* W13, const void* W2,
                                  const float* W13_scale, const float* W2_scale, const void* Ws13,

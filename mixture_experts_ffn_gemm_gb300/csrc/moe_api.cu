@@ -265,6 +265,9 @@ struct Ctx {
   cudaStream_t st;
   int sms;
   uint32_t* err;
+  // the shared expert's rows are already computed (host-I/O path, chunk by chunk as the input
+  // arrives) and the status word already reset: the routed launches carry no dense group
+  bool shared_done = false;
 };
 
 static moe_status_t begin(Ctx& x, const moe_config_t* c, void* ws, size_t ws_bytes,
@@ -296,11 +299,14 @@ static void ready(Ctx& x) {
   (void)cudaGetLastError();  // start from a clean launch-error state
 }
 
-// Host-I/O overlap: inputs of at least kIoOverlapBytes arrive in kIoStreams pieces at once; the
+// Host-I/O overlap: inputs of at least kIoOverlapBytes arrive in kIoStreams pieces at once, or,
+// for bf16 layers with a shared expert, in up to kIoChunks token chunks of at least
+// kIoMinChunkTokens, each chunk's shared-expert rows computed while the next chunk is copied; the
 // output leaves in kIoChunks chunks, each behind its part of the combine.
 constexpr size_t kIoOverlapBytes = 32u << 20;
 constexpr int kIoStreams = 2;
 constexpr int kIoChunks = 8;
+constexpr int64_t kIoMinChunkTokens = 2048;
 constexpr int kIoMaxDevices = 64;
 
 struct OutCopy {
@@ -317,6 +323,7 @@ struct IoStreams {
   cudaEvent_t ev_in[kIoStreams] = {};
   cudaEvent_t ev_out[kIoStreams] = {};
   cudaEvent_t ev_chunk[kIoChunks] = {};
+  cudaEvent_t ev_in_chunk[kIoChunks] = {};
 };
 static std::mutex g_io_mutex;
 static IoStreams g_io[kIoMaxDevices];
@@ -332,7 +339,9 @@ static moe_status_t io_streams_init(IoStreams& io) {
   }
   if (cudaEventCreateWithFlags(&io.ev_start, ef) != cudaSuccess) return MOE_ERR_CUDA;
   for (int i = 0; i < kIoChunks; ++i)
-    if (cudaEventCreateWithFlags(&io.ev_chunk[i], ef) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaEventCreateWithFlags(&io.ev_chunk[i], ef) != cudaSuccess ||
+        cudaEventCreateWithFlags(&io.ev_in_chunk[i], ef) != cudaSuccess)
+      return MOE_ERR_CUDA;
   io.ok = true;
   return MOE_OK;
 }
@@ -653,7 +662,7 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
   // W1 | W3 with the SwiGLU epilogue -> h [P + T][I]; the shared expert is the trailing dense
   // group of the same launch (on the K3 path with its own reduction length d, since it reads the
   // full-width x while the routed experts read the latent)
-  const bool fuse_shared = c->n_shared && (x.pl.tc || !x.pl.latent);
+  const bool fuse_shared = c->n_shared && !x.shared_done && (x.pl.tc || !x.pl.latent);
   void* y_sh = static_cast<uint8_t*>(y_perm) + (size_t)P * de * (x.pl.y_bf16 ? 2 : 4);
   {
     GroupedGemm g;
@@ -728,6 +737,67 @@ static moe_status_t run_experts(Ctx& x, const void* xin, const int32_t* offsets,
     g.n128 = (c->flags & MOE_FLAG_GEMM_N128) != 0;
     g.pair = (c->flags & MOE_FLAG_GEMM_PAIR) && !g.n128;
     e = gemm(x, g, "gemm2_rows", "gemm2_swap", "gemm2_swap256", "gemm2_simt");
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  return MOE_OK;
+}
+
+// The shared expert of tokens [t0, t0 + nt) in two launches of its own: dense groups of the
+// token-rows expert GEMMs, with the tiles and K order it has as the trailing group of the routed
+// launches, so its rows come out bit for bit the same.  h rows P + t0 .., then its expert-output
+// rows (K2: rows P + t0 .. of y_perm; K3: rows t0 .. of the full-width region after y_perm).
+static moe_status_t run_shared_rows(Ctx& x, const void* xin, const void* Ws13, const void* Ws2,
+                                    int64_t t0, int64_t nt) {
+  const moe_config_t* c = x.c;
+  const int64_t T = c->T, P = T * c->k;
+  const int de = x.pl.de, I = c->I, d = c->d;
+  void* h = at<void>(x.ws, x.L.h);
+  uint8_t* y_perm = at<uint8_t>(x.ws, x.L.y_perm);
+  const size_t yb = x.pl.y_bf16 ? 2 : 4;
+  cudaError_t e;
+  {
+    GroupedGemm g;
+    g.act_d = xin;
+    g.act_d_rows = T;
+    g.dense_act_row0 = (int)t0;
+    g.w_d = Ws13;
+    g.w_d_rows = 2 * I;
+    g.dense_rows = (int)nt;
+    g.dense_out_row0 = (int)(P + t0);
+    g.u_off_d = I;
+    g.K = d;
+    g.k_wrap = d;
+    g.F = I;
+    g.epi = EPI_SWIGLU;
+    g.act_dtype = g.w_dtype = c->act_dtype;
+    g.out = h;
+    g.ldo = I;
+    g.out_dtype = c->act_dtype;
+    g.err = x.err;
+    g.label = "shared_gemm13_swiglu_rows";
+    e = launch_gemm_tc(g, 0, x.sms, x.st);
+    if (e != cudaSuccess) return from_cuda(e);
+  }
+  {
+    GroupedGemm g;
+    g.act_d = h;
+    g.act_d_rows = P + T;
+    g.dense_act_row0 = (int)(P + t0);
+    g.w_d = Ws2;
+    g.w_d_rows = d;
+    g.dense_rows = (int)nt;
+    g.K = I;
+    g.k_wrap = I;
+    g.F = d;
+    g.epi = EPI_STORE;
+    g.act_dtype = g.w_dtype = c->act_dtype;
+    g.out = y_perm + (x.pl.latent ? (size_t)P * de * yb : 0);
+    g.dense_out_row0 = (int)(x.pl.latent ? t0 : P + t0);
+    g.ldo = x.pl.latent ? d : de;
+    g.out_dtype = x.pl.y_bf16 ? MOE_BF16 : MOE_F32;
+    g.err = x.err;
+    g.label = "shared_gemm2_rows";
+    e = launch_gemm_tc(g, 0, x.sms, x.st);
     if (e != cudaSuccess) return from_cuda(e);
   }
   return MOE_OK;
@@ -901,7 +971,7 @@ static moe_status_t forward_impl(Ctx& c, const void* x, const float* W_r, const 
   for (const void* p : ptrs)
     if (p && !aligned16(p)) return MOE_ERR_INVALID_ARG;
   ready(c);
-  if (cudaMemsetAsync(c.err, 0, 256, c.st) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!c.shared_done && cudaMemsetAsync(c.err, 0, 256, c.st) != cudaSuccess) return MOE_ERR_CUDA;
   const Layout& L = c.L;
   int32_t* idx = at<int32_t>(ws, L.idx);
   float* wgt = at<float>(ws, L.weight);
@@ -1020,17 +1090,45 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
   // the copies start after the work already queued on the caller's stream (the workspace may
   // still be in use there), and the layer starts after the input copies
   if (cudaEventRecord(io.ev_start, c.st) != cudaSuccess) return MOE_ERR_CUDA;
-  const size_t piece = (bytes / kIoStreams + 255) & ~size_t(255);
-  for (int i = 0; i < kIoStreams; ++i) {
-    const size_t o = (size_t)i * piece;
-    if (o >= bytes) break;
-    const size_t n = bytes - o < piece ? bytes - o : piece;
-    if (cudaStreamWaitEvent(io.cs[i], io.ev_start, 0) != cudaSuccess ||
-        cudaMemcpyAsync(static_cast<uint8_t*>(x_dev) + o, static_cast<const uint8_t*>(x_host) + o,
-                        n, cudaMemcpyHostToDevice, io.cs[i]) != cudaSuccess ||
-        cudaEventRecord(io.ev_in[i], io.cs[i]) != cudaSuccess ||
-        cudaStreamWaitEvent(c.st, io.ev_in[i], 0) != cudaSuccess)
-      return MOE_ERR_CUDA;
+  // the shared expert chunk by chunk: bf16 token-rows layers in the default tile shapes (the
+  // shared rows then equal those of the fused launches bit for bit)
+  const bool pipe = c.pl.tc && !c.pl.fp8 && !c.pl.w4 && c.pl.swap == 0 && cfg->n_shared &&
+                    Ws13 && Ws2 && aligned16(Ws13) && aligned16(Ws2) &&
+                    !(cfg->flags & (MOE_FLAG_GEMM_PAIR | MOE_FLAG_GEMM_M2 | MOE_FLAG_GEMM_N128 |
+                                    MOE_FLAG_TEST_STALL_EXPERTS));
+  if (pipe) {
+    if (cudaMemsetAsync(c.err, 0, 256, c.st) != cudaSuccess) return MOE_ERR_CUDA;
+    const int64_t T = cfg->T;
+    int64_t chunk = ((T + kIoChunks - 1) / kIoChunks + 127) / 128 * 128;
+    if (chunk < kIoMinChunkTokens) chunk = kIoMinChunkTokens;
+    const size_t row = (size_t)cfg->d * dtype_bytes(cfg->act_dtype);
+    for (int i = 0; i * chunk < T; ++i) {
+      const int64_t t0 = i * chunk, nt = T - t0 < chunk ? T - t0 : chunk;
+      cudaStream_t cs = io.cs[i % kIoStreams];
+      if (cudaStreamWaitEvent(cs, io.ev_start, 0) != cudaSuccess ||
+          cudaMemcpyAsync(static_cast<uint8_t*>(x_dev) + (size_t)t0 * row,
+                          static_cast<const uint8_t*>(x_host) + (size_t)t0 * row,
+                          (size_t)nt * row, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
+          cudaEventRecord(io.ev_in_chunk[i], cs) != cudaSuccess ||
+          cudaStreamWaitEvent(c.st, io.ev_in_chunk[i], 0) != cudaSuccess)
+        return MOE_ERR_CUDA;
+      if ((s = run_shared_rows(c, x_dev, Ws13, Ws2, t0, nt)) != MOE_OK) return s;
+    }
+    c.shared_done = true;
+  } else {
+    const size_t piece = (bytes / kIoStreams + 255) & ~size_t(255);
+    for (int i = 0; i < kIoStreams; ++i) {
+      const size_t o = (size_t)i * piece;
+      if (o >= bytes) break;
+      const size_t n = bytes - o < piece ? bytes - o : piece;
+      if (cudaStreamWaitEvent(io.cs[i], io.ev_start, 0) != cudaSuccess ||
+          cudaMemcpyAsync(static_cast<uint8_t*>(x_dev) + o,
+                          static_cast<const uint8_t*>(x_host) + o, n, cudaMemcpyHostToDevice,
+                          io.cs[i]) != cudaSuccess ||
+          cudaEventRecord(io.ev_in[i], io.cs[i]) != cudaSuccess ||
+          cudaStreamWaitEvent(c.st, io.ev_in[i], 0) != cudaSuccess)
+        return MOE_ERR_CUDA;
+    }
   }
   OutCopy oc;
   oc.host = out_host;

@@ -468,10 +468,12 @@ def test_host_io_entry_point_matches_device_path(cuda_device):
 
 @pytest.mark.parametrize("latent", [False, True], ids=["k2", "k3_latent"])
 def test_host_io_overlapped_copies_match_device_path(cuda_device, latent):
-    """Inputs of 32 MB and more take the overlapped host-I/O path: the input in two pieces on two
-    copy streams, the combine (K3: latent combine and up-projection) in eight token chunks, each
-    copied out behind its part.  The output must equal moe_forward's bit for bit, with a ragged
-    last chunk (3001 tokens)."""
+    """Inputs of 32 MB and more take the overlapped host-I/O path: the input in token chunks of
+    2048 on two copy streams, each chunk's shared-expert rows computed in launches of their own
+    while the next chunk arrives, then the routed experts without the shared expert, and the
+    combine (K3: latent combine and up-projection) in eight token chunks, each copied out behind
+    its part.  The output must equal moe_forward's (shared expert inside the routed launches) bit
+    for bit, with ragged last chunks (3001 tokens)."""
     base = S.WORKLOADS["k3_latent_bf16" if latent else "k2_prefill_bf16"]
     w = replace(base, name="host_io_large", E=32, T=3001)
     layer = _layer(w, seed=21)
