@@ -1147,9 +1147,6 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
   return from_cuda(cudaStreamSynchronize(c.st));
 }
 
-// The dense SwiGLU MLP: one dense group through the expert GEMMs (W1|W3 + SwiGLU -> h in the
-// workspace, then W2 straight into `out`): token-rows tensor-core tiles for bf16, CUDA cores for
-// fp32.
 // K ranges of the W2 launch: with few tokens its d / 256 output tiles leave most SMs idle, so
 // each tile is computed as partial sums over consecutive K ranges (fp32 partials, then one sum
 // kernel), as many as one wave of CTAs on 152 SMs holds, at most 8.  1: no split.
@@ -1162,6 +1159,9 @@ static int dense_w2_splits(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtyp
   return s >= 2 ? (int)s : 1;
 }
 
+// The dense SwiGLU MLP: one dense group through the expert GEMMs (W1|W3 + SwiGLU -> h in the
+// workspace, then W2 straight into `out`, or through fp32 partials over K ranges): token-rows
+// tensor-core tiles for bf16, CUDA cores for fp32.
 size_t moe_dense_mlp_workspace_size(int64_t T, int32_t d, int32_t I, moe_dtype_t act_dtype) {
   if (T < 0 || d <= 0 || I <= 0 || (act_dtype != MOE_BF16 && act_dtype != MOE_F32)) return 0;
   const int splits = dense_w2_splits(T, d, I, act_dtype);
