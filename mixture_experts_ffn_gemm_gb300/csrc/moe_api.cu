@@ -1102,7 +1102,7 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
     int64_t chunk = ((T + kIoChunks - 1) / kIoChunks + 127) / 128 * 128;
     if (chunk < kIoMinChunkTokens) chunk = kIoMinChunkTokens;
     const size_t row = (size_t)cfg->d * dtype_bytes(cfg->act_dtype);
-    for (int i = 0; i * chunk < T; ++i) {
+    for (int i = 0; i * chunk < T && s == MOE_OK; ++i) {
       const int64_t t0 = i * chunk, nt = T - t0 < chunk ? T - t0 : chunk;
       cudaStream_t cs = io.cs[i % kIoStreams];
       if (cudaStreamWaitEvent(cs, io.ev_start, 0) != cudaSuccess ||
@@ -1111,8 +1111,9 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
                           (size_t)nt * row, cudaMemcpyHostToDevice, cs) != cudaSuccess ||
           cudaEventRecord(io.ev_in_chunk[i], cs) != cudaSuccess ||
           cudaStreamWaitEvent(c.st, io.ev_in_chunk[i], 0) != cudaSuccess)
-        return MOE_ERR_CUDA;
-      if ((s = run_shared_rows(c, x_dev, Ws13, Ws2, t0, nt)) != MOE_OK) return s;
+        s = MOE_ERR_CUDA;
+      else
+        s = run_shared_rows(c, x_dev, Ws13, Ws2, t0, nt);
     }
     c.shared_done = true;
   } else {
@@ -1126,8 +1127,10 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
                           static_cast<const uint8_t*>(x_host) + o, n, cudaMemcpyHostToDevice,
                           io.cs[i]) != cudaSuccess ||
           cudaEventRecord(io.ev_in[i], io.cs[i]) != cudaSuccess ||
-          cudaStreamWaitEvent(c.st, io.ev_in[i], 0) != cudaSuccess)
-        return MOE_ERR_CUDA;
+          cudaStreamWaitEvent(c.st, io.ev_in[i], 0) != cudaSuccess) {
+        s = MOE_ERR_CUDA;
+        break;
+      }
     }
   }
   OutCopy oc;
@@ -1135,9 +1138,11 @@ moe_status_t moe_forward_host_io(const moe_config_t* cfg, const void* x_host, co
   oc.n = kIoChunks;
   for (int i = 0; i < kIoStreams; ++i) oc.cs[i] = io.cs[i];
   for (int i = 0; i < kIoChunks; ++i) oc.ev[i] = io.ev_chunk[i];
-  s = forward_impl(c, x_dev, W_r, b, W13, W2, W13_scale, W2_scale, Ws13, Ws2, Ws13_scale,
-                   Ws2_scale, W_down, W_up, out_dev, &oc);
-  // whatever was queued on the copy streams finishes before the caller's stream goes on
+  if (s == MOE_OK)
+    s = forward_impl(c, x_dev, W_r, b, W13, W2, W13_scale, W2_scale, Ws13, Ws2, Ws13_scale,
+                     Ws2_scale, W_down, W_up, out_dev, &oc);
+  // whatever was queued on the copy streams (also after a failure above) finishes before the
+  // caller's stream goes on
   for (int i = 0; i < kIoStreams; ++i) {
     if (cudaEventRecord(io.ev_out[i], io.cs[i]) != cudaSuccess ||
         cudaStreamWaitEvent(c.st, io.ev_out[i], 0) != cudaSuccess)

@@ -466,18 +466,21 @@ def test_host_io_entry_point_matches_device_path(cuda_device):
     assert torch.equal(out_host, out_dev.cpu())
 
 
-@pytest.mark.parametrize("latent", [False, True], ids=["k2", "k3_latent"])
-def test_host_io_overlapped_copies_match_device_path(cuda_device, latent):
+@pytest.mark.parametrize("latent,flags", [(False, 0), (True, 0), (False, B.MOE_FLAG_EXPERT_OUT_BF16),
+                                          (False, B.MOE_FLAG_GEMM_N128)],
+                         ids=["k2", "k3_latent", "k2_bf16_outputs", "k2_two_pieces"])
+def test_host_io_overlapped_copies_match_device_path(cuda_device, latent, flags):
     """Inputs of 32 MB and more take the overlapped host-I/O path: the input in token chunks of
     2048 on two copy streams, each chunk's shared-expert rows computed in launches of their own
     while the next chunk arrives, then the routed experts without the shared expert, and the
     combine (K3: latent combine and up-projection) in eight token chunks, each copied out behind
     its part.  The output must equal moe_forward's (shared expert inside the routed launches) bit
-    for bit, with ragged last chunks (3001 tokens)."""
+    for bit, with ragged last chunks (3001 tokens); also with bf16 expert outputs, and with the
+    128-column W2 tiles, under which x arrives in two pieces instead (no shared-expert chunks)."""
     base = S.WORKLOADS["k3_latent_bf16" if latent else "k2_prefill_bf16"]
     w = replace(base, name="host_io_large", E=32, T=3001)
     layer = _layer(w, seed=21)
-    cfg = B.config_for(w)
+    cfg = B.config_for(w, flags=flags)
     ws = B.alloc_workspace(cfg)
     assert w.T * w.d * 2 >= 32 << 20
     out_dev = torch.empty(w.T, w.d, dtype=torch.bfloat16, device="cuda")
