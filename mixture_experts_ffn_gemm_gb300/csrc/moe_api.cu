@@ -85,7 +85,7 @@ struct Plan {
   int de;             // expert width: d or d_latent
   bool router_tc;     // tensor-core router (3 x bf16 split weights)
   bool router_splitk; // tensor-core router for small batches, split over K (weights split inside)
-  int router_splits;  // split-K slices of the CUDA-core or split-K tensor-core router
+  int router_splits;  // K slices of the router GEMM (partial logits the selection adds in order)
   int swap;           // expert GEMM tiles: 0 token rows as M; 1 weight rows as M with 32-token
                       // tiles; 2 the same with 256-token tiles
   bool tc;            // tensor-core expert GEMMs
@@ -164,6 +164,14 @@ static Plan make_plan(const moe_config_t* c) {
   else
     p.router_tc = tc_ok && c->T >= 1024;
   p.router_splits = 1;
+  if (p.router_tc) {
+    // few 128-token row tiles (one CTA each, all experts in one N = 384 tile) leave SMs idle: the
+    // 3 * d reduction is split into as many K ranges as one wave of 152 CTAs holds (at most 8),
+    // whose fp32 partial logits the selection kernel adds in range order
+    const int64_t tiles = (c->T + 127) / 128;
+    const int64_t s = tiles > 0 ? 152 / tiles : 1;
+    p.router_splits = s < 1 ? 1 : s > 8 ? 8 : (int)s;
+  }
   // small bf16 batches: the split-K tensor-core router, slices for one wave of CTAs on 152 SMs
   p.router_splitk = !p.router_tc && !(c->flags & MOE_FLAG_ROUTER_SIMT) &&
                     c->act_dtype == MOE_BF16 && router_splitk_tc_supported(c->T, c->E, c->d);
@@ -365,7 +373,8 @@ static moe_status_t run_router(Ctx& x, const void* xin, const float* W_r, const 
     __nv_bfloat16* ws_split = at<__nv_bfloat16>(x.ws, x.L.wsplit);
     e = launch_split_router_weights(W_r, c->E, c->d, ws_split, x.st);
     if (e != cudaSuccess) return from_cuda(e);
-    float* z = logits ? logits : at<float>(x.ws, x.L.zbuf);
+    const int S = x.pl.router_splits;
+    float* z = (S == 1 && logits) ? logits : at<float>(x.ws, x.L.zbuf);
     GroupedGemm g;
     g.act_d = xin;
     g.act_d_rows = c->T;
@@ -379,12 +388,14 @@ static moe_status_t run_router(Ctx& x, const void* xin, const float* W_r, const 
     g.out = z;
     g.ldo = c->E;
     g.out_dtype = MOE_F32;
+    g.k_splits = S;
+    g.split_stride = c->T * c->E;
     g.err = x.err;
     g.label = "router_gemm_tc";
     e = launch_gemm_tc(g, 0, x.sms, x.st);
     if (e != cudaSuccess) return from_cuda(e);
-    e = launch_router_topk(z, 1, 0, c->T, c->E, c->k, b, c->gate_scale, nullptr, idx, weight,
-                           x.st);
+    e = launch_router_topk(z, S, c->T * c->E, c->T, c->E, c->k, b, c->gate_scale,
+                           S == 1 ? nullptr : logits, idx, weight, x.st);
     return from_cuda(e);
   }
   float* zp = at<float>(x.ws, x.L.zbuf);
